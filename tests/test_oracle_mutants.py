@@ -1,0 +1,79 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (on the CPU, in
+a temporary directory), builds it, points the oracle front end at the mutant
+and runs the pins; at least one pin must fail for every mutant.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+from oracle import oracle as orc
+from oracle import build as obuild
+from tests import test_oracle_pins as pins
+
+MUTANTS = {
+    "test-uses-previous-max": ("real diff = mt[i] - mnew[i];", "real diff = mt[i] - m[i];"),
+    "margin-sign-flipped": ("real diff = mt[i] - mnew[i];", "real diff = mnew[i] - mt[i];"),
+    "no-rescale-of-O": ("for (int x = 0; x < d; ++x) Oi[x] *= alpha;", ""),
+    "no-rescale-of-l": ("l[i] = alpha * l[i] + rowsum;", "l[i] = l[i] + rowsum;"),
+    "causal-top-left": ("return c <= r + (Lkv - Lq);", "return c <= r;"),
+    "gqa-head-modulo": ("long hk = h / G;\n            for (int i = 0; i < n; ++i) {",
+                        "long hk = h % Hkv;\n            for (int i = 0; i < n; ++i) {"),
+    "any-row-instead-of-all": ("if (!vote) skip = 0;", "if (vote && i == 0) skip = 1; else if (!vote && i == 0) skip = 0;"),
+    "skip-keeps-contribution": ("if (skip) {\n            ++skipped;", "if (0) {\n            ++skipped;"),
+    "lse-missing-max": ("m[i] = m[i] + R_LOG(l[i]);", "m[i] = R_LOG(l[i]);"),
+    "split-bounds-truncated": ("int t0 = (int)(((long)s * nK) / S), t1 = (int)(((long)(s + 1) * nK) / S);",
+                               "int t0 = s * (nK / S), t1 = (s == S - 1) ? nK : (s + 1) * (nK / S);"),
+    "transposed-score-index": ("sv = score(a->qrow[i], a->kb + c * d, d, a->scale);",
+                               "sv = score(a->qrow[i], a->kb + (c0 + (Bc - 1 - cc < a->Lkv - c0 ? Bc - 1 - cc : cc)) * d, d, a->scale);"),
+}
+
+PINS = [
+    lambda: pins.test_dense_matches_textbook_matmul(True, (2, 4, 2, 20, 29, 16)),
+    lambda: pins.test_tiled_matches_brute_force_tiny((2, 4), True),
+    lambda: pins.test_tiled_lambda0_equals_dense_small(2, 4),
+    lambda: pins.test_skip_set_equals_closed_form(True),
+    lambda: pins.test_skip_set_closed_form_small_tiles_gqa(),
+    lambda: pins.test_masked_dense_identity(),
+    lambda: pins.test_decode_skip_set_closed_form_and_split_merge(),
+    lambda: pins.test_skipped_contribution_closed_form(0.1),
+]
+
+
+def _build_mutant(tmp, name, old, new):
+    src = open(obuild.SRC).read()
+    assert old in src, f"mutation anchor for {name} not found"
+    path_c = os.path.join(tmp, f"{name}.c")
+    open(path_c, "w").write(src.replace(old, new, 1))
+    objs = []
+    for real, suf in (("float", "_f32"), ("double", "_f64")):
+        o = os.path.join(tmp, f"{name}{suf}.o")
+        subprocess.run(["gcc", "-O1", "-fPIC", "-fopenmp", "-std=c11", "-ffp-contract=off",
+                        f"-DREAL={real}", f"-DSUFFIX={suf}", "-c", path_c, "-o", o], check=True)
+        objs.append(o)
+    so = os.path.join(tmp, f"lib{name}.so")
+    subprocess.run(["gcc", "-shared", "-fopenmp", "-o", so, *objs, "-lm"], check=True)
+    return so
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    so = _build_mutant(str(tmp_path), name, old, new)
+    saved = orc._lib
+    orc._lib = orc._configure(ctypes.CDLL(so))
+    caught = []
+    try:
+        for pin in PINS:
+            try:
+                pin()
+            except (AssertionError, ValueError, IndexError):
+                caught.append(pin)
+    finally:
+        orc._lib = saved
+    assert caught, f"no pin caught the planted mistake '{name}'"
