@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the skip-softmax (BLASST) attention forward on one GB300.
+
+A step is one pass of the whole path over one batch of synthetic input:
+  1. threshold resolution (blasst_lambda, lambda = a / Lkv),
+  2. causal GQA prefill, B=1, Hq=32, Hkv=8, L=16384, d=128 (blasst_prefill),
+  3. split-KV decode, B=64, Hq=32, Hkv=8, Lkv=32768, d=128 (blasst_decode: split
+     pass + merge).
+`value` is the prefill's dense-equivalent TFLOP/s (standard causal attention FLOP
+divided by the prefill kernel's CUDA-event time); the decode's KV GB/s and both
+tile-skip fractions are reported beside it.  An L2-sized buffer is rewritten
+between timed steps.
+
+`--impl reference` times the CPU oracle instead (on bounded samples of the same
+prefill workload) and prints the same JSON line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "skip-softmax attn TFLOP/s (dense-equiv) + tile-skip %; decode KV GB/s on GB300"
+UNIT = "TFLOP/s"
+PREFILL = dict(B=1, Hq=32, Hkv=8, L=16384, d=128)
+DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
+# Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
+# capture of the current kernels; None until captured for this version of the kernels.
+TRAFFIC_BYTES = {"prefill": None, "decode": None}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                "bf16_tflops_sustained": pk.get("bf16_tflops_sustained"), "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def causal_pairs(Lq, Lkv):
+    """Number of (row, key) pairs visible under bottom-right causal masking."""
+    off = Lkv - Lq
+    tot = 0
+    # rows r see min(Lkv, max(0, r + off + 1)) keys
+    lo = max(0, -off)
+    hi_full = max(lo, min(Lq, Lkv - off))  # rows that see fewer than Lkv keys end here
+    for_rows = range(lo, hi_full)
+    if for_rows:
+        a, b = for_rows.start + off + 1, for_rows.stop - 1 + off + 1
+        tot += (a + b) * (b - a + 1) // 2
+    tot += max(0, Lq - hi_full) * Lkv
+    return tot
+
+
+def visited_tiles_causal(Lq, Lkv, T=128):
+    nQ, nK = -(-Lq // T), -(-Lkv // T)
+    off = Lkv - Lq
+    tot = 0
+    for qt in range(nQ):
+        last = min(Lq, (qt + 1) * T) - 1 + off
+        tot += 0 if last < 0 else min(nK, last // T + 1)
+    return tot
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"blasst_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------- helpers
+def dist_setup(args):
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+def max_over_ranks(pg, x):
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, x):
+    if pg is None:
+        return x
+    import torch
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+def oracle_sample(a, units_by_head, lam):
+    """Run the fp32 oracle on (h, [qtiles]) units of a prefill problem; returns
+    (dense-equivalent FLOP of the sample, seconds)."""
+    from oracle import oracle as orc
+
+    G = a.Hq // a.Hkv
+    flop = 0
+    secs = 0.0
+    for h, tiles in units_by_head:
+        q = a.q[0:1, h:h + 1].float().cpu()
+        k = a.k[0:1, h // G:h // G + 1].float().cpu()
+        v = a.v[0:1, h // G:h // G + 1].float().cpu()
+        t0 = time.perf_counter()
+        orc.prefill_tiled(q, k, v, a.causal, a.scale, lam, units=[(0, 0, t) for t in tiles], precision="f32")
+        secs += time.perf_counter() - t0
+        for t in tiles:
+            r0, r1 = t * 128, min(a.Lq, (t + 1) * 128)
+            pairs = sum(min(a.Lkv, r + 1 + a.Lkv - a.Lq) for r in range(r0, r1)) if a.causal else (r1 - r0) * a.Lkv
+            flop += 4 * a.d * pairs
+    return flop, secs
+
+
+def random_units(rng, H, nQ, n):
+    """One random head and n random query tiles of it (one oracle call, so the
+    oracle's OpenMP loop spreads the tiles over the cores)."""
+    return [(int(rng.integers(H)), sorted(int(t) for t in rng.integers(nQ, size=n)))]
+
+
+# ----------------------------------------------------------------- reference arm
+def run_reference(args):
+    world, rank, local, pg = dist_setup(args)
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    from oracle import oracle as orc
+    from skip_softmax_flashattention_gb300 import workloads as W
+
+    L = PREFILL["L"]
+    a = W.llm(seed=0, L=L, device="cpu")
+    lam = args.lam_a / L
+    nQ = L // 128
+    rng = np.random.default_rng(1234)
+    per_step_units = max(1, args.ref_units)
+    for _ in range(args.warmup):
+        oracle_sample(a, random_units(rng, a.Hq, nQ, 1), lam)
+    flops, secs = 0, 0.0
+    for _ in range(args.steps):
+        f, s = oracle_sample(a, random_units(rng, a.Hq, nQ, per_step_units), lam)
+        flops += f
+        secs += s
+    value = flops / secs / 1e12
+    cores = orc.num_threads()
+    sample = (f"{args.steps} steps x {per_step_units} random (head, 128-row query tile) units of the causal "
+              f"L=16384 GQA prefill, full key rows, lambda={lam:.3g}")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "llm-prefill-causal-gqa B=1 Hq=32 Hkv=8 L=16384 d=128", "lambda": lam,
+                       "l2": "not applicable (CPU)"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    world, rank, local, pg = dist_setup(args)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from skip_softmax_flashattention_gb300 import blasst as K
+    from skip_softmax_flashattention_gb300 import workloads as W
+
+    K.load()
+    peaks = load_peaks()
+    P, Dd = PREFILL, DECODE
+    L = P["L"]
+    a = W.llm(seed=0, L=L, device=dev)
+    dcfg = W.decode(seed=0, device=dev)
+    stream = torch.cuda.current_stream()
+
+    # outputs and workspace, allocated once
+    o = torch.empty_like(a.q)
+    lse = torch.empty(P["B"], P["Hq"], L, device=dev, dtype=torch.float32)
+    skipped_p = torch.zeros(1, device=dev, dtype=torch.int64)
+    rc, S = K.blasst_decode_num_splits(Dd["B"], Dd["Hq"], Dd["Hkv"], Dd["Lkv"], Dd["d"], 0)
+    assert rc == 0
+    ws_bytes = K.blasst_decode_workspace_size(Dd["B"], Dd["Hq"], Dd["Hkv"], Dd["Lkv"], Dd["d"], S)
+    ws = torch.empty(max(16, ws_bytes), device=dev, dtype=torch.uint8)
+    od = torch.empty(Dd["B"], Dd["Hq"], Dd["d"], device=dev, dtype=torch.bfloat16)
+    lsed = torch.empty(Dd["B"], Dd["Hq"], device=dev, dtype=torch.float32)
+    skipped_d = torch.zeros(1, device=dev, dtype=torch.int64)
+    flush = W.l2_flush_buffer(dev)
+    q3 = dcfg.q.reshape(Dd["B"], Dd["Hq"], Dd["d"])
+
+    def lam_for(Lkv):
+        rc, lam = K.blasst_lambda(0 if args.threshold is not None else 1, threshold=args.threshold or 0.0,
+                                  a=args.lam_a, b=0.0, target_sparsity=0.0, Lkv=Lkv)
+        if rc < 0:
+            raise K.BlasstError(rc, "blasst_lambda")
+        return lam
+
+    def prefill(lam):
+        return K.blasst_prefill(a.q, a.k, a.v, o, lse, P["B"], P["Hq"], P["Hkv"], L, L, P["d"], 1, a.scale, lam,
+                                skipped_p, stream)
+
+    def decode(lam):
+        return K.blasst_decode(q3, dcfg.k, dcfg.v, od, lsed, Dd["B"], Dd["Hq"], Dd["Hkv"], Dd["Lkv"], Dd["d"],
+                               dcfg.scale, lam, S, ws, ws_bytes, skipped_d, None, None, stream)
+
+    launches_per_step = 2 + (1 if S > 1 else 0)
+
+    def run_steps(n, lam_fn_p, lam_fn_d, timed):
+        evs = []
+        for _ in range(n):
+            flush.zero_()
+            e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            e[0].record(stream)
+            lp = lam_fn_p()
+            ld = lam_fn_d()
+            assert prefill(lp) == 0
+            e[1].record(stream)
+            assert decode(ld) == 0
+            e[2].record(stream)
+            e[3].record(stream)
+            evs.append(e)
+        return evs
+
+    lam_p = lambda: lam_for(L)  # noqa: E731
+    lam_d = lambda: lam_for(Dd["Lkv"])  # noqa: E731
+
+    # warm-up
+    run_steps(args.warmup, lam_p, lam_d, False)
+    torch.cuda.synchronize()
+    K.blasst_device_status(1)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier(pg)
+    torch.cuda.synchronize()
+    t_wall0 = time.perf_counter()
+    evs = run_steps(args.steps, lam_p, lam_d, True)
+    torch.cuda.synchronize()
+    barrier(pg)
+    t_wall = time.perf_counter() - t_wall0
+    clk = clocks.stop()
+    st = K.blasst_device_status(1)
+    if st != 0:
+        raise K.BlasstError(st, "device status after the timed region")
+
+    p_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    d_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    n_skip_p = int(skipped_p.item())
+    n_skip_d = int(skipped_d.item())
+
+    lam_prefill, lam_decode = lam_p(), lam_d()
+    pairs = causal_pairs(L, L)
+    dense_flop = 4.0 * P["B"] * P["Hq"] * P["d"] * pairs
+    visited = visited_tiles_causal(L, L) * P["B"] * P["Hq"]
+    exec_flop = 2.0 * 128 * 128 * P["d"] * (2 * visited - n_skip_p)
+    p_mean = sum(p_ms) / len(p_ms)
+    d_mean = sum(d_ms) / len(d_ms)
+    p_max = max_over_ranks(pg, p_mean)
+    d_max = max_over_ranks(pg, d_mean)
+    value = sum_over_ranks(pg, dense_flop / (p_max * 1e-3) / 1e12)
+
+    nT = Dd["Lkv"] // 128
+    tiles_d = Dd["B"] * Dd["Hkv"] * nT
+    tile_bytes = 128 * Dd["d"] * 2
+    kv_bytes = tile_bytes * (2 * tiles_d - n_skip_d)
+    other_bytes = (Dd["B"] * Dd["Hq"] * Dd["d"] * 2 * 2 + Dd["B"] * Dd["Hq"] * 4
+                   + (2 * S * Dd["B"] * Dd["Hq"] * (Dd["d"] + 1) * 4 if S > 1 else 0))
+    dec_gbs = (kv_bytes + other_bytes) / (d_max * 1e-3) / 1e9
+    dec_dense_gbs = (tile_bytes * 2 * tiles_d) / (d_max * 1e-3) / 1e9
+
+    # ---- end to end through the C ABI with host buffers (prefill, the headline metric)
+    qh = a.q.cpu().pin_memory()
+    kh = a.k.cpu().pin_memory()
+    vh = a.v.cpu().pin_memory()
+    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lseh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    qd, kd, vd = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        rc = K.blasst_prefill(qd, kd, vd, o, lse, P["B"], P["Hq"], P["Hkv"], L, L, P["d"], 1, a.scale, lam_p(),
+                              skipped_p, stream)
+        assert rc == 0
+        oh.copy_(o, non_blocking=True)
+        lseh.copy_(lse, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_s.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(pg, e_s.elapsed_time(e_e) / args.steps)
+    e2e_value = sum_over_ranks(pg, dense_flop / (e2e_ms * 1e-3) / 1e12)
+    h2d = qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2
+    d2h = oh.numel() * 2 + lseh.numel() * 4
+
+    # ---- CPU baseline: the oracle on a bounded sample of the same prefill workload
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rng = np.random.default_rng(7)
+        flops, secs, n_units = 0, 0.0, 0
+        while secs < args.cpu_seconds and n_units < 512:
+            f, s_ = oracle_sample(a, random_units(rng, a.Hq, L // 128, 16), lam_prefill)
+            flops += f
+            secs += s_
+            n_units += 16
+        from oracle import oracle as orc
+
+        cpu = {"value": flops / secs / 1e12, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+               "sample": f"{n_units} random (head, query-tile) units of the same prefill, full key rows, "
+                         f"{secs:.1f} s of fp32 oracle time"}
+
+    ach = exec_flop / (p_max * 1e-3) / 1e12
+    roof = {"bound": "tensor", "kernel": "prefill_kernel<128,P-in-TMEM>", "achieved": ach,
+            "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
+            "peak_source": peaks["source"] + " burst bf16",
+            "traffic": TRAFFIC_BYTES["prefill"]}
+    roof_d = {"bound": "hbm", "kernel": "decode_kernel<4> + combine", "achieved": dec_gbs,
+              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
+              "peak_source": peaks["source"] + " HBM copy", "traffic": TRAFFIC_BYTES["decode"]}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": max_over_ranks(pg, sum(step_ms) / len(step_ms)),
+        "wall_ms_per_step": t_wall / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) with sink keys)",
+        "config": {"workload": "llm-prefill-causal-gqa B=1 Hq=32 Hkv=8 L=16384 d=128 + "
+                               "split-kv-decode B=64 Hq=32 Hkv=8 Lkv=32768 d=128",
+                   "lambda": {"prefill": lam_prefill, "decode": lam_decode,
+                              "rule": (f"threshold {args.threshold}" if args.threshold is not None
+                                       else f"a/Lkv, a={args.lam_a}")},
+                   "l2": "512 MB buffer rewritten between timed steps", "decode_splits": S,
+                   "parallelism": f"replicas x{world}"},
+        "prefill": {"ms": p_max, "dense_tflops": value / max(1, world), "executed_tflops": ach,
+                    "skipped_tiles": n_skip_p, "visited_tiles": visited, "skip_pct": 100.0 * n_skip_p / visited},
+        "decode": {"ms": d_max, "kv_gbs": dec_gbs, "dense_equiv_gbs": dec_dense_gbs,
+                   "frac_of_measured_hbm": dec_gbs / peaks["hbm_gbs"], "frac_of_8tbs": dec_gbs / 8000.0,
+                   "skipped_tiles": n_skip_d, "tiles": tiles_d, "skip_pct": 100.0 * n_skip_d / tiles_d,
+                   "splits": S},
+        "roofline": roof, "roofline_decode": roof_d,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--lam-a", type=float, default=40.0, help="lambda = a / Lkv (the LLM workloads' rule)")
+    ap.add_argument("--threshold", type=float, default=None, help="use lambda = threshold instead")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-units", type=int, default=16)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,156 @@
+/*
+ * blasst.h -- C ABI of the GB300 (sm_103a) skip-softmax FlashAttention library.
+ *
+ * The method (BLASST, "Dynamic BLocked Attention Sparsity via Softmax
+ * Thresholding"): in the streaming online-softmax pass over key tiles, a tile
+ * whose best score lies more than ln(lambda) below the running maximum in EVERY
+ * query row of the tile skips its exponentials, its row sums, its V load and its
+ * P.V product.  Definitions followed:
+ *   - online-softmax recurrence and tiling: Hitchhiker's Guide Phase 08,
+ *     Section 1 ("FlashAttention: IO-Optimal Attention", "FlashAttention Tiling
+ *     Strategy");
+ *   - the skip test m~ - m < ln(lambda), m the running max after the tile's own
+ *     update, required for every row: Skip-Softmax design doc, "Algorithm";
+ *     BLASST talk notes, "BLASST algorithm" (Eq. 2);
+ *   - lambda = threshold_scale_factor / max_kv_len with the two mutually
+ *     exclusive controls: Skip-Softmax design doc, "From configuration to the
+ *     kernel threshold";
+ *   - prefill skips softmax + PV, decode additionally skips the V load (loads K
+ *     tiles first, issues V only for tiles that pass): BLASST talk notes,
+ *     "kernel design: skip predicate reduction" (Figs. 3 and 4).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, row-major, bf16 (uint16 bit pattern), in DEVICE memory
+ *     owned by the caller, 16-byte aligned:
+ *         q [B, Hq, Lq, d]     k, v [B, Hkv, Lkv, d]     o [B, Hq, Lq, d]
+ *     (decode: q and o are [B, Hq, d]).  Query head h reads KV head h / (Hq/Hkv).
+ *   - lse is fp32 [B, Hq, Lq] (decode [B, Hq]): m + ln(l) in natural-log units of
+ *     the scaled scores; -inf for a row that sees no key (its o row is 0).
+ *   - scores are scale * (q . k); scale must be finite and > 0.
+ *   - lambda in [0, 1].  0 skips nothing.  Values above 1 are rejected: the test's
+ *     left side exp(m~ - m) never exceeds 1, so lambda > 1 would skip every tile
+ *     including the first and leave O/l undefined.
+ *   - Key/query tiles are 128 x 128.  Causal masking is bottom-right aligned:
+ *     key c is visible to query row r iff c <= r + (Lkv - Lq).
+ *   - Every call only enqueues work on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) after validating its arguments on the host; nothing is
+ *     synchronous.  The library allocates nothing and keeps no state except one
+ *     device status word per device (see blasst_device_status).
+ *   - Return value: BLASST_OK (0), a positive warning, or a negative error
+ *     code; no work is enqueued when an error is returned.
+ */
+#ifndef BLASST_H
+#define BLASST_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define BLASST_OK 0
+#define BLASST_WARN_LAMBDA_GE_1 1        /* blasst_lambda: curve gave lambda > 1 (value still returned) */
+#define BLASST_ERR_INVALID_ARG (-1)      /* null required pointer, bad size, lambda/scale out of range */
+#define BLASST_ERR_UNSUPPORTED (-2)      /* valid request this build does not run (d, G, alignment) */
+#define BLASST_ERR_WORKSPACE_TOO_SMALL (-3)
+#define BLASST_ERR_CUDA (-4)             /* a CUDA runtime/driver call failed */
+#define BLASST_ERR_TIMEOUT (-5)          /* a device-side wait ran past its limit (see blasst_device_status) */
+#define BLASST_ERR_NO_CALIBRATION (-6)   /* target-sparsity mode without finite coefficients a, b */
+
+/* flags for blasst_prefill_ex */
+#define BLASST_PREFILL_ELIDE_V 0x1u      /* also skip the V tile load of skipped tiles (not in this build: UNSUPPORTED) */
+#define BLASST_PREFILL_P_VIA_SMEM 0x2u   /* stage P in shared memory instead of tensor memory (results identical) */
+#define BLASST_FLAG_TEST_SHORT_WATCHDOG 0x80000000u /* test only: device waits give up after ~1 us */
+
+/*
+ * Prefill / non-causal self-attention forward.
+ *   q, k, v, o          see conventions; o is written for rows r < Lq only.
+ *   lse                 nullable fp32 [B, Hq, Lq].
+ *   B, Hq, Hkv          batch, query heads, KV heads (Hq % Hkv == 0).
+ *   Lq, Lkv             query / key lengths (>= 1).
+ *   d                   head dim: 64 or 128.
+ *   causal              0 or 1.
+ *   scale, lambda       see conventions.
+ *   skipped_tiles_out   nullable device uint64: set to the number of skipped
+ *                       (query tile, key tile) pairs over the whole call.
+ * The skip unit is 128 query rows of ONE query head x 128 keys.  Key tiles that no
+ * row of a query tile can see (causal) are not visited and not counted.
+ */
+int blasst_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                   int Lq, int Lkv, int d, int causal, float scale, float lambda,
+                   unsigned long long* skipped_tiles_out, void* stream);
+
+/*
+ * As blasst_prefill, plus:
+ *   skip_map   nullable device uint8 [B, Hq, ceil(Lq/128), ceil(Lkv/128)]:
+ *              0 = computed, 1 = skipped, 2 = not visited.
+ *   margins    nullable device fp32, same shape: max over the tile's rows of
+ *              (m~ - m) in scaled-score units (+inf when a row has no visible key
+ *              yet, NaN for tiles not visited).  lambda-independent for lambda <= 1;
+ *              a tile is skipped iff margin < ln(lambda).
+ *   flags      BLASST_PREFILL_P_VIA_SMEM, BLASST_FLAG_TEST_SHORT_WATCHDOG;
+ *              BLASST_PREFILL_ELIDE_V is reserved and returns BLASST_ERR_UNSUPPORTED.
+ */
+int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                      int Hkv, int Lq, int Lkv, int d, int causal, float scale, float lambda,
+                      unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                      unsigned flags, void* stream);
+
+/*
+ * Split-KV plan for decode.  Split s of S covers key tiles
+ * [floor(s*nT/S), floor((s+1)*nT/S)), nT = ceil(Lkv/128); each split is an
+ * independent pass (its running max starts at -inf), so S changes which tiles are
+ * skipped and is part of the result's definition.
+ *   requested  0 = choose automatically for this GPU, else 1 <= requested <= nT.
+ *   out        receives S.
+ */
+int blasst_decode_num_splits(int B, int Hq, int Hkv, int Lkv, int d, int requested, int* out);
+
+/* Workspace bytes blasst_decode needs for num_splits splits (0 when num_splits == 1). */
+size_t blasst_decode_workspace_size(int B, int Hq, int Hkv, int Lkv, int d, int num_splits);
+
+/*
+ * Decode forward: one query token per sequence against a KV cache.
+ *   q [B, Hq, d], k_cache/v_cache [B, Hkv, Lkv, d], o [B, Hq, d] bf16; lse nullable fp32 [B, Hq].
+ *   The skip unit is the G = Hq/Hkv query heads that read one KV head x 128 keys;
+ *   G must be <= 16.  V tiles of skipped key tiles are never loaded.
+ *   num_splits   S from blasst_decode_num_splits (explicit: the split plan is part
+ *                of the result).
+ *   workspace    device memory of at least blasst_decode_workspace_size() bytes,
+ *                16-byte aligned (may be NULL when S == 1).  Holds per-split
+ *                partial results; a second kernel merges them by log-sum-exp.
+ *   skipped_tiles_out  nullable device uint64 (count of skipped (b, hkv, tile)).
+ *   skip_map     nullable device uint8 [B, Hkv, nT] (0 computed, 1 skipped).
+ *   margins      nullable device fp32 [B, Hkv, nT] (as for prefill).
+ */
+int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
+                  int Hkv, int Lkv, int d, float scale, float lambda, int num_splits, void* workspace,
+                  size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
+                  float* margins, void* stream);
+
+/*
+ * Threshold resolution (Skip-Softmax design doc, "From configuration to the
+ * kernel threshold"; BLASST talk notes, "threshold calibration", Eq. 3):
+ *   mode 0 (threshold):        lambda = threshold           (any Lkv)
+ *   mode 1 (target sparsity):  lambda = a * exp(b * s) / Lkv
+ * Returns BLASST_ERR_INVALID_ARG for a bad mode, Lkv < 1, a negative or
+ * non-finite threshold, or s outside [0, 1]; BLASST_ERR_NO_CALIBRATION when mode 1
+ * is asked without finite a and b (use mode 0 instead); BLASST_WARN_LAMBDA_GE_1
+ * (with the raw value in *lambda_out) when the result exceeds 1.
+ */
+int blasst_lambda(int mode, double threshold, double a, double b, double target_sparsity, long long Lkv,
+                  double* lambda_out);
+
+/* Read (and with clear != 0, reset) this device's status word after synchronising
+ * the device.  Returns BLASST_OK, or BLASST_ERR_TIMEOUT if a kernel of this library
+ * gave up a wait since the last clear (its outputs are then invalid). */
+int blasst_device_status(int clear);
+
+/* Static English description of a status code. */
+const char* blasst_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* BLASST_H */

@@ -1,0 +1,314 @@
+// api.cu -- the C ABI declared in include/blasst.h: argument validation, the
+// threshold resolution, TMA descriptor encoding and kernel launches.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include "blasst.h"
+#include "kernels.cuh"
+
+// The library's one piece of device state: a sticky status word per device that a
+// kernel sets when one of its bounded waits gives up.
+__device__ int g_blasst_status = 0;
+
+namespace {
+
+using blasst::kTile;
+
+constexpr unsigned long long kWatchdogNs = 4000000000ull;  // 4 s per wait
+constexpr unsigned long long kShortWatchdogNs = 1000ull;   // test flag: 1 us
+constexpr int kMaxDevices = 64;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+int* status_word() {
+    static int* ptrs[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (!ptrs[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_blasst_status) != cudaSuccess) return nullptr;
+        ptrs[dev] = static_cast<int*>(p);
+    }
+    return ptrs[dev];
+}
+
+// [Z][L][d] bf16 viewed as a 3-D tensor (d fastest); boxes of 64 columns x 128 rows,
+// 128-byte swizzle, zero fill outside [0, L).
+bool encode_3d(CUtensorMap* map, const void* base, int d, int L, long long Z) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)L, (cuuint64_t)Z};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)L * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)kTile, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool lambda_ok(float lambda) { return std::isfinite(lambda) && lambda >= 0.f && lambda <= 1.f; }
+
+bool scale_ok(float scale) { return std::isfinite(scale) && scale > 0.f; }
+
+struct Thresholds {
+    float c_log2, thr_raw, lazy_raw;
+};
+
+// Convert (scale, lambda) into the kernels' raw-score units: a score s = scale*x,
+// the test m~ - m < ln(lambda) becomes x~ - x_m < ln(lambda)/scale.
+Thresholds thresholds(float scale, float lambda) {
+    const double log2e = 1.4426950408889634;
+    Thresholds t;
+    t.c_log2 = (float)((double)scale * log2e);
+    t.thr_raw = lambda > 0.f ? (float)(std::log((double)lambda) / (double)scale) : -INFINITY;
+    t.lazy_raw = (float)(8.0 / ((double)scale * log2e));
+    return t;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? BLASST_OK : BLASST_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int blasst_prefill(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                   int Lq, int Lkv, int d, int causal, float scale, float lambda,
+                   unsigned long long* skipped_tiles_out, void* stream) {
+    return blasst_prefill_ex(q, k, v, o, lse, B, Hq, Hkv, Lq, Lkv, d, causal, scale, lambda, skipped_tiles_out,
+                             nullptr, nullptr, 0u, stream);
+}
+
+int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                      int Hkv, int Lq, int Lkv, int d, int causal, float scale, float lambda,
+                      unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                      unsigned flags, void* stream) {
+    if (!q || !k || !v || !o) return BLASST_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lkv < 1 || Hq % Hkv != 0) return BLASST_ERR_INVALID_ARG;
+    if (causal != 0 && causal != 1) return BLASST_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || !lambda_ok(lambda)) return BLASST_ERR_INVALID_ARG;
+    const unsigned known = BLASST_PREFILL_ELIDE_V | BLASST_PREFILL_P_VIA_SMEM | BLASST_FLAG_TEST_SHORT_WATCHDOG;
+    if (flags & ~known) return BLASST_ERR_INVALID_ARG;
+    if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
+    if (flags & BLASST_PREFILL_ELIDE_V) return BLASST_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
+        (reinterpret_cast<uintptr_t>(skipped_tiles_out) & 7u))
+        return BLASST_ERR_UNSUPPORTED;
+    if (Hq > 65535 || B > 65535) return BLASST_ERR_UNSUPPORTED;
+    const long long nQ = (Lq + kTile - 1) / kTile, nK = (Lkv + kTile - 1) / kTile;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* status = status_word();
+    if (!status) return BLASST_ERR_CUDA;
+    CUtensorMap tq, tk, tv;
+    if (!encode_3d(&tq, q, d, Lq, (long long)B * Hq) || !encode_3d(&tk, k, d, Lkv, (long long)B * Hkv) ||
+        !encode_3d(&tv, v, d, Lkv, (long long)B * Hkv))
+        return BLASST_ERR_CUDA;
+
+    const long long map_n = (long long)B * Hq * nQ * nK;
+    if (skipped_tiles_out && cudaMemsetAsync(skipped_tiles_out, 0, sizeof(unsigned long long), st) != cudaSuccess)
+        return BLASST_ERR_CUDA;
+    if (skip_map && cudaMemsetAsync(skip_map, 2, (size_t)map_n, st) != cudaSuccess) return BLASST_ERR_CUDA;
+    if (margins && cudaMemsetAsync(margins, 0xFF, (size_t)map_n * sizeof(float), st) != cudaSuccess)
+        return BLASST_ERR_CUDA;
+
+    const Thresholds t = thresholds(scale, lambda);
+    blasst::PrefillParams p{};
+    p.o = o;
+    p.lse = lse;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Lq = Lq; p.Lkv = Lkv; p.causal = causal;
+    p.nQ = (int)nQ; p.nK = (int)nK;
+    p.c_log2 = t.c_log2;
+    p.scale = scale;
+    p.thr_raw = t.thr_raw;
+    p.lazy_raw = t.lazy_raw;
+    p.skipped = skipped_tiles_out;
+    p.skip_map = skip_map;
+    p.margins = margins;
+    p.status = status;
+    p.watchdog_ns = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? kShortWatchdogNs : kWatchdogNs;
+    p.elide_v = 0;
+    const bool p_in_tmem = (flags & BLASST_PREFILL_P_VIA_SMEM) == 0;
+    return cuda_status(blasst::launch_prefill(tq, tk, tv, p, d, p_in_tmem, st));
+}
+
+int blasst_decode_num_splits(int B, int Hq, int Hkv, int Lkv, int d, int requested, int* out) {
+    if (!out || B < 1 || Hq < 1 || Hkv < 1 || Lkv < 1 || d < 1 || Hq % Hkv != 0 || requested < 0)
+        return BLASST_ERR_INVALID_ARG;
+    const int nT = (Lkv + kTile - 1) / kTile;
+    if (requested > 0) {
+        if (requested > nT) return BLASST_ERR_INVALID_ARG;
+        *out = requested;
+        return BLASST_OK;
+    }
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return BLASST_ERR_CUDA;
+    // One decode CTA fits per SM.  Take the fewest splits whose CTA count fills the
+    // last wave to at least 90%; more splits restart the running max more often.
+    const long long units = (long long)B * Hkv;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int S = 1; S <= nT && S <= 64; ++S) {
+        const double waves = (double)(units * S) / sms;
+        const double eff = waves / std::ceil(waves);
+        if (eff >= 0.9) {
+            best = S;
+            best_eff = eff;
+            break;
+        }
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = S;
+        }
+    }
+    *out = best;
+    return BLASST_OK;
+}
+
+size_t blasst_decode_workspace_size(int B, int Hq, int Hkv, int Lkv, int d, int num_splits) {
+    (void)Hkv;
+    (void)Lkv;
+    if (B < 1 || Hq < 1 || d < 1 || num_splits <= 1) return 0;
+    const size_t o_bytes = (size_t)num_splits * B * Hq * d * sizeof(float);
+    const size_t l_bytes = (size_t)num_splits * B * Hq * sizeof(float);
+    return ((o_bytes + 255) & ~size_t(255)) + l_bytes;
+}
+
+int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
+                  int Hkv, int Lkv, int d, float scale, float lambda, int num_splits, void* workspace,
+                  size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
+                  float* margins, void* stream) {
+    if (!q || !k_cache || !v_cache || !o) return BLASST_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Lkv < 1 || Hq % Hkv != 0) return BLASST_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || !lambda_ok(lambda)) return BLASST_ERR_INVALID_ARG;
+    const int nT = (Lkv + kTile - 1) / kTile;
+    if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (d != 128) return BLASST_ERR_UNSUPPORTED;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BLASST_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
+        (reinterpret_cast<uintptr_t>(skipped_tiles_out) & 7u))
+        return BLASST_ERR_UNSUPPORTED;
+    if (Hkv > 65535 || B > 65535) return BLASST_ERR_UNSUPPORTED;
+    const size_t need = blasst_decode_workspace_size(B, Hq, Hkv, Lkv, d, num_splits);
+    if (num_splits > 1) {
+        if (!workspace) return BLASST_ERR_INVALID_ARG;
+        if (workspace_bytes < need) return BLASST_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned16(workspace)) return BLASST_ERR_UNSUPPORTED;
+    }
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* status = status_word();
+    if (!status) return BLASST_ERR_CUDA;
+    CUtensorMap tk, tv;
+    if (!encode_3d(&tk, k_cache, d, Lkv, (long long)B * Hkv) || !encode_3d(&tv, v_cache, d, Lkv, (long long)B * Hkv))
+        return BLASST_ERR_CUDA;
+    const long long map_n = (long long)B * Hkv * nT;
+    if (skipped_tiles_out && cudaMemsetAsync(skipped_tiles_out, 0, sizeof(unsigned long long), st) != cudaSuccess)
+        return BLASST_ERR_CUDA;
+    if (skip_map && cudaMemsetAsync(skip_map, 2, (size_t)map_n, st) != cudaSuccess) return BLASST_ERR_CUDA;
+    if (margins && cudaMemsetAsync(margins, 0xFF, (size_t)map_n * sizeof(float), st) != cudaSuccess)
+        return BLASST_ERR_CUDA;
+
+    const Thresholds t = thresholds(scale, lambda);
+    blasst::DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.o = o;
+    p.lse = lse;
+    const size_t o_bytes = (size_t)num_splits * B * Hq * d * sizeof(float);
+    p.o_part = num_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    p.lse_part = num_splits > 1
+                     ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) & ~size_t(255)))
+                     : nullptr;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Lkv = Lkv; p.G = G; p.nK = nT; p.S = num_splits;
+    p.c_log2 = t.c_log2;
+    p.scale = scale;
+    p.thr_raw = t.thr_raw;
+    p.lazy_raw = t.lazy_raw;
+    p.skipped = skipped_tiles_out;
+    p.skip_map = skip_map;
+    p.margins = margins;
+    p.status = status;
+    p.watchdog_ns = kWatchdogNs;
+    cudaError_t e = blasst::launch_decode(tk, tv, p, d, st);
+    if (e != cudaSuccess) return BLASST_ERR_CUDA;
+    if (num_splits > 1) {
+        blasst::CombineParams c{};
+        c.o_part = p.o_part;
+        c.lse_part = p.lse_part;
+        c.o = o;
+        c.lse = lse;
+        c.B = B; c.Hq = Hq; c.S = num_splits; c.d = d;
+        e = blasst::launch_combine(c, st);
+    }
+    return cuda_status(e);
+}
+
+int blasst_lambda(int mode, double threshold, double a, double b, double target_sparsity, long long Lkv,
+                  double* lambda_out) {
+    if (!lambda_out || Lkv < 1) return BLASST_ERR_INVALID_ARG;
+    double factor;
+    if (mode == 0) {
+        if (!std::isfinite(threshold) || threshold < 0.0) return BLASST_ERR_INVALID_ARG;
+        factor = threshold * (double)Lkv;  // threshold_scale_factor = threshold * max_kv_len
+    } else if (mode == 1) {
+        if (!std::isfinite(a) || !std::isfinite(b)) return BLASST_ERR_NO_CALIBRATION;
+        if (!std::isfinite(target_sparsity) || target_sparsity < 0.0 || target_sparsity > 1.0 || a < 0.0)
+            return BLASST_ERR_INVALID_ARG;
+        factor = a * std::exp(b * target_sparsity);  // threshold_scale_factor = a * exp(b * s)
+    } else {
+        return BLASST_ERR_INVALID_ARG;
+    }
+    const double lam = mode == 0 ? threshold : factor / (double)Lkv;  // lambda = factor / max_kv_len
+    if (!std::isfinite(lam)) return BLASST_ERR_INVALID_ARG;
+    *lambda_out = lam;
+    return lam > 1.0 ? BLASST_WARN_LAMBDA_GE_1 : BLASST_OK;
+}
+
+int blasst_device_status(int clear) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return BLASST_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_blasst_status, sizeof(int)) != cudaSuccess) return BLASST_ERR_CUDA;
+    if (clear && v) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_blasst_status, &zero, sizeof(int)) != cudaSuccess) return BLASST_ERR_CUDA;
+    }
+    return v ? BLASST_ERR_TIMEOUT : BLASST_OK;
+}
+
+const char* blasst_status_string(int status) {
+    switch (status) {
+        case BLASST_OK: return "ok";
+        case BLASST_WARN_LAMBDA_GE_1: return "lambda from the calibration curve exceeds 1";
+        case BLASST_ERR_INVALID_ARG: return "invalid argument";
+        case BLASST_ERR_UNSUPPORTED: return "unsupported configuration";
+        case BLASST_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case BLASST_ERR_CUDA: return "CUDA error";
+        case BLASST_ERR_TIMEOUT: return "device wait timed out";
+        case BLASST_ERR_NO_CALIBRATION: return "target sparsity requested without calibration coefficients; use a threshold";
+        default: return "unknown status";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+// kernels.cuh -- launch-side view of the prefill, decode and combine kernels:
+// parameter blocks and launcher declarations shared by the C ABI (api.cu) and
+// the kernel translation units.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace blasst {
+
+constexpr int kTile = 128;  // B_r = B_c = 128
+
+struct PrefillParams {
+    void* o;                  // bf16 [B,Hq,Lq,d]
+    float* lse;               // [B,Hq,Lq] or null
+    int B, Hq, Hkv, Lq, Lkv, causal;
+    int nQ, nK;
+    float c_log2;             // scale * log2(e): raw score -> log2 units
+    float scale;              // raw score -> natural-log units
+    float thr_raw;            // ln(lambda) / scale (-inf when lambda == 0)
+    float lazy_raw;           // reference max is moved only when the max grows by more than this
+    unsigned long long* skipped;
+    unsigned char* skip_map;  // [B,Hq,nQ,nK] or null
+    float* margins;           // [B,Hq,nQ,nK] or null
+    int* status;              // device status word
+    unsigned long long watchdog_ns;
+    int elide_v;
+};
+
+struct DecodeParams {
+    const uint16_t* q;        // bf16 [B,Hq,d]
+    void* o;                  // bf16 [B,Hq,d]
+    float* lse;               // [B,Hq] or null
+    float* o_part;            // [S,B,Hq,d] (S > 1)
+    float* lse_part;          // [S,B,Hq]   (S > 1)
+    int B, Hq, Hkv, Lkv, G, nK, S;
+    float c_log2, scale, thr_raw, lazy_raw;
+    unsigned long long* skipped;
+    unsigned char* skip_map;  // [B,Hkv,nK] or null
+    float* margins;           // [B,Hkv,nK] or null
+    int* status;
+    unsigned long long watchdog_ns;
+};
+
+struct CombineParams {
+    const float* o_part;
+    const float* lse_part;
+    void* o;
+    float* lse;
+    int B, Hq, S, d;
+};
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int d, bool p_in_tmem, cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int d,
+                          cudaStream_t stream);
+cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+
+size_t prefill_smem_bytes(int d, bool p_in_tmem);
+size_t decode_smem_bytes(int d);
+
+}  // namespace blasst

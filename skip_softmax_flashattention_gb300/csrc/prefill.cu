@@ -1,0 +1,434 @@
+// prefill.cu -- skip-softmax (BLASST) FlashAttention forward for prefill on sm_103a.
+//
+// One CTA computes one 128-row query tile of one query head against the key tiles
+// it can see, in ascending order (Hitchhiker's Guide Phase 08, Section 1,
+// "FlashAttention Tiling Strategy"), with the BLASST per-tile test between S and
+// the softmax (Skip-Softmax design doc, "Algorithm"; BLASST talk notes, Eq. 2).
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax: thread t owns query row t = TMEM lane t.  Reads S_j from
+//              TMEM, masks, takes the row's tile max m~, updates the exact running
+//              max m, votes (m~ - m < ln lambda), reduces the vote with __all and a
+//              shared-memory atomicAnd across the four warps (BLASST talk notes,
+//              "kernel design: skip predicate reduction"), and for computed tiles
+//              writes P = 2^(S*c - m_ref*c) (bf16) and rescales its O row when the
+//              reference max moves.
+//   warp 4     TMA producer: Q once, then K_j / V_j into a ring of shared-memory
+//              stages (128-byte swizzled boxes of 64 columns).
+//   warp 5     MMA issuer (one thread) and TMEM owner: S_j = Q K_j^T into one of
+//              two TMEM S buffers (issued one tile ahead so the tensor core runs
+//              while the softmax works), and O += P_j V_j for computed tiles only.
+//
+// Skipped tiles omit the exponentials, the row sums and the P.V product; the V
+// tile is still staged (the prefill kernel keeps its prefetch predictable, as the
+// BLASST kernel design describes for prefill).
+//
+// TMEM columns: S buffer 0 = [0,128), S buffer 1 = [128,256), O = [256, 256+D).
+// When P lives in TMEM it overwrites the first 64 columns of its S buffer (two
+// bf16 per 32-bit column); otherwise it is staged in shared memory.
+//
+// The reference max m_ref used for the exponentials only moves when the exact
+// running max exceeds it by more than `lazy_raw` (2^8 in probability units), so
+// the O rescale (a TMEM read-modify-write) is rare; the skip test always uses the
+// exact running max.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace blasst {
+namespace {
+
+constexpr unsigned long long kDrainNs = 1000000000ull;  // drain waits: 1 s
+
+template <int NK, int NV>
+struct PrefillCtrl {
+    uint64_t q_full;
+    uint64_t k_full[NK], k_empty[NK];
+    uint64_t v_full[NV], v_empty[NV];
+    uint64_t s_full[2], p_full[2], p_free[2];
+    uint64_t o_done, drain;
+    uint32_t tmem_base;
+    int vote[3];
+    int dec[2];
+    int abort;
+    float mred[2][4];
+};
+
+template <int D, bool PT>
+struct PrefillCfg {
+    static constexpr int TILE_BYTES = kTile * D * 2;  // a 128 x D bf16 tile
+    static constexpr int BOX_BYTES = kTile * 128;     // one 128-row box of 64 bf16 columns
+    static constexpr int NK = (D == 128) ? (PT ? 3 : 2) : (PT ? 4 : 3);
+    static constexpr int NV = NK;
+    static constexpr int P_BYTES = PT ? 0 : 2 * kTile * kTile * 2;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
+    static constexpr int OFF_P = OFF_V + NV * TILE_BYTES;
+    static constexpr int OFF_CTRL = OFF_P + P_BYTES;
+    using Ctrl = PrefillCtrl<NK, NV>;
+    static constexpr int SMEM = OFF_CTRL + (int)sizeof(Ctrl) + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t O_COL = 256;
+};
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int D, bool PT>
+__global__ void __launch_bounds__(192, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                   const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
+    using C = PrefillCfg<D, PT>;
+    using Ctrl = typename C::Ctrl;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + C::OFF_CTRL);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int G = p.Hq / p.Hkv;
+    const int qt = p.causal ? (p.nQ - 1 - (int)blockIdx.x) : (int)blockIdx.x;  // heavy tiles first
+    const int h = blockIdx.y, b = blockIdx.z, hk = h / G;
+    const int r0 = qt * kTile;
+    const int rows = min(kTile, p.Lq - r0);
+    const int off = p.Lkv - p.Lq;  // bottom-right causal alignment
+    int n = p.nK;                  // key tiles visited
+    if (p.causal) {
+        const int maxkey = r0 + rows - 1 + off;
+        n = maxkey < 0 ? 0 : min(p.nK, maxkey / kTile + 1);
+    }
+
+    if (tid == 0) {
+        mbar_init(&ctrl->q_full, 1);
+        for (int i = 0; i < C::NK; ++i) {
+            mbar_init(&ctrl->k_full[i], 1);
+            mbar_init(&ctrl->k_empty[i], 1);
+        }
+        for (int i = 0; i < C::NV; ++i) {
+            mbar_init(&ctrl->v_full[i], 1);
+            mbar_init(&ctrl->v_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&ctrl->s_full[i], 1);
+            mbar_init(&ctrl->p_full[i], 4);
+            mbar_init(&ctrl->p_free[i], 1);
+        }
+        mbar_init(&ctrl->o_done, 1);
+        mbar_init(&ctrl->drain, 1);
+        ctrl->vote[0] = ctrl->vote[1] = ctrl->vote[2] = 1;
+        ctrl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&ctrl->tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    const Watchdog wd{&ctrl->abort, p.status, p.watchdog_ns};
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && n > 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            const int zq = b * p.Hq + h, zkv = b * p.Hkv + hk;
+            mbar_arrive_expect_tx(&ctrl->q_full, C::TILE_BYTES);
+#pragma unroll
+            for (int x = 0; x < D / 64; ++x)
+                tma_load_3d(smem + C::OFF_Q + x * C::BOX_BYTES, &tq, &ctrl->q_full, x * 64, r0, zq);
+            int issued_k = 0, issued_v = 0;
+            for (int j = 0; j < n; ++j) {
+                const int ks = j % C::NK;
+                if (j >= C::NK && !mbar_wait(&ctrl->k_empty[ks], ((j / C::NK) - 1) & 1, wd)) break;
+                mbar_arrive_expect_tx(&ctrl->k_full[ks], C::TILE_BYTES);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(smem + C::OFF_K + ks * C::TILE_BYTES + x * C::BOX_BYTES, &tk, &ctrl->k_full[ks],
+                                x * 64, j * kTile, zkv);
+                issued_k = j + 1;
+                const int vs = j % C::NV;
+                if (j >= C::NV && !mbar_wait(&ctrl->v_empty[vs], ((j / C::NV) - 1) & 1, wd)) break;
+                mbar_arrive_expect_tx(&ctrl->v_full[vs], C::TILE_BYTES);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(smem + C::OFF_V + vs * C::TILE_BYTES + x * C::BOX_BYTES, &tv, &ctrl->v_full[vs],
+                                x * 64, j * kTile, zkv);
+                issued_v = j + 1;
+            }
+            // Every copy this thread started must land before the CTA can exit.
+            mbar_wait_drain(&ctrl->q_full, 0, kDrainNs);
+            for (int j = max(0, issued_k - C::NK); j < issued_k; ++j)
+                mbar_wait_drain(&ctrl->k_full[j % C::NK], (j / C::NK) & 1, kDrainNs);
+            for (int j = max(0, issued_v - C::NV); j < issued_v; ++j)
+                mbar_wait_drain(&ctrl->v_full[j % C::NV], (j / C::NV) & 1, kDrainNs);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
+            const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+            const uint32_t sK = smem_u32(smem + C::OFF_K);
+            const uint32_t sV = smem_u32(smem + C::OFF_V);
+            const uint32_t sP = smem_u32(smem + C::OFF_P);
+            auto issue_s = [&](int j) -> bool {
+                const int ks = j % C::NK;
+                if (!mbar_wait(&ctrl->k_full[ks], (j / C::NK) & 1, wd)) return false;
+                tc_fence_after();
+                const uint32_t dcol = tmem + (uint32_t)(j & 1) * 128u;
+                const uint32_t kb = sK + ks * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t o = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                    mma_ss(dcol, desc_kmajor_sw128(sQ + o), desc_kmajor_sw128(kb + o), kIdescS, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&ctrl->s_full[j & 1]);
+                mma_commit(&ctrl->k_empty[ks]);
+                return true;
+            };
+            bool ok = mbar_wait(&ctrl->q_full, 0, wd);
+            if (ok) ok = issue_s(0);
+            int npv = 0;
+            for (int j = 0; j < n && ok; ++j) {
+                if (j + 1 < n && !(ok = issue_s(j + 1))) break;
+                if (!(ok = mbar_wait(&ctrl->p_full[j & 1], (j >> 1) & 1, wd))) break;
+                const int vs = j % C::NV;
+                if (!(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
+                tc_fence_after();
+                const bool skip = reinterpret_cast<volatile int*>(ctrl->dec)[j & 1] != 0;
+                if (!skip) {
+                    const uint32_t vb = sV + vs * C::TILE_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t bdesc = desc_mnmajor_sw128(vb + kk * 2048, C::BOX_BYTES);
+                        const uint32_t acc = (npv > 0 || kk > 0) ? 1u : 0u;
+                        if constexpr (PT) {
+                            mma_ts(tmem + C::O_COL, tmem + (uint32_t)(j & 1) * 128u + kk * 8, bdesc, kIdescO, acc);
+                        } else {
+                            const uint32_t pa = sP + (j & 1) * (kTile * kTile * 2) + (kk >> 2) * C::BOX_BYTES +
+                                                (kk & 3) * 32;
+                            mma_ss(tmem + C::O_COL, desc_kmajor_sw128(pa), bdesc, kIdescO, acc);
+                        }
+                    }
+                    mma_commit(&ctrl->o_done);
+                    if constexpr (!PT) mma_commit(&ctrl->p_free[j & 1]);
+                    mma_commit(&ctrl->v_empty[vs]);
+                    ++npv;
+                } else {
+                    mbar_arrive(&ctrl->v_empty[vs]);
+                }
+            }
+            mma_commit(&ctrl->drain);
+            mbar_wait_drain(&ctrl->drain, 0, kDrainNs);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int row = tid;
+        const int rabs = r0 + row;
+        const bool valid = rabs < p.Lq;
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        const int lim_row = p.causal ? rabs + off : 0x3fffffff;
+        const long long mapbase = ((long long)(b * p.Hq + h) * p.nQ + qt) * p.nK;
+        float m_exact = -CUDART_INF_F, m_ref = -CUDART_INF_F, l = 0.f;
+        int npv = 0;
+        int puse0 = 0, puse1 = 0;
+        unsigned long long nskip = 0;
+        uint8_t* sP = smem + C::OFF_P;
+
+        for (int j = 0; j < n; ++j) {
+            mbar_wait(&ctrl->s_full[j & 1], (j >> 1) & 1, wd);
+            tc_fence_after();
+            uint32_t xr[128];
+            const uint32_t sc = tl + (uint32_t)(j & 1) * 128u;
+            tmem_ld32(sc + 0, xr);
+            tmem_ld32(sc + 32, xr + 32);
+            tmem_ld32(sc + 64, xr + 64);
+            tmem_ld32(sc + 96, xr + 96);
+            tmem_ld_wait();
+            fence_regs<128>(xr);
+
+            // mask keys beyond Lkv and (causal) beyond the row's diagonal
+            const int lim = min(p.Lkv - 1, lim_row) - j * kTile;
+            if (lim < kTile - 1) {
+#pragma unroll
+                for (int c = 0; c < kTile; ++c)
+                    if (c > lim) xr[c] = __float_as_uint(-CUDART_INF_F);
+            }
+            float mt = -CUDART_INF_F;
+#pragma unroll
+            for (int c = 0; c < kTile; ++c) mt = fmaxf(mt, __uint_as_float(xr[c]));
+            const float mnew = fmaxf(m_exact, mt);
+            const float diff = mt - mnew;  // NaN when both are -inf: votes "compute"
+            const bool vote = !valid || (diff < p.thr_raw);
+            const unsigned all = __all_sync(0xffffffffu, vote);
+            if (lane == 0) atomicAnd(&ctrl->vote[j % 3], (int)all);
+            if (p.margins) {
+                float g = valid ? ((mt == -CUDART_INF_F && mnew == -CUDART_INF_F) ? CUDART_INF_F : diff)
+                                : -CUDART_INF_F;
+#pragma unroll
+                for (int s = 16; s > 0; s >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, s));
+                if (lane == 0) ctrl->mred[j & 1][warp] = g;
+            }
+            named_bar_sync(1, 128);
+            const bool skip = reinterpret_cast<volatile int*>(ctrl->vote)[j % 3] != 0;
+            if (tid == 0) {
+                ctrl->vote[(j + 2) % 3] = 1;
+                reinterpret_cast<volatile int*>(ctrl->dec)[j & 1] = skip ? 1 : 0;
+                if (p.skip_map) p.skip_map[mapbase + j] = skip ? 1 : 0;
+                if (p.margins) {
+                    const volatile float* mr = ctrl->mred[j & 1];
+                    const float g = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3]));
+                    p.margins[mapbase + j] = g * p.scale;
+                }
+                nskip += skip ? 1 : 0;
+            }
+            m_exact = mnew;
+
+            if (!skip) {
+                // move the reference max (rarely, see lazy_raw) and rescale this row of O
+                const bool move = mnew != -CUDART_INF_F && (m_ref == -CUDART_INF_F || mnew > m_ref + p.lazy_raw);
+                const float alpha = move ? (m_ref == -CUDART_INF_F ? 0.f : ex2((m_ref - mnew) * p.c_log2)) : 1.f;
+                if (__any_sync(0xffffffffu, move) && npv > 0) {
+                    mbar_wait(&ctrl->o_done, (npv - 1) & 1, wd);
+                    tc_fence_after();
+#pragma unroll
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t t[32];
+                        tmem_ld32(tl + C::O_COL + cc, t);
+                        tmem_ld_wait();
+                        fence_regs<32>(t);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) t[i] = __float_as_uint(__uint_as_float(t[i]) * alpha);
+                        tmem_st32(tl + C::O_COL + cc, t);
+                    }
+                    tmem_st_wait();
+                }
+                if (move) {
+                    l *= alpha;
+                    m_ref = mnew;
+                }
+                const float mc = (m_ref == -CUDART_INF_F ? 0.f : m_ref) * p.c_log2;
+                const float cl = p.c_log2;
+                if constexpr (!PT) {
+                    const int pb = j & 1;
+                    const int uses = pb ? puse1 : puse0;
+                    if (uses > 0) mbar_wait(&ctrl->p_free[pb], (uses - 1) & 1, wd);
+                }
+                float rs = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float p0 = ex2(fmaf(__uint_as_float(xr[ch * 32 + 2 * i]), cl, -mc));
+                        const float p1 = ex2(fmaf(__uint_as_float(xr[ch * 32 + 2 * i + 1]), cl, -mc));
+                        rs += p0 + p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    if constexpr (PT) {
+                        tmem_st16(tl + (uint32_t)(j & 1) * 128u + ch * 16, pk);
+                    } else {
+                        // P buffer: [key half][128 rows][64 keys], 16-byte chunks swizzled by row
+                        uint8_t* pbuf = sP + (j & 1) * (kTile * kTile * 2) + (ch >> 1) * C::BOX_BYTES + row * 128;
+#pragma unroll
+                        for (int q4 = 0; q4 < 4; ++q4) {
+                            const int chunk = (ch & 1) * 4 + q4;
+                            uint4 v4 = make_uint4(pk[q4 * 4], pk[q4 * 4 + 1], pk[q4 * 4 + 2], pk[q4 * 4 + 3]);
+                            *reinterpret_cast<uint4*>(pbuf + ((chunk ^ (row & 7)) << 4)) = v4;
+                        }
+                    }
+                }
+                l += rs;
+                ++npv;
+                if constexpr (PT) {
+                    tmem_st_wait();
+                } else {
+                    if (j & 1) ++puse1; else ++puse0;
+                    fence_proxy_async_smem();
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->p_full[j & 1]);
+        }
+
+        // ---------------------------------------------------------------- epilogue
+        if (npv > 0) {
+            mbar_wait(&ctrl->o_done, (npv - 1) & 1, wd);
+            tc_fence_after();
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((long long)(b * p.Hq + h) * p.Lq + rabs) * D;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+            uint32_t t[32];
+            if (npv > 0) {
+                tmem_ld32(tl + C::O_COL + cc, t);
+                tmem_ld_wait();
+                fence_regs<32>(t);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) t[i] = 0u;
+            }
+            if (valid) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 v4;
+                    v4.x = pack_bf16x2(__uint_as_float(t[q4 * 8 + 0]) * inv, __uint_as_float(t[q4 * 8 + 1]) * inv);
+                    v4.y = pack_bf16x2(__uint_as_float(t[q4 * 8 + 2]) * inv, __uint_as_float(t[q4 * 8 + 3]) * inv);
+                    v4.z = pack_bf16x2(__uint_as_float(t[q4 * 8 + 4]) * inv, __uint_as_float(t[q4 * 8 + 5]) * inv);
+                    v4.w = pack_bf16x2(__uint_as_float(t[q4 * 8 + 6]) * inv, __uint_as_float(t[q4 * 8 + 7]) * inv);
+                    *reinterpret_cast<uint4*>(orow + cc + q4 * 8) = v4;
+                }
+            }
+        }
+        if (valid && p.lse) {
+            p.lse[(long long)(b * p.Hq + h) * p.Lq + rabs] =
+                l > 0.f ? m_ref * p.scale + __logf(l) : -CUDART_INF_F;
+        }
+        if (tid == 0 && p.skipped && nskip) atomicAdd(p.skipped, nskip);
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D, bool PT>
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                     cudaStream_t stream) {
+    using C = PrefillCfg<D, PT>;
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.nQ, p.Hq, p.B);
+    prefill_kernel<D, PT><<<grid, 192, C::SMEM, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                           const PrefillParams& p, int d, bool p_in_tmem, cudaStream_t stream) {
+    if (d == 128) return p_in_tmem ? launch_t<128, true>(tq, tk, tv, p, stream) : launch_t<128, false>(tq, tk, tv, p, stream);
+    return p_in_tmem ? launch_t<64, true>(tq, tk, tv, p, stream) : launch_t<64, false>(tq, tk, tv, p, stream);
+}
+
+size_t prefill_smem_bytes(int d, bool p_in_tmem) {
+    if (d == 128) return p_in_tmem ? PrefillCfg<128, true>::SMEM : PrefillCfg<128, false>::SMEM;
+    return p_in_tmem ? PrefillCfg<64, true>::SMEM : PrefillCfg<64, false>::SMEM;
+}
+
+}  // namespace blasst

@@ -1,0 +1,170 @@
+"""GPU-vs-oracle comparison rules shared by the GPU tests and the smoke check.
+
+Acceptance (per tile and per element):
+  * every visited tile's skip decision equals the oracle's, except tiles whose
+    oracle margin lies within 1e-3 of ln(lambda) -- those are logged, not failed;
+  * the skipped-tile count the kernel reports equals the number of skipped tiles
+    in its map, and (where the oracle covers the whole problem) the oracle's count
+    up to the logged band tiles;
+  * O (bf16) is within max-abs 2e-2 and mean-abs 2e-3 of the fp32 oracle run with
+    the GPU's skip map forced; lse is within 1e-3 (both -inf for rows with no key).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from oracle import oracle as orc
+
+BAND = 1e-3
+O_MAX_ABS = 2e-2
+O_MEAN_ABS = 2e-3
+LSE_ABS = 1e-3
+TILE = 128
+
+
+def _lnlam(lam):
+    return -math.inf if lam <= 0 else math.log(lam)
+
+
+def _check_rows(o_gpu, lse_gpu, o_ref, lse_ref, what):
+    o_gpu = np.asarray(o_gpu, np.float64)
+    o_ref = np.asarray(o_ref, np.float64)
+    err = np.abs(o_gpu - o_ref)
+    assert np.isfinite(o_gpu).all(), f"{what}: non-finite O"
+    mx, mean = float(err.max()), float(err.mean())
+    assert mx <= O_MAX_ABS, f"{what}: O max-abs {mx:.3e} > {O_MAX_ABS}"
+    assert mean <= O_MEAN_ABS, f"{what}: O mean-abs {mean:.3e} > {O_MEAN_ABS}"
+    lse_gpu = np.asarray(lse_gpu, np.float64)
+    lse_ref = np.asarray(lse_ref, np.float64)
+    inf_g, inf_r = np.isneginf(lse_gpu), np.isneginf(lse_ref)
+    assert np.array_equal(inf_g, inf_r), f"{what}: -inf lse rows differ"
+    fin = ~inf_r
+    if fin.any():
+        le = float(np.abs(lse_gpu[fin] - lse_ref[fin]).max())
+        assert le <= LSE_ABS, f"{what}: lse abs err {le:.3e} > {LSE_ABS}"
+    return mx, mean
+
+
+def _decisions(gpu_map, ora_map, ora_margin, lam, what):
+    gpu_map = np.asarray(gpu_map)
+    ora_map = np.asarray(ora_map)
+    assert np.array_equal(gpu_map == 2, ora_map == 2), f"{what}: visited tiles differ"
+    vis = ora_map != 2
+    diff = vis & (gpu_map != ora_map)
+    band = np.abs(np.asarray(ora_margin, np.float64) - _lnlam(lam)) < BAND
+    bad = diff & ~band
+    assert not bad.any(), (f"{what}: {int(bad.sum())} tile decisions differ outside the 1e-3 band "
+                           f"(first at {np.argwhere(bad)[0].tolist()})")
+    return int(diff.sum())
+
+
+def prefill_units_check(a, res, lam, units, log=None):
+    """Compare the GPU prefill result on the given (b, h, qtile) units.
+
+    a: workloads.Attn on the GPU; res: dict from blasst.prefill(..., want_map=True).
+    Returns (#band tiles, max abs O err, mean abs O err)."""
+    G = a.Hq // a.Hkv
+    gmap = res["map"].cpu().numpy()
+    o_gpu = res["o"]
+    lse_gpu = res["lse"]
+    by_head = {}
+    for (b, h, t) in units:
+        by_head.setdefault((b, h), []).append(t)
+    band_total, errs = 0, []
+    for (b, h), tiles in sorted(by_head.items()):
+        hk = h // G
+        q = a.q[b:b + 1, h:h + 1].float().cpu()
+        k = a.k[b:b + 1, hk:hk + 1].float().cpu()
+        v = a.v[b:b + 1, hk:hk + 1].float().cpu()
+        uu = [(0, 0, t) for t in tiles]
+        own = orc.prefill_tiled(q, k, v, a.causal, a.scale, lam, units=uu, precision="f32")
+        forced_map = np.full(own["map"].shape, 0, np.uint8)
+        forced_map[0, 0] = gmap[b, h]
+        ref = orc.prefill_tiled(q, k, v, a.causal, a.scale, lam, units=uu, forced=forced_map, precision="f32")
+        for t in tiles:
+            what = f"{a.name} lam={lam:g} b={b} h={h} qtile={t}"
+            band_total += _decisions(gmap[b, h, t], own["map"][0, 0, t], own["margin"][0, 0, t], lam, what)
+            rows = slice(t * TILE, min(a.Lq, (t + 1) * TILE))
+            og = o_gpu[b, h, rows].float().cpu().numpy()
+            lg = lse_gpu[b, h, rows].cpu().numpy()
+            errs.append(_check_rows(og, lg, ref["o"][0, 0, rows], ref["lse"][0, 0, rows], what))
+    if log is not None and band_total:
+        log.append(f"{a.name} lam={lam:g}: {band_total} tiles inside the 1e-3 margin band")
+    return band_total, max(e[0] for e in errs), float(np.mean([e[1] for e in errs]))
+
+
+def prefill_full_check(a, res, lam, log=None):
+    """Whole-problem comparison (small problems): decisions, exact count, O, lse."""
+    own = orc.prefill_tiled(a.q.float().cpu(), a.k.float().cpu(), a.v.float().cpu(), a.causal, a.scale, lam,
+                            precision="f32")
+    gmap = res["map"].cpu().numpy()
+    band = _decisions(gmap, own["map"], own["margin"], lam, f"{a.name} lam={lam:g}")
+    n_gpu = int(res["skipped"].item())
+    assert n_gpu == int((gmap == 1).sum()), "reported count differs from the map"
+    assert abs(n_gpu - own["skipped"]) <= band, f"count {n_gpu} vs oracle {own['skipped']} (band {band})"
+    if band == 0:
+        assert n_gpu == own["skipped"]
+    ref = orc.prefill_tiled(a.q.float().cpu(), a.k.float().cpu(), a.v.float().cpu(), a.causal, a.scale, lam,
+                            forced=gmap, precision="f32")
+    mx, mean = _check_rows(res["o"].float().cpu().numpy(), res["lse"].cpu().numpy(), ref["o"], ref["lse"],
+                           f"{a.name} lam={lam:g}")
+    if log is not None and band:
+        log.append(f"{a.name} lam={lam:g}: {band} tiles inside the 1e-3 margin band")
+    return band, mx, mean, n_gpu
+
+
+def decode_units_check(a, res, lam, S, units, log=None):
+    """Compare a GPU decode result on (b, hkv) units (q is [B,Hq,1,d])."""
+    G = a.Hq // a.Hkv
+    gmap = res["map"].cpu().numpy()
+    band_total, errs = 0, []
+    for (b, hk) in units:
+        q = a.q[b:b + 1, hk * G:(hk + 1) * G].float().cpu()
+        k = a.k[b:b + 1, hk:hk + 1].float().cpu()
+        v = a.v[b:b + 1, hk:hk + 1].float().cpu()
+        own = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=S, precision="f32")
+        ref = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=S, forced=gmap[b:b + 1, hk:hk + 1],
+                               precision="f32")
+        what = f"{a.name} lam={lam:g} S={S} b={b} hkv={hk}"
+        band_total += _decisions(gmap[b, hk], own["map"][0, 0], own["margin"][0, 0], lam, what)
+        og = res["o"][b, hk * G:(hk + 1) * G].float().cpu().numpy()
+        lg = res["lse"][b, hk * G:(hk + 1) * G].cpu().numpy()
+        errs.append(_check_rows(og, lg, ref["o"][0], ref["lse"][0], what))
+    if log is not None and band_total:
+        log.append(f"{a.name} lam={lam:g} S={S}: {band_total} tiles inside the 1e-3 margin band")
+    return band_total, max(e[0] for e in errs), float(np.mean([e[1] for e in errs]))
+
+
+def decode_full_check(a, res, lam, S, log=None):
+    own = orc.decode_tiled(a.q.float().cpu(), a.k.float().cpu(), a.v.float().cpu(), a.scale, lam, num_splits=S,
+                           precision="f32")
+    gmap = res["map"].cpu().numpy()
+    band = _decisions(gmap, own["map"], own["margin"], lam, f"{a.name} lam={lam:g} S={S}")
+    n_gpu = int(res["skipped"].item())
+    assert n_gpu == int((gmap == 1).sum())
+    assert abs(n_gpu - own["skipped"]) <= band
+    if band == 0:
+        assert n_gpu == own["skipped"]
+    ref = orc.decode_tiled(a.q.float().cpu(), a.k.float().cpu(), a.v.float().cpu(), a.scale, lam, num_splits=S,
+                           forced=gmap, precision="f32")
+    mx, mean = _check_rows(res["o"].float().cpu().numpy(), res["lse"].cpu().numpy(), ref["o"], ref["lse"],
+                           f"{a.name} lam={lam:g} S={S}")
+    if log is not None and band:
+        log.append(f"{a.name} lam={lam:g} S={S}: {band} tiles inside the 1e-3 margin band")
+    return band, mx, mean, n_gpu
+
+
+def sample_units(rng, B, H, nQ, k, always=()):
+    """k random (b, h, qtile) units plus the listed ones (first/last tiles)."""
+    units = set(always)
+    while len(units) < k + len(always):
+        units.add((int(rng.integers(B)), int(rng.integers(H)), int(rng.integers(nQ))))
+    return sorted(units)
+
+
+def to_gpu(a, device="cuda"):
+    a.q, a.k, a.v = a.q.to(device), a.k.to(device), a.v.to(device)
+    return a

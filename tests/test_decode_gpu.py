@@ -1,0 +1,64 @@
+"""Split-KV decode parity on the GPU: the CUDA kernels (split pass + merge)
+against the CPU oracle, whole on small problems and on sampled (batch, KV head)
+pairs at the full decode workload size."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from skip_softmax_flashattention_gb300 import blasst as K
+from skip_softmax_flashattention_gb300 import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    K.blasst_device_status(1)
+    yield
+    assert K.blasst_device_status(1) == K.BLASST_OK, "a kernel wait timed out"
+
+
+SHAPES = [
+    # B, Hq, Hkv, Lkv
+    (2, 8, 2, 1000),
+    (3, 4, 4, 129),
+    (1, 16, 1, 5000),
+    (2, 32, 2, 777),
+    (1, 2, 1, 128),
+    (4, 32, 8, 2048),
+]
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+@pytest.mark.parametrize("S", [1, 2, 5])
+@pytest.mark.parametrize("lam", [0.0, 0.05, 0.3])
+def test_decode_small(shape, S, lam):
+    B, Hq, Hkv, L = shape
+    if S > -(-L // 128):
+        pytest.skip("more splits than key tiles")
+    a = parity.to_gpu(W.decode(seed=21, B=B, Hq=Hq, Hkv=Hkv, Lkv=L))
+    res = K.decode(a.q, a.k, a.v, a.scale, lam, num_splits=S, want_map=True)
+    torch.cuda.synchronize()
+    band, mx, mean, n = parity.decode_full_check(a, res, lam, S)
+    if lam == 0.0:
+        assert n == 0
+
+
+def test_decode_full_size():
+    a = parity.to_gpu(W.decode(seed=0, device="cuda"))
+    rc, S = K.blasst_decode_num_splits(a.B, a.Hq, a.Hkv, a.Lkv, a.d, 0)
+    assert rc == 0
+    rng = np.random.default_rng(3)
+    units = sorted({(0, 0), (a.B - 1, a.Hkv - 1)} | {(int(rng.integers(a.B)), int(rng.integers(a.Hkv)))
+                                                       for _ in range(6)})
+    for lam in (0.0, 4 / a.Lkv, 40 / a.Lkv, 0.3):
+        res = K.decode(a.q, a.k, a.v, a.scale, lam, num_splits=S, want_map=True)
+        torch.cuda.synchronize()
+        n = int(res["skipped"].item())
+        assert n == int((res["map"] == 1).sum().item())
+        if lam == 0.0:
+            assert n == 0
+        parity.decode_units_check(a, res, lam, S, units)

@@ -1,0 +1,140 @@
+"""Prefill parity on the GPU: the CUDA kernel against the CPU oracle.
+
+Small problems are compared whole (every tile decision, the exact skipped count,
+every output row); the full-size LLM-prefill, video-DiT and planted-70 workloads
+are compared on sampled query tiles (first, last and random ones), in the same
+launch configuration the benchmark times."""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from skip_softmax_flashattention_gb300 import blasst as K
+from skip_softmax_flashattention_gb300 import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [0, K.BLASST_PREFILL_P_VIA_SMEM]
+VARIANT_IDS = ["P-in-TMEM", "P-in-SMEM"]
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    K.blasst_device_status(1)
+    yield
+    assert K.blasst_device_status(1) == K.BLASST_OK, "a kernel wait timed out"
+
+
+@pytest.mark.parametrize("flags", VARIANTS, ids=VARIANT_IDS)
+@pytest.mark.parametrize("planted", [False, True])
+@pytest.mark.parametrize("lam", [0.0, 1e-3, 1e-2])
+def test_tiny_workload(flags, planted, lam):
+    a = parity.to_gpu(W.tiny(seed=0, planted=planted))
+    res = K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam, want_map=True, flags=flags)
+    torch.cuda.synchronize()
+    band, mx, mean, n = parity.prefill_full_check(a, res, lam)
+    if lam == 0.0:
+        assert n == 0
+    if planted and lam == 1e-2:
+        assert n == 16  # keys 256..511 = tiles 2,3 of every query tile: 2 heads x 4 q-tiles x 2
+
+
+SHAPES = [
+    # B, Hq, Hkv, Lq, Lkv, d, causal
+    (1, 2, 1, 1, 1, 128, False),
+    (1, 2, 2, 120, 120, 64, True),
+    (2, 4, 2, 300, 300, 128, True),
+    (1, 4, 1, 257, 1000, 128, True),   # Lq < Lkv: bottom-right diagonal
+    (1, 2, 1, 500, 200, 128, True),    # Lq > Lkv: the first 300 rows see no key
+    (1, 2, 2, 129, 513, 64, False),
+    (1, 8, 2, 640, 640, 128, False),
+]
+
+
+@pytest.mark.parametrize("flags", VARIANTS, ids=VARIANT_IDS)
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+@pytest.mark.parametrize("lam", [0.0, 0.05, 0.5])
+def test_ragged_and_edge_shapes(shape, lam, flags):
+    B, Hq, Hkv, Lq, Lkv, d, causal = shape
+    a = parity.to_gpu(W.small_random(11, B, Hq, Hkv, Lq, Lkv, d, causal, logit_mult=3.0))
+    res = K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam, want_map=True, flags=flags)
+    torch.cuda.synchronize()
+    parity.prefill_full_check(a, res, lam)
+
+
+def test_margins_output_matches_oracle():
+    a = parity.to_gpu(W.small_random(12, 1, 4, 2, 384, 640, 128, True, logit_mult=3.0))
+    res = K.prefill(a.q, a.k, a.v, True, a.scale, 0.0, want_map=True, want_margins=True)
+    torch.cuda.synchronize()
+    from oracle import oracle as orc
+
+    own = orc.prefill_tiled(a.q.float().cpu(), a.k.float().cpu(), a.v.float().cpu(), True, a.scale, 0.0)
+    g = res["margins"].cpu().numpy()
+    ref = own["margin"]
+    assert np.array_equal(np.isnan(g), np.isnan(ref))
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isinf(g), np.isinf(ref))
+    assert np.abs(g[fin] - ref[fin]).max() < 1e-3
+
+
+def test_llm_prefill_full_size():
+    L = 16384
+    a = parity.to_gpu(W.llm(seed=0, L=L, device="cuda"))
+    rng = np.random.default_rng(0)
+    nQ = L // 128
+    units = parity.sample_units(rng, 1, a.Hq, nQ, 6, always=[(0, 0, 0), (0, 31, nQ - 1), (0, 17, nQ // 2)])
+    for A in (0, 4, 40):
+        lam = A / L
+        res = K.prefill(a.q, a.k, a.v, True, a.scale, lam, want_map=True)
+        torch.cuda.synchronize()
+        n = int(res["skipped"].item())
+        assert n == int((res["map"] == 1).sum().item())
+        if A == 0:
+            assert n == 0
+        parity.prefill_units_check(a, res, lam, units)
+
+
+def test_dit_full_size():
+    a = parity.to_gpu(W.dit(seed=0, device="cuda"))
+    rng = np.random.default_rng(1)
+    nQ = -(-a.Lq // 128)
+    units = parity.sample_units(rng, 1, a.Hq, nQ, 4, always=[(0, 0, 0), (0, a.Hq - 1, nQ - 1)])
+    for lam in (0.0, 1e-4, 1e-3, 1e-2):
+        res = K.prefill(a.q, a.k, a.v, False, a.scale, lam, want_map=True)
+        torch.cuda.synchronize()
+        n = int(res["skipped"].item())
+        assert n == int((res["map"] == 1).sum().item())
+        if lam == 0:
+            assert n == 0
+        parity.prefill_units_check(a, res, lam, units)
+
+
+def test_planted70_skip_set_and_parity():
+    L = 16384
+    a = parity.to_gpu(W.planted70(seed=0, L=L, device="cuda"))
+    first = a.extra["first_zero_tile"]
+    res = K.prefill(a.q, a.k, a.v, False, a.scale, 1e-2, want_map=True)
+    torch.cuda.synchronize()
+    mp = res["map"].cpu().numpy()
+    assert (mp[..., first:] == 1).all()
+    assert (mp[..., :first] == 0).mean() > 0.99
+    rng = np.random.default_rng(2)
+    units = parity.sample_units(rng, 1, a.Hq, L // 128, 3, always=[(0, 0, 0)])
+    parity.prefill_units_check(a, res, 1e-2, units)
+
+
+def test_short_watchdog_reports_timeout_and_context_survives():
+    """Waits with a ~1 us limit give up; the kernel records a timeout, drains its
+    copies, frees its tensor memory and exits; the next normal call is correct."""
+    a = parity.to_gpu(W.small_random(13, 1, 4, 2, 1024, 4096, 128, True))
+    K.blasst_device_status(1)
+    K.prefill(a.q, a.k, a.v, True, a.scale, 0.0, flags=K.BLASST_FLAG_TEST_SHORT_WATCHDOG)
+    assert K.blasst_device_status(1) == K.BLASST_ERR_TIMEOUT
+    res = K.prefill(a.q, a.k, a.v, True, a.scale, 0.0, want_map=True)
+    torch.cuda.synchronize()
+    assert K.blasst_device_status(0) == K.BLASST_OK
+    parity.prefill_full_check(a, res, 0.0)
