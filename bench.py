@@ -439,6 +439,32 @@ def run_ours(args):
     return 0
 
 
+def run_only(args):
+    """One kernel on its own (`--only prefill|decode`), `--steps` launches after
+    `--warmup`: the small case the ncu captures run (no timing is reported)."""
+    import torch
+
+    from skip_softmax_flashattention_gb300 import blasst as K
+    from skip_softmax_flashattention_gb300 import workloads as W
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    if args.only == "prefill":
+        a = W.llm(seed=0, L=args.prefill_len, device=dev)
+        lam = args.lam_a / a.Lkv
+        for _ in range(args.warmup + args.steps):
+            K.prefill(a.q, a.k, a.v, True, a.scale, lam)
+    else:
+        a = W.decode(seed=0, B=args.decode_batch, device=dev)
+        lam = args.threshold if args.threshold is not None else args.lam_a / a.Lkv
+        for _ in range(args.warmup + args.steps):
+            K.decode(a.q, a.k, a.v, a.scale, lam, num_splits=args.splits)
+    torch.cuda.synchronize()
+    st = K.blasst_device_status(1)
+    print(json.dumps({"only": args.only, "status": st}))
+    return 0 if st == 0 else 1
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -450,9 +476,16 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-units", type=int, default=16)
+    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+                    help="launch one kernel only (profiling case); no JSON metric line")
+    ap.add_argument("--prefill-len", type=int, default=16384)
+    ap.add_argument("--decode-batch", type=int, default=64)
+    ap.add_argument("--splits", type=int, default=0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.only:
+        return run_only(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -61,7 +61,9 @@ extern "C" {
 /* flags for blasst_prefill_ex */
 #define BLASST_PREFILL_ELIDE_V 0x1u      /* also skip the V tile load of skipped tiles (not in this build: UNSUPPORTED) */
 #define BLASST_PREFILL_P_VIA_SMEM 0x2u   /* stage P in shared memory instead of tensor memory (results identical) */
-#define BLASST_FLAG_TEST_SHORT_WATCHDOG 0x80000000u /* test only: device waits give up after ~1 us */
+#define BLASST_FLAG_TEST_SHORT_WATCHDOG 0x80000000u /* test only: waits give up after 200 us and the MMA issuer
+                                                       first waits on a barrier nothing arrives on, so the call
+                                                       always ends in BLASST_ERR_TIMEOUT (outputs invalid) */
 
 /*
  * Prefill / non-causal self-attention forward.

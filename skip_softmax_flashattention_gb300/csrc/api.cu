@@ -19,7 +19,7 @@ namespace {
 using blasst::kTile;
 
 constexpr unsigned long long kWatchdogNs = 4000000000ull;  // 4 s per wait
-constexpr unsigned long long kShortWatchdogNs = 1000ull;   // test flag: 1 us
+constexpr unsigned long long kShortWatchdogNs = 200000ull;  // test flag: 200 us
 constexpr int kMaxDevices = 64;
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -146,6 +146,7 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
     p.status = status;
     p.watchdog_ns = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? kShortWatchdogNs : kWatchdogNs;
     p.elide_v = 0;
+    p.test_stall = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? 1 : 0;
     const bool p_in_tmem = (flags & BLASST_PREFILL_P_VIA_SMEM) == 0;
     return cuda_status(blasst::launch_prefill(tq, tk, tv, p, d, p_in_tmem, st));
 }

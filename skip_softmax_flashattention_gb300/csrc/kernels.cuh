@@ -25,6 +25,7 @@ struct PrefillParams {
     int* status;              // device status word
     unsigned long long watchdog_ns;
     int elide_v;
+    int test_stall;           // test only: the MMA issuer first waits on a barrier nothing arrives on
 };
 
 struct DecodeParams {

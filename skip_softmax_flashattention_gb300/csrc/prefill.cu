@@ -50,7 +50,7 @@ struct PrefillCtrl {
     uint64_t k_full[NK], k_empty[NK];
     uint64_t v_full[NV], v_empty[NV];
     uint64_t s_full[2], p_full[2], p_free[2];
-    uint64_t o_done, drain;
+    uint64_t o_done, drain, never;
     uint32_t tmem_base;
     int vote[3];
     int dec[2];
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(192, 1)
         }
         mbar_init(&ctrl->o_done, 1);
         mbar_init(&ctrl->drain, 1);
+        mbar_init(&ctrl->never, 1);
         ctrl->vote[0] = ctrl->vote[1] = ctrl->vote[2] = 1;
         ctrl->abort = 0;
         fence_mbar_init();
@@ -195,7 +196,9 @@ __global__ void __launch_bounds__(192, 1)
                 mma_commit(&ctrl->k_empty[ks]);
                 return true;
             };
-            bool ok = mbar_wait(&ctrl->q_full, 0, wd);
+            // test hook: a wait on a barrier nothing arrives on runs into the watchdog
+            bool ok = p.test_stall ? mbar_wait(&ctrl->never, 0, wd) : true;
+            ok = ok && mbar_wait(&ctrl->q_full, 0, wd);
             if (ok) ok = issue_s(0);
             int npv = 0;
             for (int j = 0; j < n && ok; ++j) {

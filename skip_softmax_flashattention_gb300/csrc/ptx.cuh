@@ -63,16 +63,13 @@ struct Watchdog {
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    uint32_t n = 0;
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((++n & 15u) == 0) {
-            if (*wd.abort_flag) return false;
-            if (globaltimer_ns() - t0 > wd.limit_ns) {
-                *wd.abort_flag = 1;
-                atomicOr(wd.status, kStatusTimeout);
-                return false;
-            }
+        if (*wd.abort_flag) return false;
+        if (globaltimer_ns() - t0 > wd.limit_ns) {
+            *wd.abort_flag = 1;
+            atomicOr(wd.status, kStatusTimeout);
+            return false;
         }
     }
 }
