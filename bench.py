@@ -35,7 +35,8 @@ PREFILL = dict(B=1, Hq=32, Hkv=8, L=16384, d=128)
 DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the current kernels; None until captured for this version of the kernels.
-TRAFFIC_BYTES = {"prefill": None, "decode": None}
+# decode: B=8 capture (1073.9 MB read + 4.3 MB written) x 8 for the B=64 launch.
+TRAFFIC_BYTES = {"prefill": None, "decode": 8 * (1073888000 + 4261888)}
 
 
 def load_peaks():
@@ -399,7 +400,7 @@ def run_ours(args):
                          f"{secs:.1f} s of fp32 oracle time"}
 
     ach = exec_flop / (p_max * 1e-3) / 1e12
-    roof = {"bound": "tensor", "kernel": "prefill_kernel<128,P-in-TMEM>", "achieved": ach,
+    roof = {"bound": "tensor", "kernel": "prefill2_kernel<128> (two query tiles per CTA)", "achieved": ach,
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
             "peak_source": peaks["source"] + " burst bf16",
             "traffic": TRAFFIC_BYTES["prefill"]}

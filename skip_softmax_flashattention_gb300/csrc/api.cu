@@ -104,7 +104,8 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
     if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lkv < 1 || Hq % Hkv != 0) return BLASST_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return BLASST_ERR_INVALID_ARG;
     if (!scale_ok(scale) || !lambda_ok(lambda)) return BLASST_ERR_INVALID_ARG;
-    const unsigned known = BLASST_PREFILL_ELIDE_V | BLASST_PREFILL_P_VIA_SMEM | BLASST_FLAG_TEST_SHORT_WATCHDOG;
+    const unsigned known = BLASST_PREFILL_ELIDE_V | BLASST_PREFILL_P_VIA_SMEM | BLASST_PREFILL_ONE_QTILE |
+                           BLASST_FLAG_TEST_SHORT_WATCHDOG;
     if (flags & ~known) return BLASST_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
     if (flags & BLASST_PREFILL_ELIDE_V) return BLASST_ERR_UNSUPPORTED;
@@ -147,8 +148,10 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
     p.watchdog_ns = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? kShortWatchdogNs : kWatchdogNs;
     p.elide_v = 0;
     p.test_stall = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? 1 : 0;
-    const bool p_in_tmem = (flags & BLASST_PREFILL_P_VIA_SMEM) == 0;
-    return cuda_status(blasst::launch_prefill(tq, tk, tv, p, d, p_in_tmem, st));
+    const blasst::PrefillVariant var = (flags & BLASST_PREFILL_P_VIA_SMEM) ? blasst::PrefillVariant::kOneTilePSmem
+                                       : (flags & BLASST_PREFILL_ONE_QTILE) ? blasst::PrefillVariant::kOneTilePTmem
+                                                                            : blasst::PrefillVariant::kTwoTiles;
+    return cuda_status(blasst::launch_prefill(tq, tk, tv, p, d, var, st));
 }
 
 int blasst_decode_num_splits(int B, int Hq, int Hkv, int Lkv, int d, int requested, int* out) {

@@ -51,14 +51,18 @@ struct CombineParams {
     int B, Hq, S, d;
 };
 
+// Prefill kernel variants (identical results):
+//   kTwoTiles       two 128-row query tiles per CTA, P in TMEM (default)
+//   kOneTilePTmem   one query tile per CTA, S double-buffered, P in TMEM
+//   kOneTilePSmem   one query tile per CTA, S double-buffered, P staged in shared memory
+enum class PrefillVariant { kTwoTiles, kOneTilePTmem, kOneTilePSmem };
+
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int d, bool p_in_tmem, cudaStream_t stream);
+                           const PrefillParams& p, int d, PrefillVariant v, cudaStream_t stream);
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int d,
                           cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 
-size_t prefill_smem_bytes(int d, bool p_in_tmem);
-size_t decode_smem_bytes(int d);
 
 }  // namespace blasst

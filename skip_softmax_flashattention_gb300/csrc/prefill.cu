@@ -410,6 +410,384 @@ __global__ void __launch_bounds__(192, 1)
     }
 }
 
+// ============================================================================
+// Two query tiles per CTA (the default path).
+//
+// The CTA owns query tiles A = 2i and B = 2i+1 of one head; each K/V tile is
+// staged once and used by both.  Warps 0-3 run the softmax of tile A, warps 4-7
+// that of tile B, warp 8 is the TMA producer, warp 9 the MMA issuer (warps 10-11
+// only complete the third warpgroup, whose registers move to the softmax
+// warpgroups: 168 per thread at launch, 72 for warpgroup 2 and 216 for the
+// softmax warpgroups afterwards -- 2*128*216 + 128*72 = 384*168).  TMEM:
+// S_A = [0,128), S_B = [128,256), O_A = [256, 256+D), O_B = [256+D, 256+2D);
+// P_w overwrites the first 64 columns of S_w.  The tensor core runs, per key
+// tile j:  ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...  so the softmax of one
+// tile runs while the tensor core works on the other tile.
+// ============================================================================
+template <int NK, int NV>
+struct Prefill2Ctrl {
+    uint64_t q_full;
+    uint64_t k_full[NK], k_empty[NK];
+    uint64_t v_full[NV], v_empty[NV];
+    uint64_t s_full[2], p_full[2], o_done[2];
+    uint64_t drain, never;
+    uint32_t tmem_base;
+    int vote[2][3];
+    int dec[2];
+    int abort;
+    float mred[2][2][4];
+};
+
+template <int D>
+struct Prefill2Cfg {
+    static constexpr int TILE_BYTES = kTile * D * 2;
+    static constexpr int BOX_BYTES = kTile * 128;
+    static constexpr int NK = (D == 128) ? 3 : 4;
+    static constexpr int NV = (D == 128) ? 2 : 4;
+    static constexpr int OFF_Q = 0;  // Q_A, then Q_B
+    static constexpr int OFF_K = 2 * TILE_BYTES;
+    static constexpr int OFF_V = OFF_K + NK * TILE_BYTES;
+    static constexpr int OFF_CTRL = OFF_V + NV * TILE_BYTES;
+    using Ctrl = Prefill2Ctrl<NK, NV>;
+    static constexpr int SMEM = OFF_CTRL + (int)sizeof(Ctrl) + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t O_COL = 256;
+};
+
+constexpr int kRegsLaunch2 = 168, kRegsSoftmax2 = 216, kRegsProducer2 = 72;
+static_assert(2 * 128 * kRegsSoftmax2 + 128 * kRegsProducer2 <= 384 * kRegsLaunch2, "register split");
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    prefill2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
+    using C = Prefill2Cfg<D>;
+    using Ctrl = typename C::Ctrl;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    Ctrl* ctrl = reinterpret_cast<Ctrl*>(smem + C::OFF_CTRL);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    const int G = p.Hq / p.Hkv;
+    const int npairs = (p.nQ + 1) >> 1;
+    const int pi = p.causal ? (npairs - 1 - (int)blockIdx.x) : (int)blockIdx.x;  // heavy pairs first
+    const int h = blockIdx.y, b = blockIdx.z, hk = h / G;
+    const int off = p.Lkv - p.Lq;
+    int nvis[2];
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const int qt = 2 * pi + w;
+        if (qt >= p.nQ) {
+            nvis[w] = 0;
+        } else if (p.causal) {
+            const int maxkey = min(p.Lq, (qt + 1) * kTile) - 1 + off;
+            nvis[w] = maxkey < 0 ? 0 : min(p.nK, maxkey / kTile + 1);
+        } else {
+            nvis[w] = p.nK;
+        }
+    }
+    const int N = max(nvis[0], nvis[1]);
+
+    if (tid == 0) {
+        mbar_init(&ctrl->q_full, 1);
+        for (int i = 0; i < C::NK; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
+        for (int i = 0; i < C::NV; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
+        for (int w = 0; w < 2; ++w) {
+            mbar_init(&ctrl->s_full[w], 1);
+            mbar_init(&ctrl->p_full[w], 4);
+            mbar_init(&ctrl->o_done[w], 1);
+            ctrl->vote[w][0] = ctrl->vote[w][1] = ctrl->vote[w][2] = 1;
+        }
+        mbar_init(&ctrl->drain, 1);
+        mbar_init(&ctrl->never, 1);
+        ctrl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(&ctrl->tmem_base, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    const Watchdog wd{&ctrl->abort, p.status, p.watchdog_ns};
+    if (warp >= 8) {
+      regs_dec<kRegsProducer2>();
+      if (warp == 8) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0 && N > 0) {
+            tma_prefetch_desc(&tq);
+            tma_prefetch_desc(&tk);
+            tma_prefetch_desc(&tv);
+            const int zq = b * p.Hq + h, zkv = b * p.Hkv + hk;
+            const int nq = (nvis[0] > 0) + (nvis[1] > 0);
+            mbar_arrive_expect_tx(&ctrl->q_full, nq * C::TILE_BYTES);
+#pragma unroll
+            for (int w = 0; w < 2; ++w) {
+                if (nvis[w] == 0) continue;
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(smem + C::OFF_Q + w * C::TILE_BYTES + x * C::BOX_BYTES, &tq, &ctrl->q_full, x * 64,
+                                (2 * pi + w) * kTile, zq);
+            }
+            int issued_k = 0, issued_v = 0;
+            for (int j = 0; j < N; ++j) {
+                const int ks = j % C::NK;
+                if (j >= C::NK && !mbar_wait(&ctrl->k_empty[ks], ((j / C::NK) - 1) & 1, wd)) break;
+                mbar_arrive_expect_tx(&ctrl->k_full[ks], C::TILE_BYTES);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(smem + C::OFF_K + ks * C::TILE_BYTES + x * C::BOX_BYTES, &tk, &ctrl->k_full[ks],
+                                x * 64, j * kTile, zkv);
+                issued_k = j + 1;
+                const int vs = j % C::NV;
+                if (j >= C::NV && !mbar_wait(&ctrl->v_empty[vs], ((j / C::NV) - 1) & 1, wd)) break;
+                mbar_arrive_expect_tx(&ctrl->v_full[vs], C::TILE_BYTES);
+#pragma unroll
+                for (int x = 0; x < D / 64; ++x)
+                    tma_load_3d(smem + C::OFF_V + vs * C::TILE_BYTES + x * C::BOX_BYTES, &tv, &ctrl->v_full[vs],
+                                x * 64, j * kTile, zkv);
+                issued_v = j + 1;
+            }
+            mbar_wait_drain(&ctrl->q_full, 0, kDrainNs);
+            for (int j = max(0, issued_k - C::NK); j < issued_k; ++j)
+                mbar_wait_drain(&ctrl->k_full[j % C::NK], (j / C::NK) & 1, kDrainNs);
+            for (int j = max(0, issued_v - C::NV); j < issued_v; ++j)
+                mbar_wait_drain(&ctrl->v_full[j % C::NV], (j / C::NV) & 1, kDrainNs);
+        }
+    } else if (warp == 9) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0 && N > 0) {
+            constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
+            constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
+            const uint32_t sQ = smem_u32(smem + C::OFF_Q);
+            const uint32_t sK = smem_u32(smem + C::OFF_K);
+            const uint32_t sV = smem_u32(smem + C::OFF_V);
+            auto issue_qk = [&](int w, int j) {
+                const uint32_t qb = sQ + w * C::TILE_BYTES;
+                const uint32_t kb = sK + (j % C::NK) * C::TILE_BYTES;
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t o = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
+                    mma_ss(tmem + (uint32_t)w * 128u, desc_kmajor_sw128(qb + o), desc_kmajor_sw128(kb + o), kIdescS,
+                           kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&ctrl->s_full[w]);
+            };
+            bool ok = p.test_stall ? mbar_wait(&ctrl->never, 0, wd) : true;
+            ok = ok && mbar_wait(&ctrl->q_full, 0, wd);
+            ok = ok && mbar_wait(&ctrl->k_full[0], 0, wd);
+            if (ok) {
+                tc_fence_after();
+                if (nvis[0] > 0) issue_qk(0, 0);
+                if (nvis[1] > 0) issue_qk(1, 0);
+                mma_commit(&ctrl->k_empty[0]);
+            }
+            int npv[2] = {0, 0};
+            for (int j = 0; j < N && ok; ++j) {
+                bool v_ready = false, k_ready = false, any_pv = false;
+                const int vs = j % C::NV;
+#pragma unroll
+                for (int w = 0; w < 2; ++w) {
+                    if (j >= nvis[w]) continue;
+                    if (!(ok = mbar_wait(&ctrl->p_full[w], j & 1, wd))) break;
+                    tc_fence_after();
+                    const bool skip = reinterpret_cast<volatile int*>(ctrl->dec)[w] != 0;
+                    if (!skip) {
+                        if (!v_ready) {
+                            if (!(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
+                            tc_fence_after();
+                            v_ready = true;
+                        }
+                        const uint32_t vb = sV + vs * C::TILE_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < kTile / 16; ++kk) {
+                            const uint64_t bdesc = desc_mnmajor_sw128(vb + kk * 2048, C::BOX_BYTES);
+                            mma_ts(tmem + C::O_COL + (uint32_t)w * D, tmem + (uint32_t)w * 128u + kk * 8, bdesc,
+                                   kIdescO, (npv[w] > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        mma_commit(&ctrl->o_done[w]);
+                        ++npv[w];
+                        any_pv = true;
+                    }
+                    if (j + 1 < nvis[w]) {
+                        if (!k_ready) {
+                            const int ks = (j + 1) % C::NK;
+                            if (!(ok = mbar_wait(&ctrl->k_full[ks], ((j + 1) / C::NK) & 1, wd))) break;
+                            tc_fence_after();
+                            k_ready = true;
+                        }
+                        issue_qk(w, j + 1);
+                    }
+                }
+                if (!ok) break;
+                if (k_ready) mma_commit(&ctrl->k_empty[(j + 1) % C::NK]);
+                if (any_pv) {
+                    mma_commit(&ctrl->v_empty[vs]);
+                } else {
+                    if (!v_ready && !(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
+                    mbar_arrive(&ctrl->v_empty[vs]);
+                }
+            }
+            mma_commit(&ctrl->drain);
+            mbar_wait_drain(&ctrl->drain, 0, kDrainNs);
+        }
+      }
+    } else {
+        // ------------------------------------------------------------ softmax (WG 0: tile A, WG 1: tile B)
+        regs_inc<kRegsSoftmax2>();
+        const int w = warp >> 2;
+        const int t = tid & 127;
+        const int qt = 2 * pi + w;
+        const int n = nvis[w];
+        const int rabs = qt * kTile + t;
+        const bool valid = rabs < p.Lq;
+        const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+        const uint32_t s_col = (uint32_t)w * 128u;
+        const uint32_t o_col = C::O_COL + (uint32_t)w * D;
+        const int lim_row = p.causal ? rabs + off : 0x3fffffff;
+        const long long mapbase = ((long long)(b * p.Hq + h) * p.nQ + qt) * p.nK;
+        float m_exact = -CUDART_INF_F, m_ref = -CUDART_INF_F, l = 0.f;
+        int npv = 0;
+        unsigned long long nskip = 0;
+        int* vote = ctrl->vote[w];
+
+        for (int j = 0; j < n; ++j) {
+            mbar_wait(&ctrl->s_full[w], j & 1, wd);
+            tc_fence_after();
+            uint32_t xr[128];
+            tmem_ld32(tl + s_col + 0, xr);
+            tmem_ld32(tl + s_col + 32, xr + 32);
+            tmem_ld32(tl + s_col + 64, xr + 64);
+            tmem_ld32(tl + s_col + 96, xr + 96);
+            tmem_ld_wait();
+            fence_regs<128>(xr);
+            const int lim = min(p.Lkv - 1, lim_row) - j * kTile;
+            if (lim < kTile - 1) {
+#pragma unroll
+                for (int c = 0; c < kTile; ++c)
+                    if (c > lim) xr[c] = __float_as_uint(-CUDART_INF_F);
+            }
+            const float mt = row_max128(xr);
+            const float mnew = fmaxf(m_exact, mt);
+            const float diff = mt - mnew;
+            const bool vote_skip = !valid || (diff < p.thr_raw);
+            const unsigned all = __all_sync(0xffffffffu, vote_skip);
+            if (lane == 0) atomicAnd(&vote[j % 3], (int)all);
+            if (p.margins) {
+                float g = valid ? ((mt == -CUDART_INF_F && mnew == -CUDART_INF_F) ? CUDART_INF_F : diff)
+                                : -CUDART_INF_F;
+#pragma unroll
+                for (int sh = 16; sh > 0; sh >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, sh));
+                if (lane == 0) ctrl->mred[w][j & 1][warp & 3] = g;
+            }
+            named_bar_sync(1 + w, 128);
+            const bool skip = reinterpret_cast<volatile int*>(vote)[j % 3] != 0;
+            if (t == 0) {
+                vote[(j + 2) % 3] = 1;
+                reinterpret_cast<volatile int*>(ctrl->dec)[w] = skip ? 1 : 0;
+                if (p.skip_map) p.skip_map[mapbase + j] = skip ? 1 : 0;
+                if (p.margins) {
+                    const volatile float* mr = ctrl->mred[w][j & 1];
+                    p.margins[mapbase + j] = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * p.scale;
+                }
+                nskip += skip ? 1 : 0;
+            }
+            m_exact = mnew;
+            if (!skip) {
+                const bool move = mnew != -CUDART_INF_F && (m_ref == -CUDART_INF_F || mnew > m_ref + p.lazy_raw);
+                const float alpha = move ? (m_ref == -CUDART_INF_F ? 0.f : ex2((m_ref - mnew) * p.c_log2)) : 1.f;
+                if (__any_sync(0xffffffffu, move) && npv > 0) {
+                    mbar_wait(&ctrl->o_done[w], (npv - 1) & 1, wd);
+                    tc_fence_after();
+#pragma unroll
+                    for (int cc = 0; cc < D; cc += 32) {
+                        uint32_t tt[32];
+                        tmem_ld32(tl + o_col + cc, tt);
+                        tmem_ld_wait();
+                        fence_regs<32>(tt);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) tt[i] = __float_as_uint(__uint_as_float(tt[i]) * alpha);
+                        tmem_st32(tl + o_col + cc, tt);
+                    }
+                    tmem_st_wait();
+                }
+                if (move) {
+                    l *= alpha;
+                    m_ref = mnew;
+                }
+                const float mc = (m_ref == -CUDART_INF_F ? 0.f : m_ref) * p.c_log2;
+                float rs = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t pk[16];
+                    rs += exp_pack32(xr + ch * 32, p.c_log2, mc, pk);
+                    tmem_st16(tl + s_col + ch * 16, pk);
+                }
+                l += rs;
+                ++npv;
+                tmem_st_wait();
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->p_full[w]);
+        }
+
+        if (npv > 0) {
+            mbar_wait(&ctrl->o_done[w], (npv - 1) & 1, wd);
+            tc_fence_after();
+        }
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        uint16_t* orow = reinterpret_cast<uint16_t*>(p.o) + ((long long)(b * p.Hq + h) * p.Lq + rabs) * D;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+            uint32_t tt[32];
+            if (npv > 0) {
+                tmem_ld32(tl + o_col + cc, tt);
+                tmem_ld_wait();
+                fence_regs<32>(tt);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) tt[i] = 0u;
+            }
+            if (valid) {
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 v4;
+                    v4.x = pack_bf16x2(__uint_as_float(tt[q4 * 8 + 0]) * inv, __uint_as_float(tt[q4 * 8 + 1]) * inv);
+                    v4.y = pack_bf16x2(__uint_as_float(tt[q4 * 8 + 2]) * inv, __uint_as_float(tt[q4 * 8 + 3]) * inv);
+                    v4.z = pack_bf16x2(__uint_as_float(tt[q4 * 8 + 4]) * inv, __uint_as_float(tt[q4 * 8 + 5]) * inv);
+                    v4.w = pack_bf16x2(__uint_as_float(tt[q4 * 8 + 6]) * inv, __uint_as_float(tt[q4 * 8 + 7]) * inv);
+                    *reinterpret_cast<uint4*>(orow + cc + q4 * 8) = v4;
+                }
+            }
+        }
+        if (valid && p.lse)
+            p.lse[(long long)(b * p.Hq + h) * p.Lq + rabs] = l > 0.f ? m_ref * p.scale + __logf(l) : -CUDART_INF_F;
+        if (t == 0 && p.skipped && nskip) atomicAdd(p.skipped, nskip);
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::TMEM_COLS);
+    }
+}
+
+template <int D>
+cudaError_t launch2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
+                      cudaStream_t stream) {
+    using C = Prefill2Cfg<D>;
+    cudaError_t e = cudaFuncSetAttribute(prefill2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid((p.nQ + 1) / 2, p.Hq, p.B);
+    prefill2_kernel<D><<<grid, 384, C::SMEM, stream>>>(tq, tk, tv, p);
+    return cudaGetLastError();
+}
+
 template <int D, bool PT>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                      cudaStream_t stream) {
@@ -424,14 +802,15 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                           const PrefillParams& p, int d, bool p_in_tmem, cudaStream_t stream) {
-    if (d == 128) return p_in_tmem ? launch_t<128, true>(tq, tk, tv, p, stream) : launch_t<128, false>(tq, tk, tv, p, stream);
-    return p_in_tmem ? launch_t<64, true>(tq, tk, tv, p, stream) : launch_t<64, false>(tq, tk, tv, p, stream);
-}
-
-size_t prefill_smem_bytes(int d, bool p_in_tmem) {
-    if (d == 128) return p_in_tmem ? PrefillCfg<128, true>::SMEM : PrefillCfg<128, false>::SMEM;
-    return p_in_tmem ? PrefillCfg<64, true>::SMEM : PrefillCfg<64, false>::SMEM;
+                           const PrefillParams& p, int d, PrefillVariant v, cudaStream_t stream) {
+    switch (v) {
+        case PrefillVariant::kTwoTiles:
+            return d == 128 ? launch2_t<128>(tq, tk, tv, p, stream) : launch2_t<64>(tq, tk, tv, p, stream);
+        case PrefillVariant::kOneTilePTmem:
+            return d == 128 ? launch_t<128, true>(tq, tk, tv, p, stream) : launch_t<64, true>(tq, tk, tv, p, stream);
+        default:
+            return d == 128 ? launch_t<128, false>(tq, tk, tv, p, stream) : launch_t<64, false>(tq, tk, tv, p, stream);
+    }
 }
 
 }  // namespace blasst

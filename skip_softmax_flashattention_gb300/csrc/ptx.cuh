@@ -95,6 +95,15 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// Per-warpgroup register budget moves (all four warps of a warpgroup execute them).
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -258,6 +267,59 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+// Three-input maximum (one instruction on sm_100+).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// (d0, d1) = (a0, a1) * b + c on the packed two-wide fp32 path.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %5};\n\t"
+        "fma.rn.ftz.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (s0, s1) += (a0, a1) on the packed two-wide fp32 path.
+__device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float a1) {
+    asm("{\n\t.reg .b64 ra, rs;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rs, {%0, %1};\n\t"
+        "add.rn.ftz.f32x2 rs, rs, ra;\n\tmov.b64 {%0, %1}, rs;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "f"(a0), "f"(a1));
+}
+
+// Maximum of 128 fp32 values held as raw bits, as a shallow tree of 3-input maxima.
+__device__ __forceinline__ float row_max128(const uint32_t* x) {
+    float m[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float* f = reinterpret_cast<const float*>(x + 8 * i);
+        m[i] = fmax3(fmax3(f[0], f[1], f[2]), fmax3(f[3], f[4], f[5]), fmaxf(f[6], f[7]));
+    }
+    const float a = fmax3(m[0], m[1], m[2]), b = fmax3(m[3], m[4], m[5]), c = fmax3(m[6], m[7], m[8]);
+    const float d = fmax3(m[9], m[10], m[11]), e = fmax3(m[12], m[13], m[14]);
+    return fmax3(fmax3(a, b, c), fmax3(d, e, m[15]), a);
+}
+
+// For 32 scores x (raw bits): p = 2^(x*c - mc), packed to 16 bf16x2 words in pk;
+// returns the fp32 sum of the 32 p values (four independent partial sums).
+__device__ __forceinline__ float exp_pack32(const uint32_t* x, float c, float mc, uint32_t* pk) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float a0, a1;
+        ffma2(a0, a1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), c, -mc);
+        const float p0 = ex2(a0), p1 = ex2(a1);
+        pk[i] = pack_bf16x2(p0, p1);
+        if (i & 1)
+            fadd2_acc(s2, s3, p0, p1);
+        else
+            fadd2_acc(s0, s1, p0, p1);
+    }
+    return (s0 + s1) + (s2 + s3);
 }
 
 }  // namespace blasst
