@@ -62,6 +62,7 @@ extern "C" {
 #define BLASST_PREFILL_ELIDE_V 0x1u      /* also skip the V tile load of skipped tiles (not in this build: UNSUPPORTED) */
 #define BLASST_PREFILL_P_VIA_SMEM 0x2u   /* one query tile per CTA, P staged in shared memory (results identical) */
 #define BLASST_PREFILL_ONE_QTILE 0x4u    /* one query tile per CTA, P in tensor memory (results identical) */
+#define BLASST_PREFILL_WIDE 0x8u         /* two query tiles per CTA, two softmax threads per row (results identical) */
 #define BLASST_FLAG_TEST_SHORT_WATCHDOG 0x80000000u /* test only: waits give up after 200 us and the MMA issuer
                                                        first waits on a barrier nothing arrives on, so the call
                                                        always ends in BLASST_ERR_TIMEOUT (outputs invalid) */
@@ -92,8 +93,9 @@ int blasst_prefill(const void* q, const void* k, const void* v, void* o, float* 
  *              (m~ - m) in scaled-score units (+inf when a row has no visible key
  *              yet, NaN for tiles not visited).  lambda-independent for lambda <= 1;
  *              a tile is skipped iff margin < ln(lambda).
- *   flags      BLASST_PREFILL_P_VIA_SMEM, BLASST_PREFILL_ONE_QTILE (kernel variants with
- *              identical results; default: two query tiles per CTA), BLASST_FLAG_TEST_SHORT_WATCHDOG;
+ *   flags      BLASST_PREFILL_P_VIA_SMEM, BLASST_PREFILL_ONE_QTILE, BLASST_PREFILL_WIDE
+ *              (kernel variants with identical results; default: two query tiles per CTA,
+ *              one softmax thread per query row), BLASST_FLAG_TEST_SHORT_WATCHDOG;
  *              BLASST_PREFILL_ELIDE_V is reserved and returns BLASST_ERR_UNSUPPORTED.
  */
 int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,

@@ -28,6 +28,7 @@ BLASST_ERR_NO_CALIBRATION = -6
 BLASST_PREFILL_ELIDE_V = 0x1
 BLASST_PREFILL_P_VIA_SMEM = 0x2
 BLASST_PREFILL_ONE_QTILE = 0x4
+BLASST_PREFILL_WIDE = 0x8
 BLASST_FLAG_TEST_SHORT_WATCHDOG = 0x80000000
 
 _lib = None

@@ -105,7 +105,7 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
     if (causal != 0 && causal != 1) return BLASST_ERR_INVALID_ARG;
     if (!scale_ok(scale) || !lambda_ok(lambda)) return BLASST_ERR_INVALID_ARG;
     const unsigned known = BLASST_PREFILL_ELIDE_V | BLASST_PREFILL_P_VIA_SMEM | BLASST_PREFILL_ONE_QTILE |
-                           BLASST_FLAG_TEST_SHORT_WATCHDOG;
+                           BLASST_PREFILL_WIDE | BLASST_FLAG_TEST_SHORT_WATCHDOG;
     if (flags & ~known) return BLASST_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
     if (flags & BLASST_PREFILL_ELIDE_V) return BLASST_ERR_UNSUPPORTED;
@@ -150,6 +150,7 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
     p.test_stall = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? 1 : 0;
     const blasst::PrefillVariant var = (flags & BLASST_PREFILL_P_VIA_SMEM) ? blasst::PrefillVariant::kOneTilePSmem
                                        : (flags & BLASST_PREFILL_ONE_QTILE) ? blasst::PrefillVariant::kOneTilePTmem
+                                       : (flags & BLASST_PREFILL_WIDE)      ? blasst::PrefillVariant::kWide
                                                                             : blasst::PrefillVariant::kTwoTiles;
     return cuda_status(blasst::launch_prefill(tq, tk, tv, p, d, var, st));
 }
@@ -298,6 +299,7 @@ int blasst_device_status(int clear) {
         const int zero = 0;
         if (cudaMemcpyToSymbol(g_blasst_status, &zero, sizeof(int)) != cudaSuccess) return BLASST_ERR_CUDA;
     }
+    if (v & 2) return BLASST_ERR_CUDA;  // a kernel found its shared memory misaligned
     return v ? BLASST_ERR_TIMEOUT : BLASST_OK;
 }
 

@@ -52,14 +52,17 @@ struct CombineParams {
 };
 
 // Prefill kernel variants (identical results):
-//   kTwoTiles       two 128-row query tiles per CTA, P in TMEM (default)
+//   kTwoTiles       two 128-row query tiles per CTA, one softmax thread per row (default)
+//   kWide           two 128-row query tiles per CTA, two softmax threads per row
 //   kOneTilePTmem   one query tile per CTA, S double-buffered, P in TMEM
 //   kOneTilePSmem   one query tile per CTA, S double-buffered, P staged in shared memory
-enum class PrefillVariant { kTwoTiles, kOneTilePTmem, kOneTilePSmem };
+enum class PrefillVariant { kWide, kTwoTiles, kOneTilePTmem, kOneTilePSmem };
 
 // Launchers (return a cudaError_t from the launch).
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int d, PrefillVariant v, cudaStream_t stream);
+cudaError_t launch_prefill_wide(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                const PrefillParams& p, int d, cudaStream_t stream);
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int d,
                           cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);

@@ -39,6 +39,16 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 
+// Tile-vote reduction of the two-query-tile kernel: 0 = warp vote + shared-memory
+// atomicAnd + named barrier, 1 = barrier with AND reduction.
+#ifndef BLASST_VOTE_BARRIER_RED
+#define BLASST_VOTE_BARRIER_RED 0
+#endif
+// 2^x of the two-query-tile kernel: 0 = fp32 ex2 per element, 1 = bf16x2 ex2 per pair.
+#ifndef BLASST_EXP_BF16X2
+#define BLASST_EXP_BF16X2 0
+#endif
+
 namespace blasst {
 namespace {
 
@@ -415,26 +425,32 @@ __global__ void __launch_bounds__(192, 1)
 //
 // The CTA owns query tiles A = 2i and B = 2i+1 of one head; each K/V tile is
 // staged once and used by both.  Warps 0-3 run the softmax of tile A, warps 4-7
-// that of tile B, warp 8 is the TMA producer, warp 9 the MMA issuer (warps 10-11
-// only complete the third warpgroup, whose registers move to the softmax
+// that of tile B, warp 8 is the TMA producer, warps 9 and 10 issue the MMAs of
+// tiles A and B (one thread each, so that one issuer's barrier waits overlap the
+// other's MMAs; warp 11 only completes the third warpgroup, whose registers move to the softmax
 // warpgroups: 168 per thread at launch, 72 for warpgroup 2 and 216 for the
 // softmax warpgroups afterwards -- 2*128*216 + 128*72 = 384*168).  TMEM:
 // S_A = [0,128), S_B = [128,256), O_A = [256, 256+D), O_B = [256+D, 256+2D);
 // P_w overwrites the first 64 columns of S_w.  The tensor core runs, per key
 // tile j:  ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...  so the softmax of one
-// tile runs while the tensor core works on the other tile.
+// tile runs while the tensor core works on the other tile.  Each issuer releases
+// K/V slots on its own barriers, always through tcgen05.commit, so its releases
+// stay ordered behind its MMAs; the producer waits only for the issuers whose
+// tile read the previous occupant of a slot.
 // ============================================================================
 template <int NK, int NV>
 struct Prefill2Ctrl {
     uint64_t q_full;
-    uint64_t k_full[NK], k_empty[NK];
-    uint64_t v_full[NV], v_empty[NV];
-    uint64_t s_full[2], p_full[2], o_done[2];
-    uint64_t drain, never;
+    uint64_t k_full[NK], v_full[NV];
+    uint64_t k_empty[2][NK], v_empty[2][NV];      // released by the MMA issuer of query tile w
+    uint64_t s_full[2], p_full[2][2], o_done[2];  // p_full[w][h]: half h (keys 64h..64h+63) of P_w stored
+    uint64_t drain[2], never;
     uint32_t tmem_base;
     int vote[2][3];
     int dec[2];
     int abort;
+    int turn;       // which issuer may put its next group of MMAs into the tensor queue
+    int active[2];  // issuer w still has key tiles to process
     float mred[2][2][4];
 };
 
@@ -490,17 +506,30 @@ __global__ void __launch_bounds__(384, 1)
 
     if (tid == 0) {
         mbar_init(&ctrl->q_full, 1);
-        for (int i = 0; i < C::NK; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
-        for (int i = 0; i < C::NV; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
+        for (int i = 0; i < C::NK; ++i) {
+            mbar_init(&ctrl->k_full[i], 1);
+            mbar_init(&ctrl->k_empty[0][i], 1);
+            mbar_init(&ctrl->k_empty[1][i], 1);
+        }
+        for (int i = 0; i < C::NV; ++i) {
+            mbar_init(&ctrl->v_full[i], 1);
+            mbar_init(&ctrl->v_empty[0][i], 1);
+            mbar_init(&ctrl->v_empty[1][i], 1);
+        }
         for (int w = 0; w < 2; ++w) {
             mbar_init(&ctrl->s_full[w], 1);
-            mbar_init(&ctrl->p_full[w], 4);
+            mbar_init(&ctrl->p_full[w][0], 4);
+            mbar_init(&ctrl->p_full[w][1], 4);
             mbar_init(&ctrl->o_done[w], 1);
             ctrl->vote[w][0] = ctrl->vote[w][1] = ctrl->vote[w][2] = 1;
         }
-        mbar_init(&ctrl->drain, 1);
+        mbar_init(&ctrl->drain[0], 1);
+        mbar_init(&ctrl->drain[1], 1);
         mbar_init(&ctrl->never, 1);
         ctrl->abort = 0;
+        ctrl->turn = nvis[0] > 0 ? 0 : 1;
+        ctrl->active[0] = nvis[0] > 0;
+        ctrl->active[1] = nvis[1] > 0;
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -531,10 +560,17 @@ __global__ void __launch_bounds__(384, 1)
                     tma_load_3d(smem + C::OFF_Q + w * C::TILE_BYTES + x * C::BOX_BYTES, &tq, &ctrl->q_full, x * 64,
                                 (2 * pi + w) * kTile, zq);
             }
+            // A slot is reused once every query tile that read its previous occupant released it.
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < N; ++j) {
                 const int ks = j % C::NK;
-                if (j >= C::NK && !mbar_wait(&ctrl->k_empty[ks], ((j / C::NK) - 1) & 1, wd)) break;
+                bool okk = true;
+                if (j >= C::NK) {
+                    const int prev = j - C::NK;
+                    for (int w = 0; w < 2 && okk; ++w)
+                        if (prev < nvis[w]) okk = mbar_wait(&ctrl->k_empty[w][ks], (prev / C::NK) & 1, wd);
+                }
+                if (!okk) break;
                 mbar_arrive_expect_tx(&ctrl->k_full[ks], C::TILE_BYTES);
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x)
@@ -542,7 +578,13 @@ __global__ void __launch_bounds__(384, 1)
                                 x * 64, j * kTile, zkv);
                 issued_k = j + 1;
                 const int vs = j % C::NV;
-                if (j >= C::NV && !mbar_wait(&ctrl->v_empty[vs], ((j / C::NV) - 1) & 1, wd)) break;
+                bool okv = true;
+                if (j >= C::NV) {
+                    const int prev = j - C::NV;
+                    for (int w = 0; w < 2 && okv; ++w)
+                        if (prev < nvis[w]) okv = mbar_wait(&ctrl->v_empty[w][vs], (prev / C::NV) & 1, wd);
+                }
+                if (!okv) break;
                 mbar_arrive_expect_tx(&ctrl->v_full[vs], C::TILE_BYTES);
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x)
@@ -556,82 +598,89 @@ __global__ void __launch_bounds__(384, 1)
             for (int j = max(0, issued_v - C::NV); j < issued_v; ++j)
                 mbar_wait_drain(&ctrl->v_full[j % C::NV], (j / C::NV) & 1, kDrainNs);
         }
-    } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0 && N > 0) {
+    } else if (warp == 9 || warp == 10) {
+        // ------------------------------------------------------------ MMA issuers (warp 9: tile A, warp 10: tile B)
+        const int w = warp - 9;
+        const int n = nvis[w];
+        if (lane == 0 && n > 0) {
             constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
             constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
-            const uint32_t sQ = smem_u32(smem + C::OFF_Q);
-            const uint32_t sK = smem_u32(smem + C::OFF_K);
-            const uint32_t sV = smem_u32(smem + C::OFF_V);
-            auto issue_qk = [&](int w, int j) {
-                const uint32_t qb = sQ + w * C::TILE_BYTES;
-                const uint32_t kb = sK + (j % C::NK) * C::TILE_BYTES;
+            constexpr uint32_t kTileLo = C::TILE_BYTES >> 4;
+            // low descriptor words of the operand bases (offsets within a tile are added per k-step)
+            const uint32_t qlo = desc_lo(smem_u32(smem + C::OFF_Q + w * C::TILE_BYTES), 16);
+            const uint32_t klo = desc_lo(smem_u32(smem + C::OFF_K), 16);
+            const uint32_t vlo = desc_lo(smem_u32(smem + C::OFF_V), C::BOX_BYTES);
+            const uint32_t s_t = tmem + (uint32_t)w * 128u;
+            const uint32_t o_t = tmem + C::O_COL + (uint32_t)w * D;
+            auto issue_qk = [&](int j) {
+                const uint32_t b0 = klo + (uint32_t)(j % C::NK) * kTileLo;
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t o = (kk >> 2) * C::BOX_BYTES + (kk & 3) * 32;
-                    mma_ss(tmem + (uint32_t)w * 128u, desc_kmajor_sw128(qb + o), desc_kmajor_sw128(kb + o), kIdescS,
-                           kk > 0 ? 1u : 0u);
+                    const uint32_t o = ((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4;
+                    mma_ss_split(s_t, qlo + o, b0 + o, kIdescS, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&ctrl->s_full[w]);
+                mma_commit(&ctrl->k_empty[w][j % C::NK]);
             };
-            bool ok = p.test_stall ? mbar_wait(&ctrl->never, 0, wd) : true;
+            auto issue_pv_half = [&](int vs, int half, bool first) {
+                const uint32_t b0 = vlo + (uint32_t)vs * kTileLo;
+#pragma unroll
+                for (int k4 = 0; k4 < 4; ++k4) {
+                    const int kk = half * 4 + k4;
+                    mma_ts_split(o_t, s_t + kk * 8, b0 + ((kk * 2048) >> 4), kIdescO, (!first || kk > 0) ? 1u : 0u);
+                }
+            };
+            bool ok = (p.test_stall && w == 0) ? mbar_wait(&ctrl->never, 0, wd) : true;
             ok = ok && mbar_wait(&ctrl->q_full, 0, wd);
             ok = ok && mbar_wait(&ctrl->k_full[0], 0, wd);
             if (ok) {
                 tc_fence_after();
-                if (nvis[0] > 0) issue_qk(0, 0);
-                if (nvis[1] > 0) issue_qk(1, 0);
-                mma_commit(&ctrl->k_empty[0]);
+                issue_qk(0);
             }
-            int npv[2] = {0, 0};
-            for (int j = 0; j < N && ok; ++j) {
-                bool v_ready = false, k_ready = false, any_pv = false;
+            volatile int* turn = &ctrl->turn;
+            volatile int* active = ctrl->active;
+            // The two issuers alternate groups (PV_w(j) + QK_w(j+1)) so that the tensor
+            // queue runs PV_A, QK_A, PV_B, QK_B, ... and the two softmaxes stay half a
+            // period apart; an issuer waits for its turn only while the other is active.
+            auto take_turn = [&]() -> bool {
+                if (*turn == w || !active[1 - w]) return true;
+                const uint64_t t0 = globaltimer_ns();
+                while (*turn != w && active[1 - w]) {
+                    if (*wd.abort_flag) return false;
+                    if (globaltimer_ns() - t0 > wd.limit_ns) {
+                        *wd.abort_flag = 1;
+                        atomicOr(wd.status, kStatusTimeout);
+                        return false;
+                    }
+                }
+                return true;
+            };
+            int npv = 0;
+            for (int j = 0; j < n && ok; ++j) {
                 const int vs = j % C::NV;
-#pragma unroll
-                for (int w = 0; w < 2; ++w) {
-                    if (j >= nvis[w]) continue;
-                    if (!(ok = mbar_wait(&ctrl->p_full[w], j & 1, wd))) break;
-                    tc_fence_after();
-                    const bool skip = reinterpret_cast<volatile int*>(ctrl->dec)[w] != 0;
-                    if (!skip) {
-                        if (!v_ready) {
-                            if (!(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
-                            tc_fence_after();
-                            v_ready = true;
-                        }
-                        const uint32_t vb = sV + vs * C::TILE_BYTES;
-#pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk) {
-                            const uint64_t bdesc = desc_mnmajor_sw128(vb + kk * 2048, C::BOX_BYTES);
-                            mma_ts(tmem + C::O_COL + (uint32_t)w * D, tmem + (uint32_t)w * 128u + kk * 8, bdesc,
-                                   kIdescO, (npv[w] > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        mma_commit(&ctrl->o_done[w]);
-                        ++npv[w];
-                        any_pv = true;
-                    }
-                    if (j + 1 < nvis[w]) {
-                        if (!k_ready) {
-                            const int ks = (j + 1) % C::NK;
-                            if (!(ok = mbar_wait(&ctrl->k_full[ks], ((j + 1) / C::NK) & 1, wd))) break;
-                            tc_fence_after();
-                            k_ready = true;
-                        }
-                        issue_qk(w, j + 1);
-                    }
+                if (!(ok = mbar_wait(&ctrl->p_full[w][0], j & 1, wd))) break;
+                const bool skip = reinterpret_cast<volatile int*>(ctrl->dec)[w] != 0;
+                // V_j must have landed before its slot is released, also when the tile is skipped
+                if (!(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
+                if (j + 1 < n && !(ok = mbar_wait(&ctrl->k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1, wd))) break;
+                if (!(ok = take_turn())) break;
+                tc_fence_after();
+                if (!skip) issue_pv_half(vs, 0, npv == 0);
+                if (!(ok = mbar_wait(&ctrl->p_full[w][1], j & 1, wd))) break;
+                tc_fence_after();
+                if (!skip) {
+                    issue_pv_half(vs, 1, npv == 0);
+                    mma_commit(&ctrl->o_done[w]);
+                    ++npv;
                 }
-                if (!ok) break;
-                if (k_ready) mma_commit(&ctrl->k_empty[(j + 1) % C::NK]);
-                if (any_pv) {
-                    mma_commit(&ctrl->v_empty[vs]);
-                } else {
-                    if (!v_ready && !(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
-                    mbar_arrive(&ctrl->v_empty[vs]);
-                }
+                mma_commit(&ctrl->v_empty[w][vs]);
+                if (j + 1 < n) issue_qk(j + 1);
+                *turn = 1 - w;
             }
-            mma_commit(&ctrl->drain);
-            mbar_wait_drain(&ctrl->drain, 0, kDrainNs);
+            active[w] = 0;
+            *turn = 1 - w;
+            mma_commit(&ctrl->drain[w]);
+            mbar_wait_drain(&ctrl->drain[w], 0, kDrainNs);
         }
       }
     } else {
@@ -673,8 +722,6 @@ __global__ void __launch_bounds__(384, 1)
             const float mnew = fmaxf(m_exact, mt);
             const float diff = mt - mnew;
             const bool vote_skip = !valid || (diff < p.thr_raw);
-            const unsigned all = __all_sync(0xffffffffu, vote_skip);
-            if (lane == 0) atomicAnd(&vote[j % 3], (int)all);
             if (p.margins) {
                 float g = valid ? ((mt == -CUDART_INF_F && mnew == -CUDART_INF_F) ? CUDART_INF_F : diff)
                                 : -CUDART_INF_F;
@@ -682,8 +729,16 @@ __global__ void __launch_bounds__(384, 1)
                 for (int sh = 16; sh > 0; sh >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, sh));
                 if (lane == 0) ctrl->mred[w][j & 1][warp & 3] = g;
             }
+#if BLASST_VOTE_BARRIER_RED
+            // AND of the 128 row votes, reduced by the barrier itself
+            const bool skip = bar_red_and(1 + w, 128, vote_skip);
+#else
+            // row vote -> warp vote -> one shared-memory atomicAnd per warp -> tile flag
+            const unsigned all = __all_sync(0xffffffffu, vote_skip);
+            if (lane == 0) atomicAnd(&vote[j % 3], (int)all);
             named_bar_sync(1 + w, 128);
             const bool skip = reinterpret_cast<volatile int*>(vote)[j % 3] != 0;
+#endif
             if (t == 0) {
                 vote[(j + 2) % 3] = 1;
                 reinterpret_cast<volatile int*>(ctrl->dec)[w] = skip ? 1 : 0;
@@ -722,16 +777,33 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t pk[16];
+#if BLASST_EXP_BF16X2
+                    rs += exp_pack32_bf16(xr + ch * 32, p.c_log2, mc, pk);
+#else
                     rs += exp_pack32(xr + ch * 32, p.c_log2, mc, pk);
+#endif
                     tmem_st16(tl + s_col + ch * 16, pk);
+                    if (ch == 1) {  // first half of P (keys 0..63) is in TMEM: let PV start on it
+                        tmem_st_wait();
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ctrl->p_full[w][0]);
+                        fence_regs<64>(xr + 64);  // keep the second half's math after the signal
+                    }
                 }
                 l += rs;
                 ++npv;
                 tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->p_full[w][1]);
+            } else {
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&ctrl->p_full[w][0]);
+                    mbar_arrive(&ctrl->p_full[w][1]);
+                }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->p_full[w]);
         }
 
         if (npv > 0) {
@@ -804,6 +876,8 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 cudaError_t launch_prefill(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                            const PrefillParams& p, int d, PrefillVariant v, cudaStream_t stream) {
     switch (v) {
+        case PrefillVariant::kWide:
+            return launch_prefill_wide(tq, tk, tv, p, d, stream);
         case PrefillVariant::kTwoTiles:
             return d == 128 ? launch2_t<128>(tq, tk, tv, p, stream) : launch2_t<64>(tq, tk, tv, p, stream);
         case PrefillVariant::kOneTilePTmem:

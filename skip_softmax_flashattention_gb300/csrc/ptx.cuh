@@ -48,7 +48,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Status bits recorded in the library's device status word.
-enum : int { kStatusTimeout = 1 };
+enum : int { kStatusTimeout = 1, kStatusMisaligned = 2 };
 
 // Per-CTA watchdog state: the abort flag lives in shared memory, the limit in ns.
 struct Watchdog {
@@ -103,6 +103,17 @@ __device__ __forceinline__ void regs_inc() {
 template <int N>
 __device__ __forceinline__ void regs_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Barrier over `nthreads` threads that also returns the AND of every thread's predicate.
+__device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.and.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -166,6 +177,34 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
            | ((b_mn_major ? 1u : 0u) << 16)       // B major-ness
            | ((uint32_t)(N >> 3) << 17)           // N / 8
            | ((uint32_t)(M >> 4) << 24);          // M / 16
+}
+
+// The two 32-bit halves of a 128-byte-swizzle descriptor.  Offsets below 256 KB
+// added to the low half only move the start address field.
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+constexpr uint32_t kDescHiSW128 = (1024u >> 4) | (1u << 14) | (2u << 29);  // SBO 1024, version 1, 128B swizzle
+
+__device__ __forceinline__ void mma_ss_split(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\t"
+        "mov.b64 da, {%1, %5};\n\tmov.b64 db, {%2, %5};\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHiSW128)
+        : "memory");
+}
+__device__ __forceinline__ void mma_ts_split(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\t"
+        "mov.b64 db, {%2, %5};\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(accumulate), "r"(kDescHiSW128)
+        : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]
@@ -254,6 +293,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // ------------------------------------------------------------------ math
@@ -291,6 +335,13 @@ __device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float 
         : "f"(a0), "f"(a1));
 }
 
+// 2^x for two values at once on the special-function unit, bf16 in and out.
+__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
+    uint32_t y;
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
 // Maximum of 128 fp32 values held as raw bits, as a shallow tree of 3-input maxima.
 __device__ __forceinline__ float row_max128(const uint32_t* x) {
     float m[16];
@@ -314,6 +365,41 @@ __device__ __forceinline__ float exp_pack32(const uint32_t* x, float c, float mc
         ffma2(a0, a1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), c, -mc);
         const float p0 = ex2(a0), p1 = ex2(a1);
         pk[i] = pack_bf16x2(p0, p1);
+        if (i & 1)
+            fadd2_acc(s2, s3, p0, p1);
+        else
+            fadd2_acc(s0, s1, p0, p1);
+    }
+    return (s0 + s1) + (s2 + s3);
+}
+// As exp_pack32 for 16 scores (8 packed words).
+__device__ __forceinline__ float exp_pack16(const uint32_t* x, float c, float mc, uint32_t* pk) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        float a0, a1;
+        ffma2(a0, a1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), c, -mc);
+        const float p0 = ex2(a0), p1 = ex2(a1);
+        pk[i] = pack_bf16x2(p0, p1);
+        if (i & 1)
+            fadd2_acc(s2, s3, p0, p1);
+        else
+            fadd2_acc(s0, s1, p0, p1);
+    }
+    return (s0 + s1) + (s2 + s3);
+}
+// As exp_pack32, with the exponent argument rounded to bf16 and 2^x taken two at a
+// time in bf16 (half the special-function instructions); the sum adds the bf16
+// values that the P.V product will use.
+__device__ __forceinline__ float exp_pack32_bf16(const uint32_t* x, float c, float mc, uint32_t* pk) {
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float a0, a1;
+        ffma2(a0, a1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), c, -mc);
+        const uint32_t e = ex2_bf16x2(pack_bf16x2(a0, a1));
+        pk[i] = e;
+        const float p0 = __uint_as_float(e << 16), p1 = __uint_as_float(e & 0xffff0000u);
         if (i & 1)
             fadd2_acc(s2, s3, p0, p1);
         else

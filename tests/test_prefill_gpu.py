@@ -18,8 +18,8 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [0, K.BLASST_PREFILL_ONE_QTILE, K.BLASST_PREFILL_P_VIA_SMEM]
-VARIANT_IDS = ["two-qtiles", "one-qtile-P-in-TMEM", "one-qtile-P-in-SMEM"]
+VARIANTS = [0, K.BLASST_PREFILL_WIDE, K.BLASST_PREFILL_ONE_QTILE, K.BLASST_PREFILL_P_VIA_SMEM]
+VARIANT_IDS = ["two-qtiles", "two-qtiles-wide", "one-qtile-P-in-TMEM", "one-qtile-P-in-SMEM"]
 
 
 @pytest.fixture(autouse=True)
