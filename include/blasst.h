@@ -57,6 +57,7 @@ extern "C" {
 #define BLASST_ERR_CUDA (-4)             /* a CUDA runtime/driver call failed */
 #define BLASST_ERR_TIMEOUT (-5)          /* a device-side wait ran past its limit (see blasst_device_status) */
 #define BLASST_ERR_NO_CALIBRATION (-6)   /* target-sparsity mode without finite coefficients a, b */
+#define BLASST_ERR_SCRATCH_LIMIT (-7)    /* blasst_decode_noalloc: partials exceed the library's static scratch */
 
 /* flags for blasst_prefill_ex */
 #define BLASST_PREFILL_ELIDE_V 0x1u      /* also skip the V tile load of skipped tiles (not in this build: UNSUPPORTED) */
@@ -134,6 +135,30 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
                   int Hkv, int Lkv, int d, float scale, float lambda, int num_splits, void* workspace,
                   size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
                   float* margins, void* stream);
+
+/*
+ * Decode without any device allocation (the pages have no counterpart: this entry
+ * point exists for callers that cannot allocate).  Same arguments and results as
+ * blasst_decode, minus the workspace: the per-split partials go to a device array
+ * of blasst_decode_noalloc_scratch_bytes() bytes (4 MiB) that the library declares
+ * statically, so code whose device memory belongs to another allocator, or a serving
+ * loop that must not allocate between steps, can still split the key range.
+ *   - Requires num_splits * B * Hq * (d + 1) * 4 bytes (rounded as for
+ *     blasst_decode_workspace_size) <= the scratch size; larger requests return
+ *     BLASST_ERR_SCRATCH_LIMIT before any work is enqueued.
+ *   - The array exists once per device, for the life of the process, and every call
+ *     on that device shares it: calls that overlap on the GPU race on it.
+ *   - The first call on a device (with that device current) looks up the array's
+ *     device address; make that first call before any stream capture.
+ *   - Allocates nothing and calls no allocating routine.
+ */
+int blasst_decode_noalloc(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B,
+                          int Hq, int Hkv, int Lkv, int d, float scale, float lambda, int num_splits,
+                          unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                          void* stream);
+
+/* Size in bytes of the static scratch array blasst_decode_noalloc uses. */
+size_t blasst_decode_noalloc_scratch_bytes(void);
 
 /*
  * Threshold resolution (Skip-Softmax design doc, "From configuration to the

@@ -24,6 +24,7 @@ BLASST_ERR_WORKSPACE_TOO_SMALL = -3
 BLASST_ERR_CUDA = -4
 BLASST_ERR_TIMEOUT = -5
 BLASST_ERR_NO_CALIBRATION = -6
+BLASST_ERR_SCRATCH_LIMIT = -7
 
 BLASST_PREFILL_ELIDE_V = 0x1
 BLASST_PREFILL_P_VIA_SMEM = 0x2
@@ -66,6 +67,10 @@ def load(build_if_missing: bool = True):
     lib.blasst_decode_workspace_size.argtypes = [I, I, I, I, I, I]
     lib.blasst_decode.restype = I
     lib.blasst_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, I, P, ctypes.c_size_t, P, P, P, P]
+    lib.blasst_decode_noalloc.restype = I
+    lib.blasst_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, I, P, P, P, P]
+    lib.blasst_decode_noalloc_scratch_bytes.restype = ctypes.c_size_t
+    lib.blasst_decode_noalloc_scratch_bytes.argtypes = []
     lib.blasst_lambda.restype = I
     lib.blasst_lambda.argtypes = [I, ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                   ctypes.c_longlong, ctypes.POINTER(ctypes.c_double)]
@@ -126,6 +131,19 @@ def blasst_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Lkv, d, scale, lambda
                                 float(scale), float(lambda_), int(num_splits), _ptr(workspace),
                                 int(workspace_bytes), _ptr(skipped_tiles_out), _ptr(skip_map), _ptr(margins),
                                 _stream(stream))
+
+
+def blasst_decode_noalloc(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Lkv, d, scale, lambda_, num_splits,
+                          skipped_tiles_out=None, skip_map=None, margins=None, stream=None) -> int:
+    """blasst_decode for callers that cannot allocate: the per-split partials live in
+    the library's static device scratch (shared by every call on the device)."""
+    return load().blasst_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(o), _ptr(lse), B, Hq, Hkv,
+                                        Lkv, d, float(scale), float(lambda_), int(num_splits),
+                                        _ptr(skipped_tiles_out), _ptr(skip_map), _ptr(margins), _stream(stream))
+
+
+def blasst_decode_noalloc_scratch_bytes() -> int:
+    return int(load().blasst_decode_noalloc_scratch_bytes())
 
 
 def blasst_lambda(mode, threshold=0.0, a=math.nan, b=math.nan, target_sparsity=0.0, Lkv=1) -> tuple:

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libblasst.so")
-SOURCES = ["api.cu", "prefill.cu", "prefill_wide.cu", "decode.cu"]
+SOURCES = ["api.cu", "prefill.cu", "prefill_wide.cu", "decode.cu", "decode_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -313,6 +313,7 @@ const char* blasst_status_string(int status) {
         case BLASST_ERR_CUDA: return "CUDA error";
         case BLASST_ERR_TIMEOUT: return "device wait timed out";
         case BLASST_ERR_NO_CALIBRATION: return "target sparsity requested without calibration coefficients; use a threshold";
+        case BLASST_ERR_SCRATCH_LIMIT: return "decode partials exceed the library's static scratch (use blasst_decode with a workspace)";
         default: return "unknown status";
     }
 }
