@@ -35,8 +35,9 @@ PREFILL = dict(B=1, Hq=32, Hkv=8, L=16384, d=128)
 DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the current kernels; None until captured for this version of the kernels.
+# prefill: prefill2_kernel<128> capture (201.9 MB read + 100.6 MB written).
 # decode: B=8 capture (1073.9 MB read + 4.3 MB written) x 8 for the B=64 launch.
-TRAFFIC_BYTES = {"prefill": None, "decode": 8 * (1073888000 + 4261888)}
+TRAFFIC_BYTES = {"prefill": 201948416 + 100640512, "decode": 8 * (1073888000 + 4261888)}
 
 
 def load_peaks():
@@ -79,7 +80,7 @@ def visited_tiles_causal(Lq, Lkv, T=128):
 class ClockSampler:
     """nvidia-smi clock / throttle sampling during the timed region."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -93,11 +94,14 @@ class ClockSampler:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)  # let the sampler start before the timed region
         except Exception:
             self.proc = None
 
-    def stop(self):
+    def stop(self, t0=None, t1=None):
+        """Stop sampling; keep the samples taken between wall-clock times t0 and t1
+        (all samples if none fall inside)."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -106,15 +110,21 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.f.close()
+        import datetime
+
         rows = []
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
+            if len(parts) < 9:
                 continue
             try:
-                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
+        inside = [r for r in rows if t0 is not None and t0 - 0.02 <= r[0] <= t1 + 0.02]
+        window = "timed region" if inside else "around the timed region"
+        rows = [r[1:] for r in (inside or rows)]
         try:
             os.remove(self.path)
         except OSError:
@@ -124,7 +134,7 @@ class ClockSampler:
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for _, _, r in rows for i, v in enumerate(r) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+                "reasons": reasons, "samples": len(rows), "window": window}
 
 
 # ----------------------------------------------------------------- helpers
@@ -316,11 +326,12 @@ def run_ours(args):
     barrier(pg)
     torch.cuda.synchronize()
     t_wall0 = time.perf_counter()
+    t_epoch0 = time.time()
     evs = run_steps(args.steps, lam_p, lam_d, True)
     torch.cuda.synchronize()
     barrier(pg)
     t_wall = time.perf_counter() - t_wall0
-    clk = clocks.stop()
+    clk = clocks.stop(t_epoch0, time.time())
     st = K.blasst_device_status(1)
     if st != 0:
         raise K.BlasstError(st, "device status after the timed region")
@@ -466,6 +477,138 @@ def run_only(args):
     return 0 if st == 0 else 1
 
 
+def _time_ms(fn, flush, iters=10, warmup=3):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def run_sweep(args):
+    """Every workload at its thresholds: time, tile-skip fraction and speedup over
+    the same kernel at lambda = 0 (one JSON line per measurement)."""
+    import numpy as np
+    import torch
+
+    from skip_softmax_flashattention_gb300 import blasst as K
+    from skip_softmax_flashattention_gb300 import calibrate
+    from skip_softmax_flashattention_gb300 import workloads as W
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    flush = W.l2_flush_buffer(dev)
+    peaks = load_peaks()
+    out = []
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+        out.append(d)
+
+    def prefill_case(name, a, lams, only=None):
+        nQ, nK = -(-a.Lq // 128), -(-a.Lkv // 128)
+        visited = (visited_tiles_causal(a.Lq, a.Lkv) if a.causal else nQ * nK) * a.B * a.Hq
+        pairs = causal_pairs(a.Lq, a.Lkv) if a.causal else a.Lq * a.Lkv
+        dense = 4.0 * a.B * a.Hq * a.d * pairs
+        base = None
+        for lam in lams:
+            res = K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam)
+            torch.cuda.synchronize()
+            sk = int(res["skipped"].item())
+            o = res["o"]
+            ms = _time_ms(lambda: K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam, out=o), flush)
+            base = ms if lam == 0 or base is None else base
+            ex = 2.0 * 128 * 128 * a.d * (2 * visited - sk)
+            emit({"sweep": name, "kind": "prefill", "lambda": lam, "ms": ms, "skip_pct": 100.0 * sk / visited,
+                  "dense_tflops": dense / (ms * 1e-3) / 1e12, "executed_tflops": ex / (ms * 1e-3) / 1e12,
+                  "frac_of_measured_bf16": ex / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+                  "speedup_vs_lambda0": base / ms})
+
+    # LLM prefill (the bench workload) at lambda = a / L
+    a = W.llm(seed=0, L=16384, device=dev)
+    prefill_case("llm-prefill-L16384", a, [0.0, 4 / 16384, 40 / 16384, 0.3, 1.0])
+    del a
+    # planted-70: last 70% of key tiles hold K = 0
+    a = W.planted70(seed=0, L=16384, device=dev)
+    prefill_case("planted70-L16384", a, [0.0, 1e-2])
+    del a
+    # video DiT
+    a = W.dit(seed=0, device=dev)
+    prefill_case("dit-H40-L32760", a, [0.0, 1e-4, 1e-3, 1e-2])
+    del a
+    torch.cuda.empty_cache()
+
+    # decode at the workload's thresholds and at ~70% sparsity
+    dcfg = W.decode(seed=0, device=dev)
+    q3 = dcfg.q.reshape(dcfg.B, dcfg.Hq, dcfg.d)
+    nT = dcfg.Lkv // 128
+    tiles = dcfg.B * dcfg.Hkv * nT
+    tile_bytes = 128 * dcfg.d * 2
+    for S in (0, 1):
+        r0 = K.decode(q3, dcfg.k, dcfg.v, dcfg.scale, 0.0, num_splits=S, want_margins=True)
+        torch.cuda.synchronize()
+        Sx = r0["num_splits"]
+        lam70 = calibrate.lambda_for_sparsity(r0["margins"].cpu().numpy(), 0.70)
+        base = None
+        for lam in (0.0, 4 / dcfg.Lkv, 40 / dcfg.Lkv, lam70):
+            r = K.decode(q3, dcfg.k, dcfg.v, dcfg.scale, lam, num_splits=Sx)
+            torch.cuda.synchronize()
+            sk = int(r["skipped"].item())
+            ms = _time_ms(lambda: K.decode(q3, dcfg.k, dcfg.v, dcfg.scale, lam, num_splits=Sx), flush)
+            base = ms if lam == 0 else base
+            kv = tile_bytes * (2 * tiles - sk)
+            emit({"sweep": "decode-B64-L32768", "kind": "decode", "splits": Sx, "lambda": lam, "ms": ms,
+                  "skip_pct": 100.0 * sk / tiles, "kv_gbs": kv / (ms * 1e-3) / 1e9,
+                  "frac_of_measured_hbm": kv / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "speedup_vs_lambda0": base / ms, "note": "lambda for 70% from lambda=0 margins" if lam == lam70 else ""})
+    del dcfg, q3
+    torch.cuda.empty_cache()
+
+    # long-context sweep: calibrate on seed 1, evaluate targets on seed 2
+    cands = [float(x) for x in np.logspace(-6, 0, 25)]
+    margins = {}
+    for L in (8192, 32768, 65536):
+        a = W.llm(seed=1, L=L, device=dev)
+        r = K.prefill(a.q, a.k, a.v, True, a.scale, 0.0, want_margins=True)
+        torch.cuda.synchronize()
+        margins[L] = r["margins"].cpu().numpy()
+        del a, r
+        torch.cuda.empty_cache()
+    pts = calibrate.sweep(margins, cands)
+    fitted = calibrate.fit(pts)
+    emit({"sweep": "calibration", "seed": 1, "lengths": sorted(margins), "candidates": len(cands),
+          "informative_points": sum(1 for _, _, S_ in pts if 0 < S_ < 1),
+          "max_sparsity_at_lambda1": {L: calibrate.sparsity_at(g, 1.0) for L, g in margins.items()},
+          "fit": None if fitted is None else {"a": fitted[0], "b": fitted[1]}})
+    for L in (8192, 32768, 65536):
+        a = W.llm(seed=2, L=L, device=dev)
+        for s_t in (0.5, 0.7):
+            if fitted is None:
+                emit({"sweep": f"long-context-L{L}", "target": s_t, "result": "no calibration: the sparsity is 0 "
+                      "for every candidate threshold <= 1 on this data, so a and b cannot be fitted"})
+                continue
+            rc, lam = K.blasst_lambda(1, a=fitted[0], b=fitted[1], target_sparsity=s_t, Lkv=L)
+            unreachable = rc == K.BLASST_WARN_LAMBDA_GE_1
+            lam_run = 1.0 if unreachable else lam
+            r = K.prefill(a.q, a.k, a.v, True, a.scale, lam_run)
+            torch.cuda.synchronize()
+            visited = visited_tiles_causal(L, L) * a.B * a.Hq
+            emit({"sweep": f"long-context-L{L}", "target": s_t, "lambda": lam, "lambda_run": lam_run,
+                  "unreachable": unreachable, "achieved_skip_pct": 100.0 * int(r["skipped"].item()) / visited})
+        del a
+        torch.cuda.empty_cache()
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -482,11 +625,14 @@ def main():
     ap.add_argument("--prefill-len", type=int, default=16384)
     ap.add_argument("--decode-batch", type=int, default=64)
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--sweep", action="store_true", help="every workload at its thresholds (JSON lines)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.only:
         return run_only(args)
+    if args.sweep:
+        return run_sweep(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)
