@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/blasst.h: argument validation, the
 // threshold resolution, TMA descriptor encoding and kernel launches.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -115,6 +116,7 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
         return BLASST_ERR_UNSUPPORTED;
     if (Hq > 65535 || B > 65535) return BLASST_ERR_UNSUPPORTED;
     const long long nQ = (Lq + kTile - 1) / kTile, nK = (Lkv + kTile - 1) / kTile;
+    if (nQ * B * Hq > 0x7fffffffLL) return BLASST_ERR_UNSUPPORTED;  // one-dimensional grid
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int* status = status_word();
@@ -148,6 +150,18 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
     p.watchdog_ns = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? kShortWatchdogNs : kWatchdogNs;
     p.elide_v = 0;
     p.test_stall = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? 1 : 0;
+    // CTA order: under a causal mask the query tiles differ in work, so hand them out
+    // longest-first within bands of whole K/V-head groups whose K and V fit in half
+    // of L2; without a mask every tile costs the same and head-major order is kept.
+    p.band = 1;
+    if (causal) {
+        int dev = 0, l2 = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess)
+            return BLASST_ERR_CUDA;
+        const long long kv_head_bytes = 2LL * Lkv * d * 2;
+        const long long groups = std::max(1LL, (long long)(l2 / 2) / kv_head_bytes);
+        p.band = (int)std::min<long long>((long long)B * Hq, groups * (Hq / Hkv));
+    }
     const blasst::PrefillVariant var = (flags & BLASST_PREFILL_P_VIA_SMEM) ? blasst::PrefillVariant::kOneTilePSmem
                                        : (flags & BLASST_PREFILL_ONE_QTILE) ? blasst::PrefillVariant::kOneTilePTmem
                                        : (flags & BLASST_PREFILL_WIDE)      ? blasst::PrefillVariant::kWide

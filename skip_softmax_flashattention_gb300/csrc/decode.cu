@@ -104,6 +104,7 @@ __global__ void __launch_bounds__(224, 1)
         tmem_alloc(&ctrl->tmem_base, TMEM_COLS);
         tmem_relinquish();
     }
+    __syncwarp();  // the set-up above diverged inside warps; bar.sync is warp-aligned
     tc_fence_before();
     __syncthreads();
     tc_fence_after();

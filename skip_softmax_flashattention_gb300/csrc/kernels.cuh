@@ -26,7 +26,29 @@ struct PrefillParams {
     unsigned long long watchdog_ns;
     int elide_v;
     int test_stall;           // test only: the MMA issuer first waits on a barrier nothing arrives on
+    int band;                 // (b, h) pairs per scheduling band, see prefill_cta_coords
 };
+
+// Position of this CTA in a one-dimensional prefill grid of nunits * B * Hq CTAs.
+// The (b, h) pairs are cut into bands of p.band consecutive pairs (b * Hq + h order,
+// so the query heads that share a K/V head sit together); a band's CTAs are handed
+// out unit-major -- unit 0 of every pair in the band, then unit 1, ... -- and bands
+// follow one another.  With units numbered heaviest first (causal mask), a band
+// then runs longest-first, which evens out the finish times of the SMs, while the
+// K/V the band reads at once stays small enough for L2.  band == 1 is head-major.
+__device__ __forceinline__ void prefill_cta_coords(const PrefillParams& p, int nunits, int& unit, int& b, int& h) {
+    const int nbh = p.B * p.Hq;
+    const int lin = (int)blockIdx.x;
+    const int per_band = p.band * nunits;
+    const int bi = lin / per_band;
+    const int r = lin - bi * per_band;
+    const int bh0 = bi * p.band;
+    const int nb = min(p.band, nbh - bh0);
+    unit = r / nb;
+    const int bh = bh0 + (r - unit * nb);
+    b = bh / p.Hq;
+    h = bh - b * p.Hq;
+}
 
 struct DecodeParams {
     const uint16_t* q;        // bf16 [B,Hq,d]

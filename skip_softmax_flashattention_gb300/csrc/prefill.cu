@@ -39,11 +39,6 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 
-// Tile-vote reduction of the two-query-tile kernel: 0 = warp vote + shared-memory
-// atomicAnd + named barrier, 1 = barrier with AND reduction.
-#ifndef BLASST_VOTE_BARRIER_RED
-#define BLASST_VOTE_BARRIER_RED 0
-#endif
 // 2^x of the two-query-tile kernel: 0 = fp32 ex2 per element, 1 = bf16x2 ex2 per pair.
 #ifndef BLASST_EXP_BF16X2
 #define BLASST_EXP_BF16X2 0
@@ -102,8 +97,10 @@ __global__ void __launch_bounds__(192, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     const int G = p.Hq / p.Hkv;
-    const int qt = p.causal ? (p.nQ - 1 - (int)blockIdx.x) : (int)blockIdx.x;  // heavy tiles first
-    const int h = blockIdx.y, b = blockIdx.z, hk = h / G;
+    int unit, b, h;
+    prefill_cta_coords(p, p.nQ, unit, b, h);
+    const int qt = p.causal ? (p.nQ - 1 - unit) : unit;  // heavy tiles first
+    const int hk = h / G;
     const int r0 = qt * kTile;
     const int rows = min(kTile, p.Lq - r0);
     const int off = p.Lkv - p.Lq;  // bottom-right causal alignment
@@ -139,6 +136,7 @@ __global__ void __launch_bounds__(192, 1)
         tmem_alloc(&ctrl->tmem_base, C::TMEM_COLS);
         tmem_relinquish();
     }
+    __syncwarp();  // the set-up above diverged inside warps; bar.sync is warp-aligned
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -433,21 +431,29 @@ __global__ void __launch_bounds__(192, 1)
 // S_A = [0,128), S_B = [128,256), O_A = [256, 256+D), O_B = [256+D, 256+2D);
 // P_w overwrites the first 64 columns of S_w.  The tensor core runs, per key
 // tile j:  ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...  so the softmax of one
-// tile runs while the tensor core works on the other tile.  Each issuer releases
-// K/V slots on its own barriers, always through tcgen05.commit, so its releases
-// stay ordered behind its MMAs; the producer waits only for the issuers whose
-// tile read the previous occupant of a slot.
+// tile runs while the tensor core works on the other tile.  The tensor core queues
+// only a couple of MMAs ahead, so every instruction the issuing thread spends
+// between MMAs (a barrier wait, a commit) can leave it idle: each issuer commits
+// once per key tile, and that one commit tells the softmax that S is ready and
+// the producer which K/V slots its tile has finished with (a commit arrives only
+// after all earlier MMAs of its thread).  The producer waits only for the issuers
+// whose tile read the previous occupant of a slot.
 // ============================================================================
 template <int NK, int NV>
 struct Prefill2Ctrl {
+    // Commit c of the MMA issuer of query tile w arrives on rel[w][c % NR] once QK_w(c)
+    // and PV_w(c-1) -- and every MMA that thread issued before them -- are done: the
+    // softmax waits commit j for S_j (and for O to hold PV_w(j-1) before a rescale), the
+    // producer waits it to reuse K and V slots.  NR > max(NK, NV) keeps every waiter
+    // within one phase of the barrier it waits on.
+    static constexpr int NR = (NK > NV ? NK : NV) + 1;
     uint64_t q_full;
     uint64_t k_full[NK], v_full[NV];
-    uint64_t k_empty[2][NK], v_empty[2][NV];      // released by the MMA issuer of query tile w
-    uint64_t s_full[2], p_full[2][2], o_done[2];  // p_full[w][h]: half h (keys 64h..64h+63) of P_w stored
-    uint64_t drain[2], never;
+    uint64_t rel[2][NR];
+    uint64_t p_full[2][2];  // p_full[w][h]: half h (keys 64h..64h+63) of P_w stored
+    uint64_t never;
     uint32_t tmem_base;
-    int vote[2][3];
-    int dec[2];
+    int keep[2];  // keep[w] = j+1 once a warp of tile w keeps key tile j (only grows)
     int abort;
     int turn;       // which issuer may put its next group of MMAs into the tensor queue
     int active[2];  // issuer w still has key tiles to process
@@ -486,8 +492,10 @@ __global__ void __launch_bounds__(384, 1)
 
     const int G = p.Hq / p.Hkv;
     const int npairs = (p.nQ + 1) >> 1;
-    const int pi = p.causal ? (npairs - 1 - (int)blockIdx.x) : (int)blockIdx.x;  // heavy pairs first
-    const int h = blockIdx.y, b = blockIdx.z, hk = h / G;
+    int unit, b, h;
+    prefill_cta_coords(p, npairs, unit, b, h);
+    const int pi = p.causal ? (npairs - 1 - unit) : unit;  // heavy pairs first
+    const int hk = h / G;
     const int off = p.Lkv - p.Lq;
     int nvis[2];
 #pragma unroll
@@ -506,25 +514,14 @@ __global__ void __launch_bounds__(384, 1)
 
     if (tid == 0) {
         mbar_init(&ctrl->q_full, 1);
-        for (int i = 0; i < C::NK; ++i) {
-            mbar_init(&ctrl->k_full[i], 1);
-            mbar_init(&ctrl->k_empty[0][i], 1);
-            mbar_init(&ctrl->k_empty[1][i], 1);
-        }
-        for (int i = 0; i < C::NV; ++i) {
-            mbar_init(&ctrl->v_full[i], 1);
-            mbar_init(&ctrl->v_empty[0][i], 1);
-            mbar_init(&ctrl->v_empty[1][i], 1);
-        }
+        for (int i = 0; i < C::NK; ++i) mbar_init(&ctrl->k_full[i], 1);
+        for (int i = 0; i < C::NV; ++i) mbar_init(&ctrl->v_full[i], 1);
         for (int w = 0; w < 2; ++w) {
-            mbar_init(&ctrl->s_full[w], 1);
+            for (int i = 0; i < Ctrl::NR; ++i) mbar_init(&ctrl->rel[w][i], 1);
             mbar_init(&ctrl->p_full[w][0], 4);
             mbar_init(&ctrl->p_full[w][1], 4);
-            mbar_init(&ctrl->o_done[w], 1);
-            ctrl->vote[w][0] = ctrl->vote[w][1] = ctrl->vote[w][2] = 1;
+            ctrl->keep[w] = 0;
         }
-        mbar_init(&ctrl->drain[0], 1);
-        mbar_init(&ctrl->drain[1], 1);
         mbar_init(&ctrl->never, 1);
         ctrl->abort = 0;
         ctrl->turn = nvis[0] > 0 ? 0 : 1;
@@ -536,6 +533,7 @@ __global__ void __launch_bounds__(384, 1)
         tmem_alloc(&ctrl->tmem_base, C::TMEM_COLS);
         tmem_relinquish();
     }
+    __syncwarp();  // the set-up above diverged inside warps; bar.sync is warp-aligned
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -560,7 +558,10 @@ __global__ void __launch_bounds__(384, 1)
                     tma_load_3d(smem + C::OFF_Q + w * C::TILE_BYTES + x * C::BOX_BYTES, &tq, &ctrl->q_full, x * 64,
                                 (2 * pi + w) * kTile, zq);
             }
-            // A slot is reused once every query tile that read its previous occupant released it.
+            // A slot is reused once every query tile that read its previous occupant is done
+            // with it: K_m by QK_w(m), covered by commit m of issuer w; V_m by PV_w(m), covered
+            // by commit m+1.
+            constexpr int NR = Ctrl::NR;
             int issued_k = 0, issued_v = 0;
             for (int j = 0; j < N; ++j) {
                 const int ks = j % C::NK;
@@ -568,7 +569,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (j >= C::NK) {
                     const int prev = j - C::NK;
                     for (int w = 0; w < 2 && okk; ++w)
-                        if (prev < nvis[w]) okk = mbar_wait(&ctrl->k_empty[w][ks], (prev / C::NK) & 1, wd);
+                        if (prev < nvis[w]) okk = mbar_wait(&ctrl->rel[w][(unsigned)prev % NR], ((unsigned)prev / NR) & 1u, wd);
                 }
                 if (!okk) break;
                 mbar_arrive_expect_tx(&ctrl->k_full[ks], C::TILE_BYTES);
@@ -582,7 +583,8 @@ __global__ void __launch_bounds__(384, 1)
                 if (j >= C::NV) {
                     const int prev = j - C::NV;
                     for (int w = 0; w < 2 && okv; ++w)
-                        if (prev < nvis[w]) okv = mbar_wait(&ctrl->v_empty[w][vs], (prev / C::NV) & 1, wd);
+                        if (prev < nvis[w])
+                            okv = mbar_wait(&ctrl->rel[w][(unsigned)(prev + 1) % NR], ((unsigned)(prev + 1) / NR) & 1u, wd);
                 }
                 if (!okv) break;
                 mbar_arrive_expect_tx(&ctrl->v_full[vs], C::TILE_BYTES);
@@ -619,8 +621,11 @@ __global__ void __launch_bounds__(384, 1)
                     const uint32_t o = ((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4;
                     mma_ss_split(s_t, qlo + o, b0 + o, kIdescS, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(&ctrl->s_full[w]);
-                mma_commit(&ctrl->k_empty[w][j % C::NK]);
+            };
+            int ncommit = 0;
+            auto commit = [&]() {
+                mma_commit(&ctrl->rel[w][(unsigned)ncommit % Ctrl::NR]);
+                ++ncommit;
             };
             auto issue_pv_half = [&](int vs, int half, bool first) {
                 const uint32_t b0 = vlo + (uint32_t)vs * kTileLo;
@@ -636,6 +641,7 @@ __global__ void __launch_bounds__(384, 1)
             if (ok) {
                 tc_fence_after();
                 issue_qk(0);
+                commit();
             }
             volatile int* turn = &ctrl->turn;
             volatile int* active = ctrl->active;
@@ -656,31 +662,42 @@ __global__ void __launch_bounds__(384, 1)
                 return true;
             };
             int npv = 0;
+            unsigned long long nskip = 0;
+            const long long mapbase = ((long long)(b * p.Hq + h) * p.nQ + (2 * pi + w)) * p.nK;
             for (int j = 0; j < n && ok; ++j) {
                 const int vs = j % C::NV;
                 if (!(ok = mbar_wait(&ctrl->p_full[w][0], j & 1, wd))) break;
-                const bool skip = reinterpret_cast<volatile int*>(ctrl->dec)[w] != 0;
+                // all four warps have voted: the tile is kept iff one of them raised keep[w] to j+1
+                const bool skip = reinterpret_cast<volatile int*>(ctrl->keep)[w] <= j;
                 // V_j must have landed before its slot is released, also when the tile is skipped
                 if (!(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
                 if (j + 1 < n && !(ok = mbar_wait(&ctrl->k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1, wd))) break;
                 if (!(ok = take_turn())) break;
                 tc_fence_after();
                 if (!skip) issue_pv_half(vs, 0, npv == 0);
+                // the tile's record, written while the tensor core works through the queued MMAs
+                nskip += skip ? 1 : 0;
+                if (p.skip_map) p.skip_map[mapbase + j] = skip ? 1 : 0;
+                if (p.margins) {
+                    const volatile float* mr = ctrl->mred[w][j & 1];
+                    p.margins[mapbase + j] = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * p.scale;
+                }
                 if (!(ok = mbar_wait(&ctrl->p_full[w][1], j & 1, wd))) break;
                 tc_fence_after();
                 if (!skip) {
                     issue_pv_half(vs, 1, npv == 0);
-                    mma_commit(&ctrl->o_done[w]);
                     ++npv;
                 }
-                mma_commit(&ctrl->v_empty[w][vs]);
                 if (j + 1 < n) issue_qk(j + 1);
+                commit();  // commit j+1: PV_w(j) and QK_w(j+1)
                 *turn = 1 - w;
             }
             active[w] = 0;
             *turn = 1 - w;
-            mma_commit(&ctrl->drain[w]);
-            mbar_wait_drain(&ctrl->drain[w], 0, kDrainNs);
+            if (p.skipped && nskip) atomicAdd(p.skipped, nskip);
+            // the last commit covers every MMA this thread issued
+            if (ncommit > 0)
+                mbar_wait_drain(&ctrl->rel[w][(unsigned)(ncommit - 1) % Ctrl::NR], ((unsigned)(ncommit - 1) / Ctrl::NR) & 1u, kDrainNs);
         }
       }
     } else {
@@ -696,14 +713,12 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t s_col = (uint32_t)w * 128u;
         const uint32_t o_col = C::O_COL + (uint32_t)w * D;
         const int lim_row = p.causal ? rabs + off : 0x3fffffff;
-        const long long mapbase = ((long long)(b * p.Hq + h) * p.nQ + qt) * p.nK;
         float m_exact = -CUDART_INF_F, m_ref = -CUDART_INF_F, l = 0.f;
         int npv = 0;
-        unsigned long long nskip = 0;
-        int* vote = ctrl->vote[w];
 
         for (int j = 0; j < n; ++j) {
-            mbar_wait(&ctrl->s_full[w], j & 1, wd);
+            // commit j: S_j is in TMEM and O holds PV_w(j-1)
+            mbar_wait(&ctrl->rel[w][(unsigned)j % Ctrl::NR], ((unsigned)j / Ctrl::NR) & 1u, wd);
             tc_fence_after();
             uint32_t xr[128];
             tmem_ld32(tl + s_col + 0, xr);
@@ -729,33 +744,26 @@ __global__ void __launch_bounds__(384, 1)
                 for (int sh = 16; sh > 0; sh >>= 1) g = fmaxf(g, __shfl_xor_sync(0xffffffffu, g, sh));
                 if (lane == 0) ctrl->mred[w][j & 1][warp & 3] = g;
             }
-#if BLASST_VOTE_BARRIER_RED
-            // AND of the 128 row votes, reduced by the barrier itself
-            const bool skip = bar_red_and(1 + w, 128, vote_skip);
-#else
-            // row vote -> warp vote -> one shared-memory atomicAnd per warp -> tile flag
+            // Tile vote.  A warp with a row that keeps the tile raises keep[w] to j+1 and
+            // arrives at the tile's barrier without waiting; only warps whose 32 rows all
+            // vote to skip wait there for the other warps.  keep[w] only grows, and key
+            // tile j+1 starts after every warp has finished tile j, so it needs no reset.
+            // The MMA issuer reads the same word and writes the tile's record.
             const unsigned all = __all_sync(0xffffffffu, vote_skip);
-            if (lane == 0) atomicAnd(&vote[j % 3], (int)all);
-            named_bar_sync(1 + w, 128);
-            const bool skip = reinterpret_cast<volatile int*>(vote)[j % 3] != 0;
-#endif
-            if (t == 0) {
-                vote[(j + 2) % 3] = 1;
-                reinterpret_cast<volatile int*>(ctrl->dec)[w] = skip ? 1 : 0;
-                if (p.skip_map) p.skip_map[mapbase + j] = skip ? 1 : 0;
-                if (p.margins) {
-                    const volatile float* mr = ctrl->mred[w][j & 1];
-                    p.margins[mapbase + j] = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * p.scale;
-                }
-                nskip += skip ? 1 : 0;
+            bool skip = false;
+            if (!all) {
+                if (lane == 0) atomicMax(&ctrl->keep[w], j + 1);
+                __syncwarp();
+                named_bar_arrive(1 + w, 128);
+            } else {
+                named_bar_sync(1 + w, 128);
+                skip = reinterpret_cast<volatile int*>(ctrl->keep)[w] <= j;
             }
             m_exact = mnew;
             if (!skip) {
                 const bool move = mnew != -CUDART_INF_F && (m_ref == -CUDART_INF_F || mnew > m_ref + p.lazy_raw);
                 const float alpha = move ? (m_ref == -CUDART_INF_F ? 0.f : ex2((m_ref - mnew) * p.c_log2)) : 1.f;
                 if (__any_sync(0xffffffffu, move) && npv > 0) {
-                    mbar_wait(&ctrl->o_done[w], (npv - 1) & 1, wd);
-                    tc_fence_after();
 #pragma unroll
                     for (int cc = 0; cc < D; cc += 32) {
                         uint32_t tt[32];
@@ -806,8 +814,8 @@ __global__ void __launch_bounds__(384, 1)
             }
         }
 
-        if (npv > 0) {
-            mbar_wait(&ctrl->o_done[w], (npv - 1) & 1, wd);
+        if (n > 0) {  // commit n covers the last PV
+            mbar_wait(&ctrl->rel[w][(unsigned)n % Ctrl::NR], ((unsigned)n / Ctrl::NR) & 1u, wd);
             tc_fence_after();
         }
         const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -837,7 +845,6 @@ __global__ void __launch_bounds__(384, 1)
         }
         if (valid && p.lse)
             p.lse[(long long)(b * p.Hq + h) * p.Lq + rabs] = l > 0.f ? m_ref * p.scale + __logf(l) : -CUDART_INF_F;
-        if (t == 0 && p.skipped && nskip) atomicAdd(p.skipped, nskip);
     }
 
     __syncwarp();
@@ -855,7 +862,7 @@ cudaError_t launch2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtens
     using C = Prefill2Cfg<D>;
     cudaError_t e = cudaFuncSetAttribute(prefill2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.nQ + 1) / 2, p.Hq, p.B);
+    const dim3 grid((unsigned)(((p.nQ + 1) / 2) * p.B * p.Hq));
     prefill2_kernel<D><<<grid, 384, C::SMEM, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -866,7 +873,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     using C = PrefillCfg<D, PT>;
     cudaError_t e = cudaFuncSetAttribute(prefill_kernel<D, PT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.nQ, p.Hq, p.B);
+    const dim3 grid((unsigned)(p.nQ * p.B * p.Hq));
     prefill_kernel<D, PT><<<grid, 192, C::SMEM, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }

@@ -101,8 +101,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int G = p.Hq / p.Hkv;
     const int npairs = (p.nQ + 1) >> 1;
-    const int pi = p.causal ? (npairs - 1 - (int)blockIdx.x) : (int)blockIdx.x;  // heavy pairs first
-    const int h = blockIdx.y, b = blockIdx.z, hk = h / G;
+    int unit, b, h;
+    prefill_cta_coords(p, npairs, unit, b, h);
+    const int pi = p.causal ? (npairs - 1 - unit) : unit;  // heavy pairs first
+    const int hk = h / G;
     const int off = p.Lkv - p.Lq;
     int nvis[2];
 #pragma unroll
@@ -150,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&ctrl->tmem_base, C::TMEM_COLS);
         tmem_relinquish();
     }
+    __syncwarp();  // the set-up above diverged inside warps; bar.sync is warp-aligned
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -461,7 +464,7 @@ cudaError_t launch_wide_t(const CUtensorMap& tq, const CUtensorMap& tk, const CU
     cudaError_t e =
         cudaFuncSetAttribute(prefill_wide_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid((p.nQ + 1) / 2, p.Hq, p.B);
+    const dim3 grid((unsigned)(((p.nQ + 1) / 2) * p.B * p.Hq));
     prefill_wide_kernel<D><<<grid, kThreads, C::SMEM, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }

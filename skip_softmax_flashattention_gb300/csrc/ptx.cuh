@@ -118,6 +118,11 @@ __device__ __forceinline__ bool bar_red_and(uint32_t id, uint32_t nthreads, bool
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
+// Arrive at named barrier `id` without waiting: memory accesses before it are
+// visible to the threads that complete the barrier with bar.sync.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
 
 // ------------------------------------------------------------------ TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
