@@ -752,7 +752,8 @@ __global__ void __launch_bounds__(384, 1)
             const unsigned all = __all_sync(0xffffffffu, vote_skip);
             bool skip = false;
             if (!all) {
-                if (lane == 0) atomicMax(&ctrl->keep[w], j + 1);
+                // every writer stores the same value j+1, so a plain store does
+                st_shared_if(&ctrl->keep[w], (uint32_t)(j + 1), lane == 0);
                 __syncwarp();
                 named_bar_arrive(1 + w, 128);
             } else {
@@ -795,7 +796,7 @@ __global__ void __launch_bounds__(384, 1)
                         tmem_st_wait();
                         tc_fence_before();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(&ctrl->p_full[w][0]);
+                        mbar_arrive_if(&ctrl->p_full[w][0], lane == 0);
                         fence_regs<64>(xr + 64);  // keep the second half's math after the signal
                     }
                 }
@@ -804,7 +805,7 @@ __global__ void __launch_bounds__(384, 1)
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ctrl->p_full[w][1]);
+                mbar_arrive_if(&ctrl->p_full[w][1], lane == 0);
             } else {
                 __syncwarp();
                 if (lane == 0) {
