@@ -514,21 +514,22 @@ def run_sweep(args):
         print(json.dumps(d), flush=True)
         out.append(d)
 
-    def prefill_case(name, a, lams, only=None):
+    def prefill_case(name, a, lams, only=None, flags=0):
         nQ, nK = -(-a.Lq // 128), -(-a.Lkv // 128)
         visited = (visited_tiles_causal(a.Lq, a.Lkv) if a.causal else nQ * nK) * a.B * a.Hq
         pairs = causal_pairs(a.Lq, a.Lkv) if a.causal else a.Lq * a.Lkv
         dense = 4.0 * a.B * a.Hq * a.d * pairs
         base = None
         for lam in lams:
-            res = K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam)
+            res = K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam, flags=flags)
             torch.cuda.synchronize()
             sk = int(res["skipped"].item())
             o = res["o"]
-            ms = _time_ms(lambda: K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam, out=o), flush)
+            ms = _time_ms(lambda: K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam, out=o, flags=flags), flush)
             base = ms if lam == 0 or base is None else base
             ex = 2.0 * 128 * 128 * a.d * (2 * visited - sk)
-            emit({"sweep": name, "kind": "prefill", "lambda": lam, "ms": ms, "skip_pct": 100.0 * sk / visited,
+            emit({"sweep": name, "kind": "prefill", "flags": flags, "lambda": lam, "ms": ms,
+                  "skip_pct": 100.0 * sk / visited,
                   "dense_tflops": dense / (ms * 1e-3) / 1e12, "executed_tflops": ex / (ms * 1e-3) / 1e12,
                   "frac_of_measured_bf16": ex / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
                   "speedup_vs_lambda0": base / ms})
@@ -540,10 +541,13 @@ def run_sweep(args):
     # planted-70: last 70% of key tiles hold K = 0
     a = W.planted70(seed=0, L=16384, device=dev)
     prefill_case("planted70-L16384", a, [0.0, 1e-2])
+    # the same with V loads of skipped key tiles elided (default off: see the notes on flags)
+    prefill_case("planted70-L16384-elide-V", a, [0.0, 1e-2], flags=K.BLASST_PREFILL_ELIDE_V)
     del a
     # video DiT
     a = W.dit(seed=0, device=dev)
     prefill_case("dit-H40-L32760", a, [0.0, 1e-4, 1e-3, 1e-2])
+    prefill_case("dit-H40-L32760-elide-V", a, [0.0, 1e-2], flags=K.BLASST_PREFILL_ELIDE_V)
     del a
     torch.cuda.empty_cache()
 

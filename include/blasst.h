@@ -60,7 +60,7 @@ extern "C" {
 #define BLASST_ERR_SCRATCH_LIMIT (-7)    /* blasst_decode_noalloc: partials exceed the library's static scratch */
 
 /* flags for blasst_prefill_ex */
-#define BLASST_PREFILL_ELIDE_V 0x1u      /* also skip the V tile load of skipped tiles (not in this build: UNSUPPORTED) */
+#define BLASST_PREFILL_ELIDE_V 0x1u      /* default kernel: load V_j only if a query tile of the CTA keeps key tile j */
 #define BLASST_PREFILL_P_VIA_SMEM 0x2u   /* one query tile per CTA, P staged in shared memory (results identical) */
 #define BLASST_PREFILL_ONE_QTILE 0x4u    /* one query tile per CTA, P in tensor memory (results identical) */
 #define BLASST_PREFILL_WIDE 0x8u         /* two query tiles per CTA, two softmax threads per row (results identical) */
@@ -96,8 +96,13 @@ int blasst_prefill(const void* q, const void* k, const void* v, void* o, float* 
  *              a tile is skipped iff margin < ln(lambda).
  *   flags      BLASST_PREFILL_P_VIA_SMEM, BLASST_PREFILL_ONE_QTILE, BLASST_PREFILL_WIDE
  *              (kernel variants with identical results; default: two query tiles per CTA,
- *              one softmax thread per query row), BLASST_FLAG_TEST_SHORT_WATCHDOG;
- *              BLASST_PREFILL_ELIDE_V is reserved and returns BLASST_ERR_UNSUPPORTED.
+ *              one softmax thread per query row), BLASST_FLAG_TEST_SHORT_WATCHDOG.
+ *              BLASST_PREFILL_ELIDE_V (default kernel only; with another variant flag:
+ *              BLASST_ERR_UNSUPPORTED) also skips the V tile load of a key tile that both
+ *              query tiles of a CTA skip.  The BLASST talk notes ("Kernel" Q&A) keep loading
+ *              V in prefill; eliding it makes each V load wait for the tile vote, so it
+ *              saves L2/HBM bytes at the cost of exposing the load latency.  Results are
+ *              identical either way.
  */
 int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                       int Hkv, int Lq, int Lkv, int d, int causal, float scale, float lambda,

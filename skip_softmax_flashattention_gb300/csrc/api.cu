@@ -109,7 +109,9 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
                            BLASST_PREFILL_WIDE | BLASST_FLAG_TEST_SHORT_WATCHDOG;
     if (flags & ~known) return BLASST_ERR_INVALID_ARG;
     if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
-    if (flags & BLASST_PREFILL_ELIDE_V) return BLASST_ERR_UNSUPPORTED;
+    if ((flags & BLASST_PREFILL_ELIDE_V) &&
+        (flags & (BLASST_PREFILL_P_VIA_SMEM | BLASST_PREFILL_ONE_QTILE | BLASST_PREFILL_WIDE)))
+        return BLASST_ERR_UNSUPPORTED;  // V elision is built into the default kernel only
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
         (reinterpret_cast<uintptr_t>(skipped_tiles_out) & 7u))
@@ -148,7 +150,7 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
     p.margins = margins;
     p.status = status;
     p.watchdog_ns = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? kShortWatchdogNs : kWatchdogNs;
-    p.elide_v = 0;
+    p.elide_v = (flags & BLASST_PREFILL_ELIDE_V) ? 1 : 0;
     p.test_stall = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? 1 : 0;
     // CTA order: under a causal mask the query tiles differ in work, so hand them out
     // longest-first within bands of whole K/V-head groups whose K and V fit in half

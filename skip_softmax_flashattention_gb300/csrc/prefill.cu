@@ -454,6 +454,7 @@ struct Prefill2Ctrl {
     uint64_t never;
     uint32_t tmem_base;
     int keep[2];  // keep[w] = j+1 once a warp of tile w keeps key tile j (only grows)
+    int dec[2];   // V elision: 2(j+1) + kept, tile w's decision on key tile j, from its issuer (only grows)
     int abort;
     int turn;       // which issuer may put its next group of MMAs into the tensor queue
     int active[2];  // issuer w still has key tiles to process
@@ -521,6 +522,7 @@ __global__ void __launch_bounds__(384, 1)
             mbar_init(&ctrl->p_full[w][0], 4);
             mbar_init(&ctrl->p_full[w][1], 4);
             ctrl->keep[w] = 0;
+            ctrl->dec[w] = 0;
         }
         mbar_init(&ctrl->never, 1);
         ctrl->abort = 0;
@@ -563,36 +565,70 @@ __global__ void __launch_bounds__(384, 1)
             // by commit m+1.
             constexpr int NR = Ctrl::NR;
             int issued_k = 0, issued_v = 0;
-            for (int j = 0; j < N; ++j) {
-                const int ks = j % C::NK;
-                bool okk = true;
-                if (j >= C::NK) {
-                    const int prev = j - C::NK;
-                    for (int w = 0; w < 2 && okk; ++w)
-                        if (prev < nvis[w]) okk = mbar_wait(&ctrl->rel[w][(unsigned)prev % NR], ((unsigned)prev / NR) & 1u, wd);
+            auto load_k = [&](int m) -> bool {
+                const int ks = m % C::NK;
+                if (m >= C::NK) {
+                    const int prev = m - C::NK;
+                    for (int w = 0; w < 2; ++w)
+                        if (prev < nvis[w] && !mbar_wait(&ctrl->rel[w][(unsigned)prev % NR], ((unsigned)prev / NR) & 1u, wd))
+                            return false;
                 }
-                if (!okk) break;
                 mbar_arrive_expect_tx(&ctrl->k_full[ks], C::TILE_BYTES);
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x)
                     tma_load_3d(smem + C::OFF_K + ks * C::TILE_BYTES + x * C::BOX_BYTES, &tk, &ctrl->k_full[ks],
-                                x * 64, j * kTile, zkv);
-                issued_k = j + 1;
-                const int vs = j % C::NV;
-                bool okv = true;
-                if (j >= C::NV) {
-                    const int prev = j - C::NV;
-                    for (int w = 0; w < 2 && okv; ++w)
-                        if (prev < nvis[w])
-                            okv = mbar_wait(&ctrl->rel[w][(unsigned)(prev + 1) % NR], ((unsigned)(prev + 1) / NR) & 1u, wd);
+                                x * 64, m * kTile, zkv);
+                issued_k = m + 1;
+                return true;
+            };
+            auto load_v = [&](int m) -> bool {
+                const int vs = m % C::NV;
+                if (m >= C::NV) {
+                    const int prev = m - C::NV;
+                    for (int w = 0; w < 2; ++w)
+                        if (prev < nvis[w] &&
+                            !mbar_wait(&ctrl->rel[w][(unsigned)(prev + 1) % NR], ((unsigned)(prev + 1) / NR) & 1u, wd))
+                            return false;
                 }
-                if (!okv) break;
-                mbar_arrive_expect_tx(&ctrl->v_full[vs], C::TILE_BYTES);
+                bool need = true;
+                if (p.elide_v) {
+                    // V_m is needed only if a query tile keeps key tile m.  Tile w's issuer
+                    // publishes its decision as dec[w] = 2(m+1) + kept; tile w cannot pass key
+                    // tile m before v_full of V_m completes (its issuer waits for it), so
+                    // dec[w] stops there.  A word that only grows, unlike a barrier phase,
+                    // may be read for any key tile without having watched the earlier ones:
+                    // tile B is asked only when tile A does not keep the tile.
+                    need = false;
+                    for (int w = 0; w < 2 && !need; ++w) {
+                        if (m >= nvis[w]) continue;
+                        int dv = 0;
+                        if (!spin_until_ge(&ctrl->dec[w], 2 * (m + 1), dv, wd)) return false;
+                        need = (dv & 1) != 0;
+                    }
+                }
+                if (need) {
+                    mbar_arrive_expect_tx(&ctrl->v_full[vs], C::TILE_BYTES);
 #pragma unroll
-                for (int x = 0; x < D / 64; ++x)
-                    tma_load_3d(smem + C::OFF_V + vs * C::TILE_BYTES + x * C::BOX_BYTES, &tv, &ctrl->v_full[vs],
-                                x * 64, j * kTile, zkv);
-                issued_v = j + 1;
+                    for (int x = 0; x < D / 64; ++x)
+                        tma_load_3d(smem + C::OFF_V + vs * C::TILE_BYTES + x * C::BOX_BYTES, &tv, &ctrl->v_full[vs],
+                                    x * 64, m * kTile, zkv);
+                } else {
+                    mbar_arrive(&ctrl->v_full[vs]);  // completes the slot's phase without data
+                }
+                issued_v = m + 1;
+                return true;
+            };
+            if (!p.elide_v) {
+                for (int j = 0; j < N; ++j)
+                    if (!load_k(j) || !load_v(j)) break;
+            } else {
+                // V loads wait for the votes, so K runs NK-1 tiles ahead of them
+                bool ok = true;
+                int jk = 0;
+                for (int j = 0; j < N && ok; ++j) {
+                    for (; ok && jk < N && jk <= j + C::NK - 1; ++jk) ok = load_k(jk);
+                    ok = ok && load_v(j);
+                }
             }
             mbar_wait_drain(&ctrl->q_full, 0, kDrainNs);
             for (int j = max(0, issued_k - C::NK); j < issued_k; ++j)
@@ -669,6 +705,7 @@ __global__ void __launch_bounds__(384, 1)
                 if (!(ok = mbar_wait(&ctrl->p_full[w][0], j & 1, wd))) break;
                 // all four warps have voted: the tile is kept iff one of them raised keep[w] to j+1
                 const bool skip = reinterpret_cast<volatile int*>(ctrl->keep)[w] <= j;
+                if (p.elide_v) reinterpret_cast<volatile int*>(ctrl->dec)[w] = 2 * (j + 1) + (skip ? 0 : 1);
                 // V_j must have landed before its slot is released, also when the tile is skipped
                 if (!(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
                 if (j + 1 < n && !(ok = mbar_wait(&ctrl->k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1, wd))) break;

@@ -90,6 +90,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Wait until the shared word *addr, which only grows, reaches `target`; its value is
+// left in `val`.  Polls with a short sleep.  Same limit and abort rules as mbar_wait.
+__device__ __forceinline__ bool spin_until_ge(const int* addr, int target, int& val, const Watchdog& wd) {
+    const volatile int* a = addr;
+    val = *a;
+    if (val >= target) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(32);
+        val = *a;
+        if (val >= target) return true;
+        if (*wd.abort_flag) return false;
+        if (globaltimer_ns() - t0 > wd.limit_ns) {
+            *wd.abort_flag = 1;
+            atomicOr(wd.status, kStatusTimeout);
+            return false;
+        }
+    }
+}
+
 // Wait that ignores the abort flag (used only to drain copies this thread issued;
 // they complete on their own).  Bounded by `limit_ns`.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {

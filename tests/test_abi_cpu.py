@@ -92,7 +92,9 @@ FAKE = 1 << 20  # never dereferenced: every call below fails validation first
     (dict(causal=2), K.BLASST_ERR_INVALID_ARG),
     (dict(flags=0x100), K.BLASST_ERR_INVALID_ARG),
     (dict(d=96), K.BLASST_ERR_UNSUPPORTED),
-    (dict(flags=K.BLASST_PREFILL_ELIDE_V), K.BLASST_ERR_UNSUPPORTED),
+    (dict(flags=K.BLASST_PREFILL_ELIDE_V | K.BLASST_PREFILL_WIDE), K.BLASST_ERR_UNSUPPORTED),
+    (dict(flags=K.BLASST_PREFILL_ELIDE_V | K.BLASST_PREFILL_ONE_QTILE), K.BLASST_ERR_UNSUPPORTED),
+    (dict(flags=K.BLASST_PREFILL_ELIDE_V | K.BLASST_PREFILL_P_VIA_SMEM), K.BLASST_ERR_UNSUPPORTED),
     (dict(q=FAKE + 8), K.BLASST_ERR_UNSUPPORTED),
 ])
 def test_prefill_validation(kw, code):

@@ -18,8 +18,9 @@ from tests import parity
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS = [0, K.BLASST_PREFILL_WIDE, K.BLASST_PREFILL_ONE_QTILE, K.BLASST_PREFILL_P_VIA_SMEM]
-VARIANT_IDS = ["two-qtiles", "two-qtiles-wide", "one-qtile-P-in-TMEM", "one-qtile-P-in-SMEM"]
+VARIANTS = [0, K.BLASST_PREFILL_ELIDE_V, K.BLASST_PREFILL_WIDE, K.BLASST_PREFILL_ONE_QTILE,
+            K.BLASST_PREFILL_P_VIA_SMEM]
+VARIANT_IDS = ["two-qtiles", "two-qtiles-elide-V", "two-qtiles-wide", "one-qtile-P-in-TMEM", "one-qtile-P-in-SMEM"]
 
 
 @pytest.fixture(autouse=True)
@@ -125,6 +126,29 @@ def test_planted70_skip_set_and_parity():
     rng = np.random.default_rng(2)
     units = parity.sample_units(rng, 1, a.Hq, L // 128, 3, always=[(0, 0, 0)])
     parity.prefill_units_check(a, res, 1e-2, units)
+
+
+@pytest.mark.parametrize("workload", ["planted70", "dit", "llm"])
+def test_elide_v_is_bitwise_identical_at_full_size(workload):
+    """Eliding V changes which V tiles are loaded, never what is computed: outputs,
+    lse, skip map and count equal the default kernel's bit for bit, with skips
+    (planted-70 at 70 %, DiT at 51 %) and without (LLM prefill)."""
+    if workload == "planted70":
+        a, causal, lam = W.planted70(seed=0, L=16384, device="cuda"), False, 1e-2
+    elif workload == "dit":
+        a, causal, lam = W.dit(seed=0, device="cuda"), False, 1e-2
+    else:
+        a, causal, lam = W.llm(seed=0, L=16384, device="cuda"), True, 40 / 16384
+    a = parity.to_gpu(a)
+    ref = K.prefill(a.q, a.k, a.v, causal, a.scale, lam, want_map=True)
+    got = K.prefill(a.q, a.k, a.v, causal, a.scale, lam, want_map=True, flags=K.BLASST_PREFILL_ELIDE_V)
+    torch.cuda.synchronize()
+    assert torch.equal(got["map"], ref["map"])
+    assert int(got["skipped"].item()) == int(ref["skipped"].item())
+    assert torch.equal(got["o"], ref["o"])
+    assert torch.equal(got["lse"], ref["lse"])
+    if workload != "llm":
+        assert int(ref["skipped"].item()) > 0
 
 
 def test_short_watchdog_reports_timeout_and_context_survives():
