@@ -577,6 +577,29 @@ def run_sweep(args):
     del dcfg, q3
     torch.cuda.empty_cache()
 
+    # paged decode (blasst_decode_paged): the same shapes with the cache in pages
+    # scattered over a pool, at full length and with 16k-32k keys per sequence
+    for ps, tmaj, lens_kind in ((16, True, "full"), (128, False, "full"), (16, True, "16k-32k")):
+        a = W.paged_decode(seed=0, B=64, Hq=32, Hkv=8, max_len=32768, page_size=ps, token_major=tmaj,
+                           lens=[32768] * 64 if lens_kind == "full" else None, min_len=16384, device=dev)
+        e = a.extra
+        keys = int(e["seq_lens"].sum().item())
+        for lam in (0.0, 0.3):
+            r = K.decode_paged(a.q, e["k_pages"], e["v_pages"], e["page_table"], e["seq_lens"], 32768, ps, tmaj,
+                               a.scale, lam, 0)
+            torch.cuda.synchronize()
+            sk = int(r["skipped"].item())
+            Sx = r["num_splits"]
+            ms = _time_ms(lambda: K.decode_paged(a.q, e["k_pages"], e["v_pages"], e["page_table"], e["seq_lens"],
+                                                 32768, ps, tmaj, a.scale, lam, Sx), flush)
+            tiles_v = int(((e["seq_lens"] + 127) // 128).sum().item()) * a.Hkv
+            kv = keys * a.Hkv * a.d * 2 + 128 * a.d * 2 * (tiles_v - sk)  # K of every key, V of computed tiles
+            emit({"sweep": f"paged-decode-B64-L32768-ps{ps}-{'key' if tmaj else 'head'}-major-{lens_kind}",
+                  "kind": "decode", "splits": Sx, "lambda": lam, "ms": ms, "skip_pct": 100.0 * sk / tiles_v,
+                  "kv_gbs": kv / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": kv / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]})
+        del a, e
+        torch.cuda.empty_cache()
+
     # long-context sweep: calibrate on seed 1, evaluate targets on seed 2
     cands = [float(x) for x in np.logspace(-6, 0, 25)]
     margins = {}

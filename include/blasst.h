@@ -58,6 +58,8 @@ extern "C" {
 #define BLASST_ERR_TIMEOUT (-5)          /* a device-side wait ran past its limit (see blasst_device_status) */
 #define BLASST_ERR_NO_CALIBRATION (-6)   /* target-sparsity mode without finite coefficients a, b */
 #define BLASST_ERR_SCRATCH_LIMIT (-7)    /* blasst_decode_noalloc: partials exceed the library's static scratch */
+#define BLASST_ERR_PAGE_TABLE (-8)       /* blasst_device_status: a page index or sequence length of a paged
+                                            decode was out of range (those keys read as zeros / length clamped) */
 
 /* flags for blasst_prefill_ex */
 #define BLASST_PREFILL_ELIDE_V 0x1u      /* default kernel: load V_j only if a query tile of the CTA keeps key tile j */
@@ -140,6 +142,41 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
                   int Hkv, int Lkv, int d, float scale, float lambda, int num_splits, void* workspace,
                   size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
                   float* margins, void* stream);
+
+/*
+ * Decode against a paged KV cache, with a key count per sequence (The Hitchhiker's
+ * Guide, Phase 08, Section 3 "Continuous Batching & Paged Attention": key i of
+ * sequence b is row i mod page_size of page page_table[b][i / page_size]; the
+ * Skip-Softmax design doc, "From configuration to the kernel threshold": lambda is
+ * one value per call, resolved against max_kv_len with blasst_lambda).
+ *   q [B, Hq, d], o [B, Hq, d] bf16; lse nullable fp32 [B, Hq].
+ *   k_pages / v_pages  bf16 page pools of num_pages pages, each page_size keys of
+ *                every KV head: token_major = 1: [num_pages][page_size][Hkv][d];
+ *                token_major = 0: [num_pages][Hkv][page_size][d].  16-byte aligned.
+ *   page_table   device int32 [B, max_pages_per_seq]; entries past a sequence's
+ *                last page are never read.  max_pages_per_seq * page_size >= max_kv_len.
+ *   seq_lens     nullable device int32 [B]: keys of sequence b, 0 <= seq_lens[b] <=
+ *                max_kv_len (NULL: every sequence has max_kv_len keys).  A sequence
+ *                of length 0 gives o = 0, lse = -inf.
+ *   page_size    8, 16, 32, 64, or a multiple of 128 (else BLASST_ERR_UNSUPPORTED).
+ *   num_splits   as for blasst_decode, planned on max_kv_len: split s of sequence b
+ *                covers its tiles [floor(s*nT_b/S), floor((s+1)*nT_b/S)), nT_b =
+ *                ceil(seq_lens[b]/128); a split with no tile contributes nothing.
+ *   workspace    as for blasst_decode (blasst_decode_workspace_size with max_kv_len).
+ *   skip_map / margins  nullable [B, Hkv, ceil(max_kv_len/128)], tiles past a
+ *                sequence's end stay "not visited" (2 / NaN).
+ *   A page index outside [0, num_pages) or a length outside [0, max_kv_len) is
+ *   not trusted: those keys read as zeros (no memory outside the pool is touched),
+ *   the length is clamped, and blasst_device_status reports BLASST_ERR_PAGE_TABLE.
+ *   Keys past seq_lens[b] on the sequence's last page are loaded but get zero
+ *   weight; they must hold finite values (a zeroed or previously written pool).
+ */
+int blasst_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* page_table,
+                        const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int max_kv_len, int d,
+                        int num_pages, int page_size, int max_pages_per_seq, int token_major, float scale,
+                        float lambda, int num_splits, void* workspace, size_t workspace_bytes,
+                        unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                        void* stream);
 
 /*
  * Decode without any device allocation (the pages have no counterpart: this entry

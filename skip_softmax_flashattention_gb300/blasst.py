@@ -25,6 +25,7 @@ BLASST_ERR_CUDA = -4
 BLASST_ERR_TIMEOUT = -5
 BLASST_ERR_NO_CALIBRATION = -6
 BLASST_ERR_SCRATCH_LIMIT = -7
+BLASST_ERR_PAGE_TABLE = -8
 
 BLASST_PREFILL_ELIDE_V = 0x1
 BLASST_PREFILL_P_VIA_SMEM = 0x2
@@ -67,6 +68,9 @@ def load(build_if_missing: bool = True):
     lib.blasst_decode_workspace_size.argtypes = [I, I, I, I, I, I]
     lib.blasst_decode.restype = I
     lib.blasst_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, I, P, ctypes.c_size_t, P, P, P, P]
+    lib.blasst_decode_paged.restype = I
+    lib.blasst_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, F, I, P, ctypes.c_size_t,
+                                        P, P, P, P]
     lib.blasst_decode_noalloc.restype = I
     lib.blasst_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, I, P, P, P, P]
     lib.blasst_decode_noalloc_scratch_bytes.restype = ctypes.c_size_t
@@ -131,6 +135,16 @@ def blasst_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Lkv, d, scale, lambda
                                 float(scale), float(lambda_), int(num_splits), _ptr(workspace),
                                 int(workspace_bytes), _ptr(skipped_tiles_out), _ptr(skip_map), _ptr(margins),
                                 _stream(stream))
+
+
+def blasst_decode_paged(q, k_pages, v_pages, page_table, seq_lens, o, lse, B, Hq, Hkv, max_kv_len, d, num_pages,
+                        page_size, max_pages_per_seq, token_major, scale, lambda_, num_splits, workspace,
+                        workspace_bytes, skipped_tiles_out=None, skip_map=None, margins=None, stream=None) -> int:
+    return load().blasst_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(seq_lens),
+                                      _ptr(o), _ptr(lse), B, Hq, Hkv, max_kv_len, d, num_pages, page_size,
+                                      max_pages_per_seq, int(token_major), float(scale), float(lambda_),
+                                      int(num_splits), _ptr(workspace), int(workspace_bytes),
+                                      _ptr(skipped_tiles_out), _ptr(skip_map), _ptr(margins), _stream(stream))
 
 
 def blasst_decode_noalloc(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Lkv, d, scale, lambda_, num_splits,
@@ -210,4 +224,33 @@ def decode(q, k, v, scale: float, lam: float, num_splits: int = 0, *, want_map=F
     mg = torch.empty(B, Hkv, nK, device=dev, dtype=torch.float32) if want_margins else None
     rc = blasst_decode(q3, k, v, o, lse, B, Hq, Hkv, Lkv, d, scale, lam, S, ws, ws_bytes, skipped, mp, mg, stream)
     _check(rc, "blasst_decode")
+    return {"o": o, "lse": lse, "skipped": skipped, "map": mp, "margins": mg, "num_splits": S}
+
+
+def decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_kv_len: int, page_size: int, token_major: bool,
+                 scale: float, lam: float, num_splits: int = 0, *, want_map=False, want_margins=False, stream=None):
+    """Run blasst_decode_paged on torch tensors.  k_pages/v_pages: [P, page_size, Hkv, d] (token_major)
+    or [P, Hkv, page_size, d]; page_table int32 [B, max_pages]; seq_lens int32 [B] or None.
+    Returns dict(o, lse, skipped, map, margins, num_splits)."""
+    import torch
+
+    q3 = q.reshape(q.shape[0], q.shape[1], q.shape[-1])
+    B, Hq, d = q3.shape
+    num_pages = k_pages.shape[0]
+    Hkv = k_pages.shape[2] if token_major else k_pages.shape[1]
+    nK = -(-max_kv_len // TILE)
+    rc, S = blasst_decode_num_splits(B, Hq, Hkv, max_kv_len, d, num_splits)
+    _check(rc, "blasst_decode_num_splits")
+    dev = q.device
+    ws_bytes = blasst_decode_workspace_size(B, Hq, Hkv, max_kv_len, d, S)
+    ws = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8) if ws_bytes else None
+    o = torch.empty(B, Hq, d, device=dev, dtype=q.dtype)
+    lse = torch.empty(B, Hq, device=dev, dtype=torch.float32)
+    skipped = torch.zeros(1, device=dev, dtype=torch.int64)
+    mp = torch.empty(B, Hkv, nK, device=dev, dtype=torch.uint8) if want_map else None
+    mg = torch.empty(B, Hkv, nK, device=dev, dtype=torch.float32) if want_margins else None
+    rc = blasst_decode_paged(q3, k_pages, v_pages, page_table, seq_lens, o, lse, B, Hq, Hkv, max_kv_len, d,
+                             num_pages, page_size, page_table.shape[1], token_major, scale, lam, S, ws, ws_bytes,
+                             skipped, mp, mg, stream)
+    _check(rc, "blasst_decode_paged")
     return {"o": o, "lse": lse, "skipped": skipped, "map": mp, "margins": mg, "num_splits": S}

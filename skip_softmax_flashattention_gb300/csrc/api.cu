@@ -63,6 +63,33 @@ bool encode_3d(CUtensorMap* map, const void* base, int d, int L, long long Z) {
     return r == CUDA_SUCCESS;
 }
 
+// 4-D map over a page pool of bf16 K or V, box = 64 columns x `rows` keys of one
+// head of one page.  Dimensions are ordered by stride:
+//   key-major pool [page][key][head][d]: (d, head, key, page)
+//   head-major pool [page][head][key][d]: (d, key, head, page)
+bool encode_pages(CUtensorMap* map, const void* base, int d, int page_size, int Hkv, long long num_pages,
+                  int token_major, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t e = 2;
+    cuuint64_t dims[4], strides[3];
+    cuuint32_t box[4];
+    if (token_major) {
+        dims[0] = d; dims[1] = Hkv; dims[2] = page_size; dims[3] = num_pages;
+        strides[0] = d * e; strides[1] = (cuuint64_t)Hkv * d * e; strides[2] = (cuuint64_t)page_size * Hkv * d * e;
+        box[0] = 64; box[1] = 1; box[2] = rows; box[3] = 1;
+    } else {
+        dims[0] = d; dims[1] = page_size; dims[2] = Hkv; dims[3] = num_pages;
+        strides[0] = d * e; strides[1] = (cuuint64_t)page_size * d * e; strides[2] = (cuuint64_t)Hkv * page_size * d * e;
+        box[0] = 64; box[1] = rows; box[2] = 1; box[3] = 1;
+    }
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool lambda_ok(float lambda) { return std::isfinite(lambda) && lambda >= 0.f && lambda <= 1.f; }
@@ -215,6 +242,11 @@ size_t blasst_decode_workspace_size(int B, int Hq, int Hkv, int Lkv, int d, int 
     return ((o_bytes + 255) & ~size_t(255)) + l_bytes;
 }
 
+static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, blasst::DecodeParams& p, const void* q, void* o,
+               float* lse, int B, int Hq, int Hkv, int Lkv, int d, float scale, float lambda, int num_splits,
+               void* workspace, unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+               void* stream);
+
 int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
                   int Hkv, int Lkv, int d, float scale, float lambda, int num_splits, void* workspace,
                   size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
@@ -239,12 +271,26 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
         if (!aligned16(workspace)) return BLASST_ERR_UNSUPPORTED;
     }
 
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    int* status = status_word();
-    if (!status) return BLASST_ERR_CUDA;
     CUtensorMap tk, tv;
     if (!encode_3d(&tk, k_cache, d, Lkv, (long long)B * Hkv) || !encode_3d(&tv, v_cache, d, Lkv, (long long)B * Hkv))
         return BLASST_ERR_CUDA;
+    blasst::DecodeParams p{};
+    return run_decode(tk, tv, p, q, o, lse, B, Hq, Hkv, Lkv, d, scale, lambda, num_splits, workspace,
+                      skipped_tiles_out, skip_map, margins, stream);
+}
+
+// The part of blasst_decode and blasst_decode_paged after validation: output
+// initialisation, parameters, the split pass and the merge.  `p` carries the
+// form-specific fields (page table, lengths) on entry.
+static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, blasst::DecodeParams& p, const void* q, void* o,
+               float* lse, int B, int Hq, int Hkv, int Lkv, int d, float scale, float lambda, int num_splits,
+               void* workspace, unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+               void* stream) {
+    const int nT = (Lkv + kTile - 1) / kTile;
+    const int G = Hq / Hkv;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* status = status_word();
+    if (!status) return BLASST_ERR_CUDA;
     const long long map_n = (long long)B * Hkv * nT;
     if (skipped_tiles_out && cudaMemsetAsync(skipped_tiles_out, 0, sizeof(unsigned long long), st) != cudaSuccess)
         return BLASST_ERR_CUDA;
@@ -253,7 +299,6 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
         return BLASST_ERR_CUDA;
 
     const Thresholds t = thresholds(scale, lambda);
-    blasst::DecodeParams p{};
     p.q = static_cast<const uint16_t*>(q);
     p.o = o;
     p.lse = lse;
@@ -286,6 +331,54 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
     return cuda_status(e);
 }
 
+int blasst_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* page_table,
+                        const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int max_kv_len, int d,
+                        int num_pages, int page_size, int max_pages_per_seq, int token_major, float scale,
+                        float lambda, int num_splits, void* workspace, size_t workspace_bytes,
+                        unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                        void* stream) {
+    if (!q || !k_pages || !v_pages || !page_table || !o) return BLASST_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || max_kv_len < 1 || Hq % Hkv != 0) return BLASST_ERR_INVALID_ARG;
+    if (num_pages < 1 || page_size < 1 || (token_major != 0 && token_major != 1)) return BLASST_ERR_INVALID_ARG;
+    if ((long long)max_pages_per_seq * page_size < max_kv_len) return BLASST_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || !lambda_ok(lambda)) return BLASST_ERR_INVALID_ARG;
+    const int nT = (max_kv_len + kTile - 1) / kTile;
+    if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (d != 128) return BLASST_ERR_UNSUPPORTED;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BLASST_ERR_UNSUPPORTED;
+    // a 128-key tile is whole pages (8, 16, 32 or 64 keys each) or lies inside one page
+    if (!(page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64 || page_size % kTile == 0))
+        return BLASST_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
+        (reinterpret_cast<uintptr_t>(page_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(skipped_tiles_out) & 7u))
+        return BLASST_ERR_UNSUPPORTED;
+    if (Hkv > 65535 || B > 65535) return BLASST_ERR_UNSUPPORTED;
+    const size_t need = blasst_decode_workspace_size(B, Hq, Hkv, max_kv_len, d, num_splits);
+    if (num_splits > 1) {
+        if (!workspace) return BLASST_ERR_INVALID_ARG;
+        if (workspace_bytes < need) return BLASST_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned16(workspace)) return BLASST_ERR_UNSUPPORTED;
+    }
+    const int rows = page_size < kTile ? page_size : kTile;
+    CUtensorMap tk, tv;
+    if (!encode_pages(&tk, k_pages, d, page_size, Hkv, num_pages, token_major, rows) ||
+        !encode_pages(&tv, v_pages, d, page_size, Hkv, num_pages, token_major, rows))
+        return BLASST_ERR_CUDA;
+    blasst::DecodeParams p{};
+    p.seq_lens = seq_lens;
+    p.page_table = page_table;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.page_size = page_size;
+    p.rows_per_box = rows;
+    p.token_major = token_major;
+    return run_decode(tk, tv, p, q, o, lse, B, Hq, Hkv, max_kv_len, d, scale, lambda, num_splits, workspace,
+                      skipped_tiles_out, skip_map, margins, stream);
+}
+
 int blasst_lambda(int mode, double threshold, double a, double b, double target_sparsity, long long Lkv,
                   double* lambda_out) {
     if (!lambda_out || Lkv < 1) return BLASST_ERR_INVALID_ARG;
@@ -316,7 +409,8 @@ int blasst_device_status(int clear) {
         if (cudaMemcpyToSymbol(g_blasst_status, &zero, sizeof(int)) != cudaSuccess) return BLASST_ERR_CUDA;
     }
     if (v & 2) return BLASST_ERR_CUDA;  // a kernel found its shared memory misaligned
-    return v ? BLASST_ERR_TIMEOUT : BLASST_OK;
+    if (v & 1) return BLASST_ERR_TIMEOUT;
+    return v ? BLASST_ERR_PAGE_TABLE : BLASST_OK;
 }
 
 const char* blasst_status_string(int status) {
@@ -328,6 +422,7 @@ const char* blasst_status_string(int status) {
         case BLASST_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
         case BLASST_ERR_CUDA: return "CUDA error";
         case BLASST_ERR_TIMEOUT: return "device wait timed out";
+        case BLASST_ERR_PAGE_TABLE: return "page table entry or sequence length out of range (read as zeros / clamped)";
         case BLASST_ERR_NO_CALIBRATION: return "target sparsity requested without calibration coefficients; use a threshold";
         case BLASST_ERR_SCRATCH_LIMIT: return "decode partials exceed the library's static scratch (use blasst_decode with a workspace)";
         default: return "unknown status";

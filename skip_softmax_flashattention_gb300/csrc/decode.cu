@@ -19,6 +19,17 @@
 //
 // Warp roles (224 threads): warps 0-3 softmax, warp 4 K loader, warp 5 MMA issuer
 // and TMEM owner, warp 6 V loader.
+//
+// Paged form (blasst_decode_paged): K and V live in a pool of fixed-size pages and
+// a page table maps each page-sized run of a sequence's keys to a physical page
+// (The Hitchhiker's Guide, Phase 08, Section 3, "Paged Attention": key i of
+// sequence b is row i mod page_size of page table[b][i / page_size]); every
+// sequence has its own key count.  A 128-key
+// tile is then fetched as 128 / page_size boxes (page_size < 128) or as one box
+// inside a page (page_size a multiple of 128), through a 4-D tensor map over the
+// pool.  Boxes past the end of the sequence, and boxes whose page index is out of
+// range, get an out-of-range page coordinate: TMA writes zeros there and reads no
+// memory (an out-of-range index is also reported in the device status word).
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -73,7 +84,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int G>
+template <int G, bool PAGED>
 __global__ void __launch_bounds__(224, 1)
     decode_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -81,8 +92,17 @@ __global__ void __launch_bounds__(224, 1)
     DecodeCtrl* ctrl = reinterpret_cast<DecodeCtrl*>(smem + OFF_CTRL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
-    const int t0 = (int)(((long long)s * p.nK) / p.S);
-    const int t1 = (int)(((long long)(s + 1) * p.nK) / p.S);
+    // This sequence's keys (its own count when seq_lens is given) and this split's
+    // share of its tiles: split s takes tiles [s*nT/S, (s+1)*nT/S).
+    int Lb = p.Lkv;
+    if (p.seq_lens) {
+        const int v = p.seq_lens[b];
+        Lb = min(max(v, 0), p.Lkv);
+        if (tid == 0 && s == 0 && hk == 0 && v != Lb) atomicOr(p.status, kStatusPageTable);
+    }
+    const int nTb = (Lb + kTile - 1) / kTile;
+    const int t0 = (int)(((long long)s * nTb) / p.S);
+    const int t1 = (int)(((long long)(s + 1) * nTb) / p.S);
     const int n = t1 - t0;
 
     if (tid == 0) {
@@ -112,46 +132,114 @@ __global__ void __launch_bounds__(224, 1)
     const Watchdog wd{&ctrl->abort, p.status, p.watchdog_ns};
     const int zkv = b * p.Hkv + hk;
 
+    // Paged form: box i of a key tile covers its keys [i*rows, (i+1)*rows), one page
+    // run; lane i of a loader warp reads that box's page index and issues it, so
+    // the page-table reads of a tile are in flight together.
+    const int nbox = PAGED ? kTile / p.rows_per_box : 1;
+    auto box_page = [&](int tile, int i) -> int {
+        int e = p.num_pages;  // out of range: the box reads as zeros
+        const int key = tile * kTile + i * p.rows_per_box;
+        if (i < nbox && key < Lb) {
+            const int v = p.page_table[(long long)b * p.max_pages + key / p.page_size];
+            if (v >= 0 && v < p.num_pages)
+                e = v;
+            else
+                atomicOr(p.status, kStatusPageTable);
+        }
+        return e;
+    };
+    auto issue_box = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile, int i, int pg) {
+        const int off = (tile * kTile + i * p.rows_per_box) % p.page_size;
+#pragma unroll
+        for (int x = 0; x < D / 64; ++x) {
+            uint8_t* dd = dst + x * BOX_BYTES + i * p.rows_per_box * 128;
+            if (p.token_major)
+                tma_load_4d(dd, map, bar, x * 64, hk, off, pg);
+            else
+                tma_load_4d(dd, map, bar, x * 64, off, hk, pg);
+        }
+    };
+
     if (warp == 4) {
         // ------------------------------------------------------------ K loader
-        if (lane == 0) {
-            tma_prefetch_desc(&tk);
+        if constexpr (!PAGED) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tk);
+                int issued = 0;
+                for (int j = 0; j < n; ++j) {
+                    const int ks = j % NK;
+                    if (j >= NK && !mbar_wait(&ctrl->k_empty[ks], ((j / NK) - 1) & 1, wd)) break;
+                    mbar_arrive_expect_tx(&ctrl->k_full[ks], TILE_BYTES);
+#pragma unroll
+                    for (int x = 0; x < D / 64; ++x)
+                        tma_load_3d(smem + OFF_K + ks * TILE_BYTES + x * BOX_BYTES, &tk, &ctrl->k_full[ks], x * 64,
+                                    (t0 + j) * kTile, zkv);
+                    issued = j + 1;
+                }
+                for (int j = max(0, issued - NK); j < issued; ++j)
+                    mbar_wait_drain(&ctrl->k_full[j % NK], (j / NK) & 1, kDrainNs);
+            }
+        } else {
+            if (lane == 0) tma_prefetch_desc(&tk);
             int issued = 0;
             for (int j = 0; j < n; ++j) {
                 const int ks = j % NK;
-                if (j >= NK && !mbar_wait(&ctrl->k_empty[ks], ((j / NK) - 1) & 1, wd)) break;
-                mbar_arrive_expect_tx(&ctrl->k_full[ks], TILE_BYTES);
-#pragma unroll
-                for (int x = 0; x < D / 64; ++x)
-                    tma_load_3d(smem + OFF_K + ks * TILE_BYTES + x * BOX_BYTES, &tk, &ctrl->k_full[ks], x * 64,
-                                (t0 + j) * kTile, zkv);
+                const int pg = box_page(t0 + j, lane);  // read while lane 0 waits for the slot
+                int ok = 1;
+                if (lane == 0) {
+                    if (j >= NK && !mbar_wait(&ctrl->k_empty[ks], ((j / NK) - 1) & 1, wd))
+                        ok = 0;
+                    else
+                        mbar_arrive_expect_tx(&ctrl->k_full[ks], TILE_BYTES);
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                if (lane < nbox) issue_box(&tk, smem + OFF_K + ks * TILE_BYTES, &ctrl->k_full[ks], t0 + j, lane, pg);
                 issued = j + 1;
             }
-            for (int j = max(0, issued - NK); j < issued; ++j)
-                mbar_wait_drain(&ctrl->k_full[j % NK], (j / NK) & 1, kDrainNs);
+            if (lane == 0)
+                for (int j = max(0, issued - NK); j < issued; ++j)
+                    mbar_wait_drain(&ctrl->k_full[j % NK], (j / NK) & 1, kDrainNs);
         }
     } else if (warp == 6) {
         // ------------------------------------------------------------ V loader
-        if (lane == 0) {
-            tma_prefetch_desc(&tv);
-            int comp = 0;
-            for (int j = 0; j < n; ++j) {
-                if (!mbar_wait(&ctrl->dec_full[j % ND], (j / ND) & 1, wd)) break;
-                const bool skipped = reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] != 0;
-                mbar_arrive(&ctrl->dec_free[j % ND]);
-                if (skipped) continue;  // skipped: V never loaded
-                const int vs = comp % NV;
-                if (comp >= NV && !mbar_wait(&ctrl->v_empty[vs], ((comp / NV) - 1) & 1, wd)) break;
-                mbar_arrive_expect_tx(&ctrl->v_full[vs], TILE_BYTES);
-#pragma unroll
-                for (int x = 0; x < D / 64; ++x)
-                    tma_load_3d(smem + OFF_V + vs * TILE_BYTES + x * BOX_BYTES, &tv, &ctrl->v_full[vs], x * 64,
-                                (t0 + j) * kTile, zkv);
-                ++comp;
+        if (lane == 0) tma_prefetch_desc(&tv);
+        int comp = 0;
+        for (int j = 0; j < n; ++j) {
+            const int pg = PAGED ? box_page(t0 + j, lane) : 0;  // read while lane 0 waits for the decision
+            int go = 0;  // 0: stop, 1: load V_j, 2: tile skipped
+            if (lane == 0) {
+                if (mbar_wait(&ctrl->dec_full[j % ND], (j / ND) & 1, wd)) {
+                    const bool skipped = reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] != 0;
+                    mbar_arrive(&ctrl->dec_free[j % ND]);
+                    go = skipped ? 2 : 1;  // skipped: V never loaded
+                    if (!skipped) {
+                        const int vs = comp % NV;
+                        if (comp >= NV && !mbar_wait(&ctrl->v_empty[vs], ((comp / NV) - 1) & 1, wd))
+                            go = 0;
+                        else
+                            mbar_arrive_expect_tx(&ctrl->v_full[vs], TILE_BYTES);
+                    }
+                }
             }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (go == 0) break;
+            if (go == 2) continue;
+            const int vs = comp % NV;
+            if constexpr (!PAGED) {
+                if (lane == 0) {
+#pragma unroll
+                    for (int x = 0; x < D / 64; ++x)
+                        tma_load_3d(smem + OFF_V + vs * TILE_BYTES + x * BOX_BYTES, &tv, &ctrl->v_full[vs], x * 64,
+                                    (t0 + j) * kTile, zkv);
+                }
+            } else {
+                if (lane < nbox) issue_box(&tv, smem + OFF_V + vs * TILE_BYTES, &ctrl->v_full[vs], t0 + j, lane, pg);
+            }
+            ++comp;
+        }
+        if (lane == 0)
             for (int c = max(0, comp - NV); c < comp; ++c)
                 mbar_wait_drain(&ctrl->v_full[c % NV], (c / NV) & 1, kDrainNs);
-        }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
@@ -267,7 +355,7 @@ __global__ void __launch_bounds__(224, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->s_free[ss]);
-            const bool key_ok = (t0 + j) * kTile + tid < p.Lkv;
+            const bool key_ok = (t0 + j) * kTile + tid < Lb;
             float x[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) x[g] = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
@@ -385,6 +473,11 @@ __global__ void combine_kernel(const CombineParams p) {
     const long long stride = (long long)p.B * p.Hq;
     float M = -CUDART_INF_F;
     for (int s = 0; s < p.S; ++s) M = fmaxf(M, p.lse_part[s * stride + bh]);
+    if (M == -CUDART_INF_F) {  // no split saw a key (a sequence of length 0)
+        reinterpret_cast<unsigned short*>(p.o)[bh * p.d + t] = 0;
+        if (t == 0 && p.lse) p.lse[bh] = -CUDART_INF_F;
+        return;
+    }
     float tot = 0.f;
     for (int s = 0; s < p.S; ++s) tot += __expf(p.lse_part[s * stride + bh] - M);
     const float L = M + __logf(tot);
@@ -397,13 +490,17 @@ __global__ void combine_kernel(const CombineParams p) {
     if (t == 0 && p.lse) p.lse[bh] = L;
 }
 
-template <int G>
-cudaError_t launch_g(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+template <int G, bool PAGED>
+cudaError_t launch_gp(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(p.S, p.Hkv, p.B);
-    decode_kernel<G><<<grid, 224, SMEM, stream>>>(tk, tv, p);
+    decode_kernel<G, PAGED><<<grid, 224, SMEM, stream>>>(tk, tv, p);
     return cudaGetLastError();
+}
+template <int G>
+cudaError_t launch_g(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+    return p.page_table ? launch_gp<G, true>(tk, tv, p, stream) : launch_gp<G, false>(tk, tv, p, stream);
 }
 
 }  // namespace

@@ -63,6 +63,12 @@ struct DecodeParams {
     float* margins;           // [B,Hkv,nK] or null
     int* status;
     unsigned long long watchdog_ns;
+    // Per-sequence key counts and paged K/V (blasst_decode_paged); null / 0 otherwise.
+    const int* seq_lens;      // [B]: keys of sequence b (clamped to [0, Lkv]); null: every sequence has Lkv
+    const int* page_table;    // [B, max_pages]: physical page of each page_size-key page of sequence b
+    int max_pages, num_pages, page_size;
+    int rows_per_box;         // keys per TMA box: min(page_size, 128)
+    int token_major;          // 1: pool [page][key][head][d]; 0: pool [page][head][key][d]
 };
 
 struct CombineParams {

@@ -64,7 +64,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Status bits recorded in the library's device status word.
-enum : int { kStatusTimeout = 1, kStatusMisaligned = 2 };
+enum : int { kStatusTimeout = 1, kStatusMisaligned = 2, kStatusPageTable = 4 };
 
 // Per-CTA watchdog state: the abort flag lives in shared memory, the limit in ns.
 struct Watchdog {
@@ -165,6 +165,15 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 // 3-D tiled load of one box into shared memory, completion counted on `bar` in bytes.
+// 4-D tiled load of one box; out-of-range coordinates read as zeros.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6}], "
+        "[%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y,
                                             int z) {
     asm volatile(

@@ -26,6 +26,12 @@ BLASST talk notes, "Results"):
 * ``planted70``  the ``llm`` shapes, non-causal, with K = 0 on the last 70% of the
                  key tiles: those tiles score 0 against a row max of several units,
                  so a threshold of 1e-2 skips exactly them.
+* ``paged_decode`` a ``decode`` problem whose cache is cut into pages of
+                 ``page_size`` keys and scattered over a page pool in a seeded
+                 random order (the paged-KV indirection of The Hitchhiker's Guide,
+                 Phase 08, Section 3), with a key count per sequence drawn
+                 uniformly from [min_len, max_len] unless given.  Unused pool rows
+                 hold N(0,1) values.
 
 All tensors are drawn with a ``torch.Generator`` seeded by ``seed`` on the device
 the tensors are made on; the values therefore depend on that device, and every
@@ -213,6 +219,56 @@ def small_random(seed: int, B: int, Hq: int, Hkv: int, Lq: int, Lkv: int, d: int
     if scale is None:
         scale = logit_mult / math.sqrt(d)
     return Attn(q, k, v, causal=causal, scale=scale, name=f"rand-{B}x{Hq}/{Hkv}x{Lq}x{Lkv}x{d}")
+
+
+def paged_decode(seed: int = 0, B: int = 8, Hq: int = 32, Hkv: int = 8, max_len: int = 4096, d: int = 128,
+                 page_size: int = 16, token_major: bool = True, lens=None, min_len: int = 1, spare_pages: int = 7,
+                 device="cpu", sinks: int = 4) -> Attn:
+    """``decode(seed, B, Hq, Hkv, max_len)`` plus a paged copy of its K and V.
+
+    extra: k_pages/v_pages [P, page_size, Hkv, d] (token_major) or [P, Hkv,
+    page_size, d]; page_table int32 [B, ceil(max_len/page_size)] (-1 past each
+    sequence's last page); seq_lens int32 [B]; page_size; token_major.  The
+    contiguous q/k/v stay in the object: key i of sequence b is k[b, :, i] for
+    i < seq_lens[b] (what the oracle reads)."""
+    a = decode(seed, B, Hq, Hkv, max_len, d, device, sinks)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed * 7919 + 11)
+    if lens is None:
+        lens = torch.randint(min_len, max_len + 1, (B,), generator=g)
+    lens = torch.as_tensor(lens, dtype=torch.int64).cpu()
+    npg_max = -(-max_len // page_size)
+    npg = (lens + page_size - 1) // page_size  # pages used by each sequence
+    used = int(npg.sum().item())
+    P = used + spare_pages
+    perm = torch.randperm(P, generator=g)  # pool slot of each used page, in (b, page) order
+    table = torch.full((B, npg_max), -1, dtype=torch.int32)
+    valid = torch.arange(npg_max).unsqueeze(0) < npg.unsqueeze(1)  # [B, npg_max]
+    table[valid] = perm[:used].to(torch.int32)
+    # pages of the contiguous cache: [B, npg_max, page_size, Hkv, d] (token-major view)
+    pad = npg_max * page_size - max_len
+    def pages_of(x):
+        x = x.permute(0, 2, 1, 3)  # [B, L, Hkv, d]
+        if pad:
+            x = torch.cat([x, torch.zeros(B, pad, Hkv, d, dtype=x.dtype, device=x.device)], dim=1)
+        x = x.reshape(B, npg_max, page_size, Hkv, d)
+        return x if token_major else x.permute(0, 1, 3, 2, 4)
+    shape = (P, page_size, Hkv, d) if token_major else (P, Hkv, page_size, d)
+    gd = _gen(seed + 101, device)
+    out = {}
+    sel = valid.to(device)
+    dst = table[valid].to(torch.int64).to(device)
+    for name, x in (("k_pages", a.k), ("v_pages", a.v)):
+        pool = torch.empty(shape, dtype=torch.bfloat16, device=device)
+        _fill_randn_bf16(pool.view(P, -1), gd)
+        src = pages_of(x)[sel]  # [used, ...] in (b, page) order
+        pool[dst] = src.contiguous()
+        out[name] = pool
+    a.extra.update(out)
+    a.extra.update(page_table=table.to(device), seq_lens=lens.to(torch.int32).to(device), page_size=page_size,
+                   token_major=token_major, max_len=max_len)
+    a.name = f"paged-decode-B{B}-L{max_len}-ps{page_size}-{'nhd' if token_major else 'hnd'}"
+    return a
 
 
 def l2_flush_buffer(device, nbytes: int = 512 << 20) -> torch.Tensor:

@@ -157,6 +157,39 @@ def decode_full_check(a, res, lam, S, log=None):
     return band, mx, mean, n_gpu
 
 
+def decode_paged_check(a, res, lam, S, seqs=None, log=None):
+    """A paged decode (workloads.paged_decode) against the oracle run on each
+    sequence alone: its own key count, the call's lambda and split count.  Tiles
+    past a sequence's end must stay "not visited"."""
+    lens = a.extra["seq_lens"].cpu().tolist()
+    gmap = res["map"].cpu().numpy()
+    o_gpu = res["o"].float().cpu().numpy()
+    lse_gpu = res["lse"].cpu().numpy()
+    B = len(lens)
+    assert int(res["skipped"].item()) == int((gmap == 1).sum())
+    for b in (range(B) if seqs is None else seqs):
+        L = lens[b]
+        nt = -(-L // 128)
+        what = f"{a.name} seq {b} (L={L}) lam={lam:g} S={S}"
+        assert (gmap[b, :, nt:] == 2).all(), f"{what}: tiles past the end visited"
+        if L == 0:
+            assert (o_gpu[b] == 0).all() and np.isneginf(lse_gpu[b]).all(), what
+            continue
+        q = a.q[b:b + 1].float().cpu()
+        k = a.k[b:b + 1, :, :L].float().cpu()
+        v = a.v[b:b + 1, :, :L].float().cpu()
+        # With more splits than tiles, split s = [floor(s*nt/S), floor((s+1)*nt/S)) puts
+        # every tile in a split of its own and leaves the rest empty (no contribution):
+        # the same partition as nt splits.
+        Sb = min(S, nt)
+        own = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=Sb, precision="f32")
+        band = _decisions(gmap[b:b + 1, :, :nt], own["map"], own["margin"], lam, what)
+        ref = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=Sb, forced=gmap[b:b + 1, :, :nt], precision="f32")
+        _check_rows(o_gpu[b:b + 1], lse_gpu[b:b + 1], ref["o"], ref["lse"], what)
+        if log is not None and band:
+            log.append(f"{what}: {band} tiles inside the 1e-3 margin band")
+
+
 def sample_units(rng, B, H, nQ, k, always=()):
     """k random (b, h, qtile) units plus the listed ones (first/last tiles)."""
     units = set(always)

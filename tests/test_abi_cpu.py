@@ -125,3 +125,25 @@ def test_decode_validation(kw, code):
     rc = K.blasst_decode(a["q"], a["k"], a["v"], a["o"], None, a["B"], a["Hq"], a["Hkv"], a["Lkv"], a["d"],
                          a["scale"], a["lam"], a["S"], a["ws"], a["wsb"], None, None, None, stream=0)
     assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(table=None), K.BLASST_ERR_INVALID_ARG),
+    (dict(mp=1), K.BLASST_ERR_INVALID_ARG),          # 1 page of 16 keys cannot hold 1000 keys
+    (dict(tm=2), K.BLASST_ERR_INVALID_ARG),
+    (dict(npg=0), K.BLASST_ERR_INVALID_ARG),
+    (dict(S=9), K.BLASST_ERR_INVALID_ARG),
+    (dict(ps=24, mp=42), K.BLASST_ERR_UNSUPPORTED),  # neither a divisor nor a multiple of 128
+    (dict(ps=200, mp=5), K.BLASST_ERR_UNSUPPORTED),
+    (dict(d=64), K.BLASST_ERR_UNSUPPORTED),
+    (dict(table=FAKE + 2), K.BLASST_ERR_UNSUPPORTED),
+    (dict(S=2, wsb=16), K.BLASST_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_decode_paged_validation(kw, code):
+    a = dict(q=FAKE, kp=FAKE, vp=FAKE, table=FAKE, lens=None, o=FAKE, B=2, Hq=8, Hkv=2, L=1000, d=128, npg=200,
+             ps=16, mp=63, tm=1, scale=0.1, lam=0.01, S=1, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    rc = K.blasst_decode_paged(a["q"], a["kp"], a["vp"], a["table"], a["lens"], a["o"], None, a["B"], a["Hq"],
+                               a["Hkv"], a["L"], a["d"], a["npg"], a["ps"], a["mp"], a["tm"], a["scale"], a["lam"],
+                               a["S"], a["ws"], a["wsb"], None, None, None, stream=0)
+    assert rc == code
