@@ -99,6 +99,29 @@ def test_llm_prefill_full_size():
         parity.prefill_units_check(a, res, lam, units)
 
 
+@pytest.mark.parametrize("L", [32768, 65536])
+def test_llm_prefill_long_context_sampled(L):
+    """The calibration lengths: causal LLM prefill at 32k and 64k keys (seed 1, as the
+    calibration fit uses), at lambda = 0 and at lambda = 1 where 20-40 % of the tiles
+    are skipped; the first, last and random query tiles checked against the oracle."""
+    a = parity.to_gpu(W.llm(seed=1, L=L, device="cuda"))
+    rng = np.random.default_rng(L)
+    nQ = L // 128
+    units = parity.sample_units(rng, 1, a.Hq, nQ, 3, always=[(0, 0, 0), (0, a.Hq - 1, nQ - 1)])
+    for lam in (0.0, 1.0):
+        res = K.prefill(a.q, a.k, a.v, True, a.scale, lam, want_map=True)
+        torch.cuda.synchronize()
+        n = int(res["skipped"].item())
+        assert n == int((res["map"] == 1).sum().item())
+        if lam == 0.0:
+            assert n == 0
+        else:
+            assert n > 0
+        parity.prefill_units_check(a, res, lam, units)
+    del a, res
+    torch.cuda.empty_cache()
+
+
 def test_dit_full_size():
     a = parity.to_gpu(W.dit(seed=0, device="cuda"))
     rng = np.random.default_rng(1)
