@@ -39,6 +39,13 @@
  *  - causal masking is bottom-right aligned: key c is visible to row r iff
  *    c <= r + (Lkv - Lq); key tiles with no visible key for any row of the query
  *    tile are not visited (map value 2) and are not counted;
+ *  - a sliding window of W >= 1 keys (BLASST talk notes, Q&A: the method applies
+ *    to windowed attention; the notes give no definition) is the causal mask cut
+ *    to the last W keys: with r' = r + (Lkv - Lq), key c is visible iff
+ *    r' - W < c <= r'.  W <= 0 means no window.  In decode the query row sits at
+ *    r' = Lkv - 1, and the splits cover the visited tiles only: with lo the first
+ *    tile holding a visible key, split s covers [lo + floor(s*(nT-lo)/S),
+ *    lo + floor((s+1)*(nT-lo)/S));
  *  - the tile's margin is max over voting rows of (m~ - m), +inf when any voting
  *    row has m~ = m = -inf; the tile is skipped iff margin < ln(lambda);
  *  - a row with no visible key at all gets O = 0 and lse = -inf;
@@ -73,11 +80,14 @@ typedef REAL real;
 
 static const real NEG_INF = -(real)INFINITY;
 
-/* key c visible to query row r? (bottom-right causal alignment) */
-static int visible(int causal, long r, long c, long Lq, long Lkv) {
+/* key c visible to query row r? (bottom-right causal alignment; window W > 0
+   keeps only the last W keys up to the row's own position) */
+static int visible(int causal, long window, long r, long c, long Lq, long Lkv) {
     if (c >= Lkv) return 0;
     if (!causal) return 1;
-    return c <= r + (Lkv - Lq);
+    const long rr = r + (Lkv - Lq);
+    if (c > rr) return 0;
+    return window <= 0 || c > rr - window;
 }
 
 /* s = scale * (q . k), accumulated in `real` in index order */
@@ -91,7 +101,8 @@ static real score(const real* q, const real* k, int d, real scale) {
 /* Dense attention: every row on its own, no tiling.                          */
 /* ------------------------------------------------------------------------- */
 int FN(oracle_dense)(const real* q, const real* k, const real* v, real* o, real* lse,
-                     int B, int Hq, int Hkv, int Lq, int Lkv, int d, int causal, double scale_d) {
+                     int B, int Hq, int Hkv, int Lq, int Lkv, int d, int causal, double scale_d,
+                     int window) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lkv <= 0 || d <= 0 || Hq % Hkv) return -1;
     const int G = Hq / Hkv;
     const real scale = (real)scale_d;
@@ -111,7 +122,7 @@ int FN(oracle_dense)(const real* q, const real* k, const real* v, real* o, real*
             real* orow = o + row * d;
             real M = NEG_INF;
             for (long c = 0; c < Lkv; ++c) {
-                if (visible(causal, r, c, Lq, Lkv)) {
+                if (visible(causal, window, r, c, Lq, Lkv)) {
                     s[c] = score(qr, kb + c * d, d, scale);
                     if (s[c] > M) M = s[c];
                 } else {
@@ -157,6 +168,7 @@ typedef struct {
     const real* vb;
     long Lq, Lkv;
     int d, Bc, causal;
+    long window;
     real scale;
     real lnlam;
 } pass_args;
@@ -177,7 +189,7 @@ static long run_pass(const pass_args* a, int t0, int t1, const uint8_t* forced,
         int vis = 0;
         for (int i = 0; i < n && !vis; ++i)
             for (long c = c0; c < c0 + Bc && !vis; ++c)
-                if (visible(a->causal, a->rpos[i], c, a->Lq, a->Lkv)) vis = 1;
+                if (visible(a->causal, a->window, a->rpos[i], c, a->Lq, a->Lkv)) vis = 1;
         if (!vis) {
             map[t] = 2;
             margin[t] = (real)NAN;
@@ -189,7 +201,7 @@ static long run_pass(const pass_args* a, int t0, int t1, const uint8_t* forced,
             for (int cc = 0; cc < Bc; ++cc) {
                 long c = c0 + cc;
                 real sv = NEG_INF;
-                if (visible(a->causal, a->rpos[i], c, a->Lq, a->Lkv))
+                if (visible(a->causal, a->window, a->rpos[i], c, a->Lq, a->Lkv))
                     sv = score(a->qrow[i], a->kb + c * d, d, a->scale);
                 S[(long)i * Bc + cc] = sv;
                 if (sv > best) best = sv;
@@ -276,7 +288,7 @@ long long FN(oracle_prefill_tiled)(const real* q, const real* k, const real* v, 
                                    int B, int Hq, int Hkv, int Lq, int Lkv, int d, int causal,
                                    double scale, double lambda, int Br, int Bc,
                                    const int32_t* units, int n_units, const uint8_t* forced,
-                                   uint8_t* map, real* margin) {
+                                   uint8_t* map, real* margin, int window) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lq <= 0 || Lkv <= 0 || d <= 0 || Hq % Hkv || Br <= 0 ||
         Bc <= 0)
         return -1;
@@ -327,6 +339,7 @@ long long FN(oracle_prefill_tiled)(const real* q, const real* k, const real* v, 
             a.d = d;
             a.Bc = Bc;
             a.causal = causal;
+            a.window = window;
             a.scale = (real)scale;
             a.lnlam = ln_lambda(lambda);
             long base = ((b * Hq + h) * (long)nQ + qt) * nK;
@@ -360,12 +373,15 @@ long long FN(oracle_decode_tiled)(const real* q, const real* k, const real* v, r
                                   int B, int Hq, int Hkv, int Lkv, int d, double scale,
                                   double lambda, int Bc, int num_splits, const int32_t* units,
                                   int n_units, const uint8_t* forced, uint8_t* map, real* margin,
-                                  real* o_part, real* lse_part) {
+                                  real* o_part, real* lse_part, int window) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Lkv <= 0 || d <= 0 || Hq % Hkv || Bc <= 0) return -1;
     const int G = Hq / Hkv;
     const int nK = (Lkv + Bc - 1) / Bc;
     const int S = num_splits;
-    if (S < 1 || S > nK) return -1;
+    /* first tile holding a visible key: the splits cover tiles lo .. nK-1 */
+    const long first_key = window > 0 && Lkv > window ? Lkv - window : 0;
+    const int lo = (int)(first_key / Bc);
+    if (S < 1 || S > nK - lo) return -1;
     const long nu = units ? n_units : (long)B * Hkv;
     long long skipped_total = 0;
 #pragma omp parallel reduction(+ : skipped_total)
@@ -406,12 +422,17 @@ long long FN(oracle_decode_tiled)(const real* q, const real* k, const real* v, r
             a.Lkv = Lkv;
             a.d = d;
             a.Bc = Bc;
-            a.causal = 0;
+            a.causal = window > 0;  /* the query row sits at Lkv - 1 */
+            a.window = window;
             a.scale = (real)scale;
             a.lnlam = ln_lambda(lambda);
             long base = (b * Hkv + hk) * (long)nK;
+            for (int t = 0; t < lo; ++t) { /* before the window: not visited */
+                lmap[t] = 2;
+                lmargin[t] = (real)NAN;
+            }
             for (int s = 0; s < S; ++s) {
-                int t0 = (int)(((long)s * nK) / S), t1 = (int)(((long)(s + 1) * nK) / S);
+                int t0 = lo + (int)(((long)s * (nK - lo)) / S), t1 = lo + (int)(((long)(s + 1) * (nK - lo)) / S);
                 skipped_total += run_pass(&a, t0, t1, forced ? forced + base : NULL, lmap,
                                           lmargin, O, l, m, Sb, mt, mn);
                 memcpy(Op + (long)s * G * d, O, sizeof(real) * (size_t)G * d);

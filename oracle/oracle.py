@@ -33,18 +33,18 @@ def _configure(lib):
         P = ctypes.POINTER(ct)
         f = getattr(lib, "oracle_dense" + suf)
         f.restype = ctypes.c_int
-        f.argtypes = [P, P, P, P, P] + [ctypes.c_int] * 7 + [ctypes.c_double]
+        f.argtypes = [P, P, P, P, P] + [ctypes.c_int] * 7 + [ctypes.c_double, ctypes.c_int]
         f = getattr(lib, "oracle_prefill_tiled" + suf)
         f.restype = ctypes.c_longlong
         f.argtypes = ([P, P, P, P, P] + [ctypes.c_int] * 7 + [ctypes.c_double, ctypes.c_double,
                       ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
-                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p])
+                      ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int])
         f = getattr(lib, "oracle_decode_tiled" + suf)
         f.restype = ctypes.c_longlong
         f.argtypes = ([P, P, P, P, P] + [ctypes.c_int] * 5 + [ctypes.c_double, ctypes.c_double,
                       ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
-                      ctypes.c_void_p])
+                      ctypes.c_void_p, ctypes.c_int])
     return lib
 
 
@@ -75,8 +75,9 @@ def _types(precision):
     raise ValueError(precision)
 
 
-def dense(q, k, v, causal: bool, scale: float, precision: str = "f32"):
-    """softmax(scale*QK^T + mask) V and lse for q [B,Hq,Lq,d], k/v [B,Hkv,Lkv,d]."""
+def dense(q, k, v, causal: bool, scale: float, precision: str = "f32", window: int = 0):
+    """softmax(scale*QK^T + mask) V and lse for q [B,Hq,Lq,d], k/v [B,Hkv,Lkv,d].
+    window > 0 (with causal): only the last `window` keys up to the row's position."""
     dt, ct, suf = _types(precision)
     q, k, v = _np(q, dt), _np(k, dt), _np(v, dt)
     B, Hq, Lq, d = q.shape
@@ -85,15 +86,17 @@ def dense(q, k, v, causal: bool, scale: float, precision: str = "f32"):
     lse = np.zeros((B, Hq, Lq), dt)
     rc = getattr(_load(), "oracle_dense" + suf)(
         _ptr(q, ct), _ptr(k, ct), _ptr(v, ct), _ptr(o, ct), _ptr(lse, ct),
-        B, Hq, Hkv, Lq, Lkv, d, int(causal), float(scale))
+        B, Hq, Hkv, Lq, Lkv, d, int(causal), float(scale), int(window))
     if rc != 0:
         raise ValueError("oracle_dense: bad arguments")
     return o, lse
 
 
 def prefill_tiled(q, k, v, causal: bool, scale: float, lam: float, Br: int = 128, Bc: int = 128,
-                  units=None, forced=None, precision: str = "f32", out=None):
+                  units=None, forced=None, precision: str = "f32", out=None, window: int = 0):
     """Tiled skip-softmax pass for prefill.
+
+    window: > 0 (with causal) keeps only the last `window` keys up to each row.
 
     units:  optional iterable of (b, h, qtile); only those query tiles are run
     forced: optional uint8 map [B,Hq,nQ,nK] (1 = skip) replacing the test
@@ -120,17 +123,18 @@ def prefill_tiled(q, k, v, causal: bool, scale: float, lam: float, Br: int = 128
     sk = getattr(_load(), "oracle_prefill_tiled" + suf)(
         _ptr(q, ct), _ptr(k, ct), _ptr(v, ct), _ptr(o, ct), _ptr(lse, ct),
         B, Hq, Hkv, Lq, Lkv, d, int(causal), float(scale), float(lam), Br, Bc,
-        _vp(u), nu, _vp(f), _vp(m), _vp(g))
+        _vp(u), nu, _vp(f), _vp(m), _vp(g), int(window))
     if sk < 0:
         raise ValueError("oracle_prefill_tiled: bad arguments")
     return {"o": o, "lse": lse, "map": m, "margin": g, "skipped": int(sk)}
 
 
 def decode_tiled(q, k, v, scale: float, lam: float, num_splits: int = 1, Bc: int = 128,
-                 units=None, forced=None, precision: str = "f32"):
+                 units=None, forced=None, precision: str = "f32", window: int = 0):
     """Tiled skip-softmax pass for decode (one query token; G heads per KV head).
 
     q [B,Hq,d] (or [B,Hq,1,d]), k/v [B,Hkv,Lkv,d].
+    window > 0: only the last `window` keys; the splits cover the visited tiles.
     units: optional iterable of (b, hkv); forced: optional uint8 [B,Hkv,nK].
     Returns dict(o [B,Hq,d], lse [B,Hq], map, margin, skipped, o_part, lse_part).
     """
@@ -160,7 +164,7 @@ def decode_tiled(q, k, v, scale: float, lam: float, num_splits: int = 1, Bc: int
     sk = getattr(_load(), "oracle_decode_tiled" + suf)(
         _ptr(q, ct), _ptr(k, ct), _ptr(v, ct), _ptr(o, ct), _ptr(lse, ct),
         B, Hq, Hkv, Lkv, d, float(scale), float(lam), Bc, S, _vp(u), nu, _vp(f), _vp(m), _vp(g),
-        _vp(op), _vp(lp))
+        _vp(op), _vp(lp), int(window))
     if sk < 0:
         raise ValueError("oracle_decode_tiled: bad arguments")
     return {"o": o, "lse": lse, "map": m, "margin": g, "skipped": int(sk), "o_part": op,

@@ -21,14 +21,16 @@ MUTANTS = {
     "margin-sign-flipped": ("real diff = mt[i] - mnew[i];", "real diff = mnew[i] - mt[i];"),
     "no-rescale-of-O": ("for (int x = 0; x < d; ++x) Oi[x] *= alpha;", ""),
     "no-rescale-of-l": ("l[i] = alpha * l[i] + rowsum;", "l[i] = l[i] + rowsum;"),
-    "causal-top-left": ("return c <= r + (Lkv - Lq);", "return c <= r;"),
+    "causal-top-left": ("const long rr = r + (Lkv - Lq);", "const long rr = r;"),
+    "window-edge-off-by-one": ("return window <= 0 || c > rr - window;", "return window <= 0 || c >= rr - window;"),
+    "decode-window-splits-from-zero": ("const int lo = (int)(first_key / Bc);", "const int lo = 0;"),
     "gqa-head-modulo": ("long hk = h / G;\n            for (int i = 0; i < n; ++i) {",
                         "long hk = h % Hkv;\n            for (int i = 0; i < n; ++i) {"),
     "any-row-instead-of-all": ("if (!vote) skip = 0;", "if (vote && i == 0) skip = 1; else if (!vote && i == 0) skip = 0;"),
     "skip-keeps-contribution": ("if (skip) {\n            ++skipped;", "if (0) {\n            ++skipped;"),
     "lse-missing-max": ("m[i] = m[i] + R_LOG(l[i]);", "m[i] = R_LOG(l[i]);"),
-    "split-bounds-truncated": ("int t0 = (int)(((long)s * nK) / S), t1 = (int)(((long)(s + 1) * nK) / S);",
-                               "int t0 = s * (nK / S), t1 = (s == S - 1) ? nK : (s + 1) * (nK / S);"),
+    "split-bounds-truncated": ("int t0 = lo + (int)(((long)s * (nK - lo)) / S), t1 = lo + (int)(((long)(s + 1) * (nK - lo)) / S);",
+                               "int t0 = lo + s * ((nK - lo) / S), t1 = (s == S - 1) ? nK : lo + (s + 1) * ((nK - lo) / S);"),
     "transposed-score-index": ("sv = score(a->qrow[i], a->kb + c * d, d, a->scale);",
                                "sv = score(a->qrow[i], a->kb + (c0 + (Bc - 1 - cc < a->Lkv - c0 ? Bc - 1 - cc : cc)) * d, d, a->scale);"),
 }
@@ -42,6 +44,8 @@ PINS = [
     lambda: pins.test_masked_dense_identity(),
     lambda: pins.test_decode_skip_set_closed_form_and_split_merge(),
     lambda: pins.test_skipped_contribution_closed_form(0.1),
+    lambda: pins.test_window_of_one_key_returns_that_keys_value(20, 29),
+    lambda: pins.test_decode_window_splits_cover_the_window(),
 ]
 
 

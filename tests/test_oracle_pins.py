@@ -22,7 +22,7 @@ GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
 
 # ---------------------------------------------------------------- helpers ---
-def np_dense(q, k, v, causal, scale, rows=None):
+def np_dense(q, k, v, causal, scale, rows=None, window=0):
     """Textbook attention with a library matmul (float64): softmax(scale*QK^T)V.
 
     q [B,Hq,Lq,d], k/v [B,Hkv,Lkv,d].  ``rows`` optionally restricts to a list of
@@ -42,7 +42,7 @@ def np_dense(q, k, v, causal, scale, rows=None):
                 if causal:
                     r = np.arange(Lq)[:, None]
                     c = np.arange(Lkv)[None, :]
-                    s = np.where(c <= r + (Lkv - Lq), s, -np.inf)
+                    s = np.where(band(r, c, Lq, Lkv, window), s, -np.inf)
                 M = s.max(axis=1, keepdims=True)
                 Mf = np.where(np.isfinite(M), M, 0.0)
                 p = np.exp(s - Mf)
@@ -62,7 +62,18 @@ def np_dense(q, k, v, causal, scale, rows=None):
     return out
 
 
-def closed_form_skip(q, k, causal, scale, lam, Br, Bc, Lq_rows=None):
+def band(r, c, Lq, Lkv, window):
+    """Causal visibility as a band of the score matrix: the key may not lie past the
+    row's own position r' = r + Lkv - Lq, and with a window W > 0 not W or more
+    keys before it."""
+    rr = r + (Lkv - Lq)
+    ok = c <= rr
+    if window > 0:
+        ok = ok & (rr - c < window)
+    return ok
+
+
+def closed_form_skip(q, k, causal, scale, lam, Br, Bc, Lq_rows=None, window=0):
     """Skip map from the dense score matrix, without the online loop.
 
     For query tile i and key tile j: the running max of row r after tile j is the
@@ -83,7 +94,7 @@ def closed_form_skip(q, k, causal, scale, lam, Br, Bc, Lq_rows=None):
             s = scale * q[b, h] @ k[b, h // G].T
             r = np.arange(Lq)[:, None]
             c = np.arange(Lkv)[None, :]
-            vis = np.ones_like(s, bool) if not causal else (c <= r + (Lkv - Lq))
+            vis = np.ones_like(s, bool) if not causal else band(r, c, Lq, Lkv, window)
             s = np.where(vis, s, -np.inf)
             for i in range(nQ):
                 rows = slice(i * Br, min(Lq, (i + 1) * Br))
@@ -511,3 +522,93 @@ def test_calibration_sweep_reads_sparsity_off_margins():
         r = orc.prefill_tiled(a.q, a.k, a.v, False, a.scale, lam, precision="f64")
         visited = int((r["map"] != 2).sum())
         assert S == pytest.approx(r["skipped"] / visited)
+
+
+# ------------------------------------------------------- sliding window ---
+# A window of W keys keeps, for query row r with r' = r + Lkv - Lq, the keys
+# r' - W < c <= r' (the causal mask cut to the last W keys).
+
+@pytest.mark.parametrize("Lq,Lkv", [(37, 37), (20, 29), (29, 20)])
+def test_window_of_one_key_returns_that_keys_value(Lq, Lkv):
+    """W = 1: every row attends to key r' alone, so O = V[r'] and lse = s(r, r');
+    a row with r' < 0 sees nothing (O = 0, lse = -inf)."""
+    q, k, v = rnd(1, 1, 2, Lq, 8), rnd(2, 1, 1, Lkv, 8), rnd(3, 1, 1, Lkv, 8)
+    o, lse = orc.dense(q, k, v, True, 0.5, precision="f64", window=1)
+    t = orc.prefill_tiled(q, k, v, True, 0.5, 0.0, Br=4, Bc=8, precision="f64", window=1)
+    for h in range(2):
+        for r in range(Lq):
+            rr = r + Lkv - Lq
+            for oo, ll in ((o, lse), (t["o"], t["lse"])):
+                if rr < 0:
+                    assert (oo[0, h, r] == 0).all() and ll[0, h, r] == -np.inf
+                    continue
+                np.testing.assert_allclose(oo[0, h, r], v[0, 0, rr], rtol=0, atol=1e-12)
+                assert ll[0, h, r] == pytest.approx(0.5 * float(q[0, h, r] @ k[0, 0, rr]), abs=1e-12)
+
+
+def test_window_of_two_keys_is_a_logistic_mix():
+    """W = 2: O = sigma(s1 - s0) V[r'] + sigma(s0 - s1) V[r'-1] with s1, s0 the
+    scores of keys r' and r'-1, and lse = s0 + ln(1 + e^(s1 - s0))."""
+    Lq = Lkv = 23
+    q, k, v = rnd(4, 1, 1, Lq, 8), rnd(5, 1, 1, Lkv, 8), rnd(6, 1, 1, Lkv, 8)
+    t = orc.prefill_tiled(q, k, v, True, 0.7, 0.0, Br=4, Bc=4, precision="f64", window=2)
+    for r in range(1, Lq):
+        s1 = 0.7 * float(q[0, 0, r] @ k[0, 0, r])
+        s0 = 0.7 * float(q[0, 0, r] @ k[0, 0, r - 1])
+        w1 = 1.0 / (1.0 + math.exp(s0 - s1))
+        np.testing.assert_allclose(t["o"][0, 0, r], w1 * v[0, 0, r] + (1 - w1) * v[0, 0, r - 1], rtol=0, atol=1e-12)
+        assert t["lse"][0, 0, r] == pytest.approx(s0 + math.log1p(math.exp(s1 - s0)), abs=1e-12)
+    np.testing.assert_allclose(t["o"][0, 0, 0], v[0, 0, 0], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("W", [29, 40, 10 ** 6])
+def test_window_covering_every_key_is_plain_causal(W):
+    q, k, v = rnd(7, 1, 2, 20, 8), rnd(8, 1, 1, 29, 8), rnd(9, 1, 1, 29, 8)
+    a = orc.prefill_tiled(q, k, v, True, 0.4, 0.2, Br=4, Bc=8, precision="f64")
+    b = orc.prefill_tiled(q, k, v, True, 0.4, 0.2, Br=4, Bc=8, precision="f64", window=W)
+    for key in ("o", "lse", "map"):
+        assert np.array_equal(a[key], b[key], equal_nan=True), key
+
+
+@pytest.mark.parametrize("W", [3, 8, 13])
+@pytest.mark.parametrize("Lq,Lkv", [(37, 37), (20, 45)])
+def test_window_tiled_lambda0_equals_textbook(W, Lq, Lkv):
+    q, k, v = rnd(10 + W, 1, 4, Lq, 16), rnd(20 + W, 1, 2, Lkv, 16), rnd(30 + W, 1, 2, Lkv, 16)
+    o_ref, lse_ref = np_dense(q, k, v, True, 0.3, window=W)
+    t = orc.prefill_tiled(q, k, v, True, 0.3, 0.0, Br=4, Bc=8, precision="f64", window=W)
+    o, lse = orc.dense(q, k, v, True, 0.3, precision="f64", window=W)
+    np.testing.assert_allclose(t["o"], o_ref, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(t["lse"], lse_ref, rtol=0, atol=1e-10)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-10)
+    assert t["skipped"] == 0
+
+
+@pytest.mark.parametrize("lam", [0.05, 0.3])
+def test_window_skip_set_equals_closed_form(lam):
+    q, k = rnd(41, 1, 4, 40, 8) * 2, rnd(42, 1, 2, 48, 8) * 2
+    v = rnd(43, 1, 2, 48, 8)
+    for W in (5, 12, 30):
+        t = orc.prefill_tiled(q, k, v, True, 0.6, lam, Br=4, Bc=8, precision="f64", window=W)
+        mp, mg = closed_form_skip(q, k, True, 0.6, lam, 4, 8, window=W)
+        assert np.array_equal(t["map"], mp), W
+        fin = np.isfinite(mg)
+        np.testing.assert_allclose(t["margin"][fin], mg[fin], rtol=0, atol=1e-12)
+        assert (t["map"] == 1).any() or lam < 0.1
+
+
+def test_decode_window_splits_cover_the_window():
+    """Decode with a window: tiles before the window are not visited, the splits
+    share the visited tiles (each non-empty when S <= their count), and at lambda = 0
+    the result is attention over the last W keys."""
+    B, Hq, Hkv, Lkv, d, W = 2, 4, 2, 1000, 16, 300
+    q, k, v = rnd(51, B, Hq, 1, d), rnd(52, B, Hkv, Lkv, d), rnd(53, B, Hkv, Lkv, d)
+    lo = (Lkv - W) // 128
+    for S in (1, 2, 3):
+        r = orc.decode_tiled(q, k, v, 0.4, 0.0, num_splits=S, precision="f64", window=W)
+        assert (r["map"][:, :, :lo] == 2).all() and (r["map"][:, :, lo:] == 0).all()
+        assert np.isfinite(r["lse_part"]).all(), S
+        o_ref, lse_ref = np_dense(q, k[:, :, Lkv - W:], v[:, :, Lkv - W:], False, 0.4)
+        np.testing.assert_allclose(r["o"], o_ref[:, :, 0], rtol=0, atol=1e-10)
+        np.testing.assert_allclose(r["lse"], lse_ref[:, :, 0], rtol=0, atol=1e-10)
+    with pytest.raises(ValueError):
+        orc.decode_tiled(q, k, v, 0.4, 0.0, num_splits=4, precision="f64", window=W)  # 3 visited tiles
