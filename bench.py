@@ -537,6 +537,16 @@ def run_sweep(args):
     # LLM prefill (the bench workload) at lambda = a / L
     a = W.llm(seed=0, L=16384, device=dev)
     prefill_case("llm-prefill-L16384", a, [0.0, 4 / 16384, 40 / 16384, 0.3, 1.0])
+    # the same with a causal sliding window of 4096 keys
+    pairs_w = sum(min(r + 1, 4096) for r in range(16384))
+    for lam in (0.0, 40 / 4096):
+        r = K.prefill(a.q, a.k, a.v, True, a.scale, lam, window=4096)
+        torch.cuda.synchronize()
+        sk = int(r["skipped"].item())
+        o = r["o"]
+        ms = _time_ms(lambda: K.prefill(a.q, a.k, a.v, True, a.scale, lam, out=o, window=4096), flush)
+        emit({"sweep": "llm-prefill-L16384-window4096", "kind": "prefill", "lambda": lam, "ms": ms,
+              "skipped_tiles": sk, "dense_tflops": 4.0 * a.B * a.Hq * a.d * pairs_w / (ms * 1e-3) / 1e12})
     del a
     # planted-70: last 70% of key tiles hold K = 0
     a = W.planted70(seed=0, L=16384, device=dev)
@@ -579,22 +589,26 @@ def run_sweep(args):
 
     # paged decode (blasst_decode_paged): the same shapes with the cache in pages
     # scattered over a pool, at full length and with 16k-32k keys per sequence
-    for ps, tmaj, lens_kind in ((16, True, "full"), (128, False, "full"), (16, True, "16k-32k")):
+    for ps, tmaj, lens_kind, win in ((16, True, "full", 0), (128, False, "full", 0), (16, True, "16k-32k", 0),
+                                     (16, True, "full", 4096)):
         a = W.paged_decode(seed=0, B=64, Hq=32, Hkv=8, max_len=32768, page_size=ps, token_major=tmaj,
                            lens=[32768] * 64 if lens_kind == "full" else None, min_len=16384, device=dev)
         e = a.extra
-        keys = int(e["seq_lens"].sum().item())
+        lens_t = e["seq_lens"].to(torch.int64)
+        first = (lens_t - win).clamp(min=0) if win else torch.zeros_like(lens_t)
+        keys = int((lens_t - first).sum().item())
         for lam in (0.0, 0.3):
             r = K.decode_paged(a.q, e["k_pages"], e["v_pages"], e["page_table"], e["seq_lens"], 32768, ps, tmaj,
-                               a.scale, lam, 0)
+                               a.scale, lam, 0, window=win)
             torch.cuda.synchronize()
             sk = int(r["skipped"].item())
             Sx = r["num_splits"]
             ms = _time_ms(lambda: K.decode_paged(a.q, e["k_pages"], e["v_pages"], e["page_table"], e["seq_lens"],
-                                                 32768, ps, tmaj, a.scale, lam, Sx), flush)
-            tiles_v = int(((e["seq_lens"] + 127) // 128).sum().item()) * a.Hkv
+                                                 32768, ps, tmaj, a.scale, lam, Sx, window=win), flush)
+            tiles_v = int(((lens_t + 127) // 128 - first // 128).sum().item()) * a.Hkv
             kv = keys * a.Hkv * a.d * 2 + 128 * a.d * 2 * (tiles_v - sk)  # K of every key, V of computed tiles
-            emit({"sweep": f"paged-decode-B64-L32768-ps{ps}-{'key' if tmaj else 'head'}-major-{lens_kind}",
+            emit({"sweep": f"paged-decode-B64-L32768-ps{ps}-{'key' if tmaj else 'head'}-major-{lens_kind}"
+                           + (f"-window{win}" if win else ""),
                   "kind": "decode", "splits": Sx, "lambda": lam, "ms": ms, "skip_pct": 100.0 * sk / tiles_v,
                   "kv_gbs": kv / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": kv / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"]})
         del a, e

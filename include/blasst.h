@@ -112,6 +112,20 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
                       unsigned flags, void* stream);
 
 /*
+ * Prefill with a causal sliding window of `window` keys (BLASST talk notes, Q&A: the
+ * method carries over to windowed attention; the notes give no definition, and this
+ * library takes the causal mask cut to the last `window` keys): query row r sees
+ * keys c with r' - window < c <= r', r' = r + Lkv - Lq.  Key tiles outside every
+ * row's window are not visited (skip map 2).  Arguments as blasst_prefill_ex with
+ * causal implied; window >= 1 (else BLASST_ERR_INVALID_ARG); flags may hold
+ * BLASST_PREFILL_ELIDE_V, the other variant flags give BLASST_ERR_UNSUPPORTED.
+ */
+int blasst_prefill_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                          int Hkv, int Lq, int Lkv, int d, int window, float scale, float lambda,
+                          unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                          unsigned flags, void* stream);
+
+/*
  * Split-KV plan for decode.  Split s of S covers key tiles
  * [floor(s*nT/S), floor((s+1)*nT/S)), nT = ceil(Lkv/128); each split is an
  * independent pass (its running max starts at -inf), so S changes which tiles are
@@ -159,9 +173,13 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
  *                max_kv_len (NULL: every sequence has max_kv_len keys).  A sequence
  *                of length 0 gives o = 0, lse = -inf.
  *   page_size    8, 16, 32, 64, or a multiple of 128 (else BLASST_ERR_UNSUPPORTED).
- *   num_splits   as for blasst_decode, planned on max_kv_len: split s of sequence b
- *                covers its tiles [floor(s*nT_b/S), floor((s+1)*nT_b/S)), nT_b =
- *                ceil(seq_lens[b]/128); a split with no tile contributes nothing.
+ *   window       0, or a sliding window: only the last `window` keys of each
+ *                sequence are attended (keys c >= seq_lens[b] - window).
+ *   num_splits   as for blasst_decode, planned on max_kv_len (or on the window when
+ *                it is shorter): split s of sequence b covers its visited tiles
+ *                [lo + floor(s*(nT_b-lo)/S), lo + floor((s+1)*(nT_b-lo)/S)), nT_b =
+ *                ceil(seq_lens[b]/128), lo = the tile holding the first key in the
+ *                window (0 without one); a split with no tile contributes nothing.
  *   workspace    as for blasst_decode (blasst_decode_workspace_size with max_kv_len).
  *   skip_map / margins  nullable [B, Hkv, ceil(max_kv_len/128)], tiles past a
  *                sequence's end stay "not visited" (2 / NaN).
@@ -172,9 +190,9 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
  *   weight; they must hold finite values (a zeroed or previously written pool).
  */
 int blasst_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* page_table,
-                        const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int max_kv_len, int d,
-                        int num_pages, int page_size, int max_pages_per_seq, int token_major, float scale,
-                        float lambda, int num_splits, void* workspace, size_t workspace_bytes,
+                        const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int max_kv_len,
+                        int window, int d, int num_pages, int page_size, int max_pages_per_seq, int token_major,
+                        float scale, float lambda, int num_splits, void* workspace, size_t workspace_bytes,
                         unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
                         void* stream);
 

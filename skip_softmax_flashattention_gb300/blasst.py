@@ -69,8 +69,10 @@ def load(build_if_missing: bool = True):
     lib.blasst_decode.restype = I
     lib.blasst_decode.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, I, P, ctypes.c_size_t, P, P, P, P]
     lib.blasst_decode_paged.restype = I
-    lib.blasst_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, F, F, I, P, ctypes.c_size_t,
-                                        P, P, P, P]
+    lib.blasst_decode_paged.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, I, I, I, I, I, F, F, I, P,
+                                        ctypes.c_size_t, P, P, P, P]
+    lib.blasst_prefill_window.restype = I
+    lib.blasst_prefill_window.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, F, P, P, P, ctypes.c_uint, P]
     lib.blasst_decode_noalloc.restype = I
     lib.blasst_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, I, P, P, P, P]
     lib.blasst_decode_noalloc_scratch_bytes.restype = ctypes.c_size_t
@@ -137,11 +139,18 @@ def blasst_decode(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Lkv, d, scale, lambda
                                 _stream(stream))
 
 
-def blasst_decode_paged(q, k_pages, v_pages, page_table, seq_lens, o, lse, B, Hq, Hkv, max_kv_len, d, num_pages,
-                        page_size, max_pages_per_seq, token_major, scale, lambda_, num_splits, workspace,
+def blasst_prefill_window(q, k, v, o, lse, B, Hq, Hkv, Lq, Lkv, d, window, scale, lambda_, skipped_tiles_out=None,
+                          skip_map=None, margins=None, flags=0, stream=None) -> int:
+    return load().blasst_prefill_window(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, Hq, Hkv, Lq, Lkv, d,
+                                        int(window), float(scale), float(lambda_), _ptr(skipped_tiles_out),
+                                        _ptr(skip_map), _ptr(margins), int(flags), _stream(stream))
+
+
+def blasst_decode_paged(q, k_pages, v_pages, page_table, seq_lens, o, lse, B, Hq, Hkv, max_kv_len, window, d,
+                        num_pages, page_size, max_pages_per_seq, token_major, scale, lambda_, num_splits, workspace,
                         workspace_bytes, skipped_tiles_out=None, skip_map=None, margins=None, stream=None) -> int:
     return load().blasst_decode_paged(_ptr(q), _ptr(k_pages), _ptr(v_pages), _ptr(page_table), _ptr(seq_lens),
-                                      _ptr(o), _ptr(lse), B, Hq, Hkv, max_kv_len, d, num_pages, page_size,
+                                      _ptr(o), _ptr(lse), B, Hq, Hkv, max_kv_len, int(window), d, num_pages, page_size,
                                       max_pages_per_seq, int(token_major), float(scale), float(lambda_),
                                       int(num_splits), _ptr(workspace), int(workspace_bytes),
                                       _ptr(skipped_tiles_out), _ptr(skip_map), _ptr(margins), _stream(stream))
@@ -183,8 +192,9 @@ def _check(rc, what):
 
 
 def prefill(q, k, v, causal: bool, scale: float, lam: float, *, want_map=False, want_margins=False,
-            flags=0, out=None, stream=None):
-    """Run blasst_prefill_ex on torch tensors; returns dict(o, lse, skipped, map, margins)."""
+            flags=0, out=None, stream=None, window=0):
+    """Run blasst_prefill_ex (blasst_prefill_window when window > 0, causal implied) on
+    torch tensors; returns dict(o, lse, skipped, map, margins)."""
     import torch
 
     B, Hq, Lq, d = q.shape
@@ -196,9 +206,14 @@ def prefill(q, k, v, causal: bool, scale: float, lam: float, *, want_map=False, 
     skipped = torch.zeros(1, device=dev, dtype=torch.int64)
     mp = torch.empty(B, Hq, nQ, nK, device=dev, dtype=torch.uint8) if want_map else None
     mg = torch.empty(B, Hq, nQ, nK, device=dev, dtype=torch.float32) if want_margins else None
-    rc = blasst_prefill_ex(q, k, v, o, lse, B, Hq, Hkv, Lq, Lkv, d, causal, scale, lam, skipped, mp, mg, flags,
-                           stream)
-    _check(rc, "blasst_prefill_ex")
+    if window > 0:
+        rc = blasst_prefill_window(q, k, v, o, lse, B, Hq, Hkv, Lq, Lkv, d, window, scale, lam, skipped, mp, mg,
+                                   flags, stream)
+        _check(rc, "blasst_prefill_window")
+    else:
+        rc = blasst_prefill_ex(q, k, v, o, lse, B, Hq, Hkv, Lq, Lkv, d, causal, scale, lam, skipped, mp, mg, flags,
+                               stream)
+        _check(rc, "blasst_prefill_ex")
     return {"o": o, "lse": lse, "skipped": skipped, "map": mp, "margins": mg}
 
 
@@ -228,7 +243,8 @@ def decode(q, k, v, scale: float, lam: float, num_splits: int = 0, *, want_map=F
 
 
 def decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_kv_len: int, page_size: int, token_major: bool,
-                 scale: float, lam: float, num_splits: int = 0, *, want_map=False, want_margins=False, stream=None):
+                 scale: float, lam: float, num_splits: int = 0, *, want_map=False, want_margins=False, stream=None,
+                 window: int = 0):
     """Run blasst_decode_paged on torch tensors.  k_pages/v_pages: [P, page_size, Hkv, d] (token_major)
     or [P, Hkv, page_size, d]; page_table int32 [B, max_pages]; seq_lens int32 [B] or None.
     Returns dict(o, lse, skipped, map, margins, num_splits)."""
@@ -239,7 +255,9 @@ def decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_kv_len: int, pag
     num_pages = k_pages.shape[0]
     Hkv = k_pages.shape[2] if token_major else k_pages.shape[1]
     nK = -(-max_kv_len // TILE)
-    rc, S = blasst_decode_num_splits(B, Hq, Hkv, max_kv_len, d, num_splits)
+    # an automatic split count is planned on the keys one sequence reads
+    plan_len = min(max_kv_len, window + TILE - 1) if (window > 0 and num_splits == 0) else max_kv_len
+    rc, S = blasst_decode_num_splits(B, Hq, Hkv, plan_len, d, num_splits)
     _check(rc, "blasst_decode_num_splits")
     dev = q.device
     ws_bytes = blasst_decode_workspace_size(B, Hq, Hkv, max_kv_len, d, S)
@@ -249,7 +267,7 @@ def decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_kv_len: int, pag
     skipped = torch.zeros(1, device=dev, dtype=torch.int64)
     mp = torch.empty(B, Hkv, nK, device=dev, dtype=torch.uint8) if want_map else None
     mg = torch.empty(B, Hkv, nK, device=dev, dtype=torch.float32) if want_margins else None
-    rc = blasst_decode_paged(q3, k_pages, v_pages, page_table, seq_lens, o, lse, B, Hq, Hkv, max_kv_len, d,
+    rc = blasst_decode_paged(q3, k_pages, v_pages, page_table, seq_lens, o, lse, B, Hq, Hkv, max_kv_len, window, d,
                              num_pages, page_size, page_table.shape[1], token_major, scale, lam, S, ws, ws_bytes,
                              skipped, mp, mg, stream)
     _check(rc, "blasst_decode_paged")

@@ -124,10 +124,34 @@ int blasst_prefill(const void* q, const void* k, const void* v, void* o, float* 
                              nullptr, nullptr, 0u, stream);
 }
 
+static int prefill_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Lq, int Lkv, int d, int causal, int window, float scale, float lambda,
+                        unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                        unsigned flags, void* stream);
+
 int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
                       int Hkv, int Lq, int Lkv, int d, int causal, float scale, float lambda,
                       unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
                       unsigned flags, void* stream) {
+    return prefill_impl(q, k, v, o, lse, B, Hq, Hkv, Lq, Lkv, d, causal, 0, scale, lambda, skipped_tiles_out,
+                        skip_map, margins, flags, stream);
+}
+
+int blasst_prefill_window(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                          int Hkv, int Lq, int Lkv, int d, int window, float scale, float lambda,
+                          unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                          unsigned flags, void* stream) {
+    if (window < 1) return BLASST_ERR_INVALID_ARG;
+    if (flags & (BLASST_PREFILL_P_VIA_SMEM | BLASST_PREFILL_ONE_QTILE | BLASST_PREFILL_WIDE))
+        return BLASST_ERR_UNSUPPORTED;  // the window is built into the default kernel only
+    return prefill_impl(q, k, v, o, lse, B, Hq, Hkv, Lq, Lkv, d, 1, window, scale, lambda, skipped_tiles_out,
+                        skip_map, margins, flags, stream);
+}
+
+static int prefill_impl(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+                        int Lq, int Lkv, int d, int causal, int window, float scale, float lambda,
+                        unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
+                        unsigned flags, void* stream) {
     if (!q || !k || !v || !o) return BLASST_ERR_INVALID_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || Lq < 1 || Lkv < 1 || Hq % Hkv != 0) return BLASST_ERR_INVALID_ARG;
     if (causal != 0 && causal != 1) return BLASST_ERR_INVALID_ARG;
@@ -178,6 +202,7 @@ int blasst_prefill_ex(const void* q, const void* k, const void* v, void* o, floa
     p.status = status;
     p.watchdog_ns = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? kShortWatchdogNs : kWatchdogNs;
     p.elide_v = (flags & BLASST_PREFILL_ELIDE_V) ? 1 : 0;
+    p.window = window;
     p.test_stall = (flags & BLASST_FLAG_TEST_SHORT_WATCHDOG) ? 1 : 0;
     // CTA order: under a causal mask the query tiles differ in work, so hand them out
     // longest-first within bands of whole K/V-head groups whose K and V fit in half
@@ -332,12 +357,13 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, blasst::Deco
 }
 
 int blasst_decode_paged(const void* q, const void* k_pages, const void* v_pages, const int* page_table,
-                        const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int max_kv_len, int d,
-                        int num_pages, int page_size, int max_pages_per_seq, int token_major, float scale,
-                        float lambda, int num_splits, void* workspace, size_t workspace_bytes,
+                        const int* seq_lens, void* o, float* lse, int B, int Hq, int Hkv, int max_kv_len,
+                        int window, int d, int num_pages, int page_size, int max_pages_per_seq, int token_major,
+                        float scale, float lambda, int num_splits, void* workspace, size_t workspace_bytes,
                         unsigned long long* skipped_tiles_out, unsigned char* skip_map, float* margins,
                         void* stream) {
     if (!q || !k_pages || !v_pages || !page_table || !o) return BLASST_ERR_INVALID_ARG;
+    if (window < 0) return BLASST_ERR_INVALID_ARG;
     if (B < 1 || Hq < 1 || Hkv < 1 || max_kv_len < 1 || Hq % Hkv != 0) return BLASST_ERR_INVALID_ARG;
     if (num_pages < 1 || page_size < 1 || (token_major != 0 && token_major != 1)) return BLASST_ERR_INVALID_ARG;
     if ((long long)max_pages_per_seq * page_size < max_kv_len) return BLASST_ERR_INVALID_ARG;
@@ -375,6 +401,7 @@ int blasst_decode_paged(const void* q, const void* k_pages, const void* v_pages,
     p.page_size = page_size;
     p.rows_per_box = rows;
     p.token_major = token_major;
+    p.window = window;
     return run_decode(tk, tv, p, q, o, lse, B, Hq, Hkv, max_kv_len, d, scale, lambda, num_splits, workspace,
                       skipped_tiles_out, skip_map, margins, stream);
 }

@@ -101,8 +101,12 @@ __global__ void __launch_bounds__(224, 1)
         if (tid == 0 && s == 0 && hk == 0 && v != Lb) atomicOr(p.status, kStatusPageTable);
     }
     const int nTb = (Lb + kTile - 1) / kTile;
-    const int t0 = (int)(((long long)s * nTb) / p.S);
-    const int t1 = (int)(((long long)(s + 1) * nTb) / p.S);
+    // Sliding window: only keys [first_key, Lb); the splits share the tiles from the
+    // one holding first_key.
+    const int first_key = (p.window > 0 && Lb > p.window) ? Lb - p.window : 0;
+    const int tlo = first_key / kTile;
+    const int t0 = tlo + (int)(((long long)s * (nTb - tlo)) / p.S);
+    const int t1 = tlo + (int)(((long long)(s + 1) * (nTb - tlo)) / p.S);
     const int n = t1 - t0;
 
     if (tid == 0) {
@@ -139,7 +143,7 @@ __global__ void __launch_bounds__(224, 1)
     auto box_page = [&](int tile, int i) -> int {
         int e = p.num_pages;  // out of range: the box reads as zeros
         const int key = tile * kTile + i * p.rows_per_box;
-        if (i < nbox && key < Lb) {
+        if (i < nbox && key < Lb && key + p.rows_per_box > first_key) {  // boxes before the window read zeros
             const int v = p.page_table[(long long)b * p.max_pages + key / p.page_size];
             if (v >= 0 && v < p.num_pages)
                 e = v;
@@ -355,7 +359,8 @@ __global__ void __launch_bounds__(224, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->s_free[ss]);
-            const bool key_ok = (t0 + j) * kTile + tid < Lb;
+            const int key = (t0 + j) * kTile + tid;
+            const bool key_ok = key < Lb && key >= first_key;
             float x[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) x[g] = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;

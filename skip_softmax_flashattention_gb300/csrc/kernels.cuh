@@ -27,6 +27,7 @@ struct PrefillParams {
     int elide_v;
     int test_stall;           // test only: the MMA issuer first waits on a barrier nothing arrives on
     int band;                 // (b, h) pairs per scheduling band, see prefill_cta_coords
+    int window;               // > 0 (causal only): row r sees keys r' - window < c <= r', r' = r + Lkv - Lq
 };
 
 // Position of this CTA in a one-dimensional prefill grid of nunits * B * Hq CTAs.
@@ -69,6 +70,7 @@ struct DecodeParams {
     int max_pages, num_pages, page_size;
     int rows_per_box;         // keys per TMA box: min(page_size, 128)
     int token_major;          // 1: pool [page][key][head][d]; 0: pool [page][head][key][d]
+    int window;               // > 0: only the last `window` keys of each sequence
 };
 
 struct CombineParams {

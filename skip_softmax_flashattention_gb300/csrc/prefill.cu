@@ -480,7 +480,7 @@ struct Prefill2Cfg {
 constexpr int kRegsLaunch2 = 168, kRegsSoftmax2 = 216, kRegsProducer2 = 72;
 static_assert(2 * 128 * kRegsSoftmax2 + 128 * kRegsProducer2 <= 384 * kRegsLaunch2, "register split");
 
-template <int D>
+template <int D, bool WIN>
 __global__ void __launch_bounds__(384, 1)
     prefill2_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const PrefillParams p) {
@@ -498,20 +498,42 @@ __global__ void __launch_bounds__(384, 1)
     const int pi = p.causal ? (npairs - 1 - unit) : unit;  // heavy pairs first
     const int hk = h / G;
     const int off = p.Lkv - p.Lq;
-    int nvis[2];
+    // Key tiles [lo[w], hi[w]) hold a key visible to some row of query tile w: all of
+    // them without a mask, up to the diagonal under the causal mask, and with a
+    // sliding window of W keys from the tile holding its first row's first visible
+    // key (that row sees keys r' - W < c <= r', r' = r + Lkv - Lq).
+    int lo[2], hi[2];
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
         const int qt = 2 * pi + w;
-        if (qt >= p.nQ) {
-            nvis[w] = 0;
-        } else if (p.causal) {
+        lo[w] = hi[w] = 0;
+        if (qt >= p.nQ) continue;
+        if (p.causal) {
             const int maxkey = min(p.Lq, (qt + 1) * kTile) - 1 + off;
-            nvis[w] = maxkey < 0 ? 0 : min(p.nK, maxkey / kTile + 1);
+            if (maxkey < 0) continue;
+            hi[w] = min(p.nK, maxkey / kTile + 1);
+            if constexpr (WIN) {
+                const int minkey = qt * kTile + off - p.window + 1;
+                lo[w] = minkey > 0 ? minkey / kTile : 0;
+            }
         } else {
-            nvis[w] = p.nK;
+            hi[w] = p.nK;
         }
     }
-    const int N = max(nvis[0], nvis[1]);
+    // The CTA walks key tiles base, base+1, ... (index i); tile w's own iteration j
+    // is index s0[w] + j.  The two ranges overlap or touch (tile B's window starts
+    // at most one key tile after A's, and A's range reaches at least that far), so
+    // every index below N is visited by at least one of the tiles.
+    // (without a window every range starts at key tile 0: base and s0 are zero)
+    const int base = WIN ? (hi[0] > lo[0] ? lo[0] : lo[1]) : 0;
+    int nvis[2], s0[2];
+    int N = 0;
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        nvis[w] = hi[w] - lo[w];
+        s0[w] = WIN ? lo[w] - base : 0;
+        if (nvis[w] > 0) N = max(N, hi[w] - base);
+    }
 
     if (tid == 0) {
         mbar_init(&ctrl->q_full, 1);
@@ -569,15 +591,18 @@ __global__ void __launch_bounds__(384, 1)
                 const int ks = m % C::NK;
                 if (m >= C::NK) {
                     const int prev = m - C::NK;
-                    for (int w = 0; w < 2; ++w)
-                        if (prev < nvis[w] && !mbar_wait(&ctrl->rel[w][(unsigned)prev % NR], ((unsigned)prev / NR) & 1u, wd))
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int jp = prev - s0[w];  // tile w's iteration that read K_prev
+                        if (jp >= 0 && jp < nvis[w] && !mbar_wait(&ctrl->rel[w][(unsigned)jp % NR], ((unsigned)jp / NR) & 1u, wd))
                             return false;
+                    }
                 }
                 mbar_arrive_expect_tx(&ctrl->k_full[ks], C::TILE_BYTES);
 #pragma unroll
                 for (int x = 0; x < D / 64; ++x)
                     tma_load_3d(smem + C::OFF_K + ks * C::TILE_BYTES + x * C::BOX_BYTES, &tk, &ctrl->k_full[ks],
-                                x * 64, m * kTile, zkv);
+                                x * 64, (base + m) * kTile, zkv);
                 issued_k = m + 1;
                 return true;
             };
@@ -585,10 +610,13 @@ __global__ void __launch_bounds__(384, 1)
                 const int vs = m % C::NV;
                 if (m >= C::NV) {
                     const int prev = m - C::NV;
-                    for (int w = 0; w < 2; ++w)
-                        if (prev < nvis[w] &&
-                            !mbar_wait(&ctrl->rel[w][(unsigned)(prev + 1) % NR], ((unsigned)(prev + 1) / NR) & 1u, wd))
+#pragma unroll
+                    for (int w = 0; w < 2; ++w) {
+                        const int jp = prev - s0[w];  // tile w's iteration that read V_prev
+                        if (jp >= 0 && jp < nvis[w] &&
+                            !mbar_wait(&ctrl->rel[w][(unsigned)(jp + 1) % NR], ((unsigned)(jp + 1) / NR) & 1u, wd))
                             return false;
+                    }
                 }
                 bool need = true;
                 if (p.elide_v) {
@@ -599,10 +627,12 @@ __global__ void __launch_bounds__(384, 1)
                     // may be read for any key tile without having watched the earlier ones:
                     // tile B is asked only when tile A does not keep the tile.
                     need = false;
+#pragma unroll
                     for (int w = 0; w < 2 && !need; ++w) {
-                        if (m >= nvis[w]) continue;
+                        const int jm = m - s0[w];
+                        if (jm < 0 || jm >= nvis[w]) continue;
                         int dv = 0;
-                        if (!spin_until_ge(&ctrl->dec[w], 2 * (m + 1), dv, wd)) return false;
+                        if (!spin_until_ge(&ctrl->dec[w], 2 * (jm + 1), dv, wd)) return false;
                         need = (dv & 1) != 0;
                     }
                 }
@@ -611,7 +641,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                     for (int x = 0; x < D / 64; ++x)
                         tma_load_3d(smem + C::OFF_V + vs * C::TILE_BYTES + x * C::BOX_BYTES, &tv, &ctrl->v_full[vs],
-                                    x * 64, m * kTile, zkv);
+                                    x * 64, (base + m) * kTile, zkv);
                 } else {
                     mbar_arrive(&ctrl->v_full[vs]);  // completes the slot's phase without data
                 }
@@ -639,7 +669,7 @@ __global__ void __launch_bounds__(384, 1)
     } else if (warp == 9 || warp == 10) {
         // ------------------------------------------------------------ MMA issuers (warp 9: tile A, warp 10: tile B)
         const int w = warp - 9;
-        const int n = nvis[w];
+        const int n = w ? nvis[1] : nvis[0];
         if (lane == 0 && n > 0) {
             constexpr uint32_t kIdescS = idesc_bf16(128, 128, false, false);
             constexpr uint32_t kIdescO = idesc_bf16(128, D, false, true);
@@ -672,11 +702,12 @@ __global__ void __launch_bounds__(384, 1)
                 }
             };
             bool ok = (p.test_stall && w == 0) ? mbar_wait(&ctrl->never, 0, wd) : true;
+            const int sw = w ? s0[1] : s0[0];  // iteration j of this tile reads K/V index sw + j
             ok = ok && mbar_wait(&ctrl->q_full, 0, wd);
-            ok = ok && mbar_wait(&ctrl->k_full[0], 0, wd);
+            ok = ok && mbar_wait(&ctrl->k_full[sw % C::NK], (sw / C::NK) & 1, wd);
             if (ok) {
                 tc_fence_after();
-                issue_qk(0);
+                issue_qk(sw);
                 commit();
             }
             volatile int* turn = &ctrl->turn;
@@ -699,16 +730,17 @@ __global__ void __launch_bounds__(384, 1)
             };
             int npv = 0;
             unsigned long long nskip = 0;
-            const long long mapbase = ((long long)(b * p.Hq + h) * p.nQ + (2 * pi + w)) * p.nK;
+            const long long mapbase = ((long long)(b * p.Hq + h) * p.nQ + (2 * pi + w)) * p.nK + (w ? lo[1] : lo[0]);
             for (int j = 0; j < n && ok; ++j) {
-                const int vs = j % C::NV;
+                const int ij = sw + j;
+                const int vs = ij % C::NV;
                 if (!(ok = mbar_wait(&ctrl->p_full[w][0], j & 1, wd))) break;
                 // all four warps have voted: the tile is kept iff one of them raised keep[w] to j+1
                 const bool skip = reinterpret_cast<volatile int*>(ctrl->keep)[w] <= j;
                 if (p.elide_v) reinterpret_cast<volatile int*>(ctrl->dec)[w] = 2 * (j + 1) + (skip ? 0 : 1);
                 // V_j must have landed before its slot is released, also when the tile is skipped
-                if (!(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
-                if (j + 1 < n && !(ok = mbar_wait(&ctrl->k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1, wd))) break;
+                if (!(ok = mbar_wait(&ctrl->v_full[vs], (ij / C::NV) & 1, wd))) break;
+                if (j + 1 < n && !(ok = mbar_wait(&ctrl->k_full[(ij + 1) % C::NK], ((ij + 1) / C::NK) & 1, wd))) break;
                 if (!(ok = take_turn())) break;
                 tc_fence_after();
                 if (!skip) issue_pv_half(vs, 0, npv == 0);
@@ -725,7 +757,7 @@ __global__ void __launch_bounds__(384, 1)
                     issue_pv_half(vs, 1, npv == 0);
                     ++npv;
                 }
-                if (j + 1 < n) issue_qk(j + 1);
+                if (j + 1 < n) issue_qk(ij + 1);
                 commit();  // commit j+1: PV_w(j) and QK_w(j+1)
                 *turn = 1 - w;
             }
@@ -743,7 +775,8 @@ __global__ void __launch_bounds__(384, 1)
         const int w = warp >> 2;
         const int t = tid & 127;
         const int qt = 2 * pi + w;
-        const int n = nvis[w];
+        const int n = w ? nvis[1] : nvis[0];
+        const int lo_w = w ? lo[1] : lo[0];
         const int rabs = qt * kTile + t;
         const bool valid = rabs < p.Lq;
         const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
@@ -764,11 +797,14 @@ __global__ void __launch_bounds__(384, 1)
             tmem_ld32(tl + s_col + 96, xr + 96);
             tmem_ld_wait();
             fence_regs<128>(xr);
-            const int lim = min(p.Lkv - 1, lim_row) - j * kTile;
-            if (lim < kTile - 1) {
+            const int kt = (lo_w + j) * kTile;  // first key of this key tile
+            const int lim = min(p.Lkv - 1, lim_row) - kt;
+            // sliding window: keys before r' - W + 1 are outside it
+            const int lim_lo = WIN ? rabs + off - p.window + 1 - kt : 0;
+            if (lim < kTile - 1 || lim_lo > 0) {
 #pragma unroll
                 for (int c = 0; c < kTile; ++c)
-                    if (c > lim) xr[c] = __float_as_uint(-CUDART_INF_F);
+                    if (c > lim || c < lim_lo) xr[c] = __float_as_uint(-CUDART_INF_F);
             }
             const float mt = row_max128(xr);
             const float mnew = fmaxf(m_exact, mt);
@@ -898,10 +934,11 @@ template <int D>
 cudaError_t launch2_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const PrefillParams& p,
                       cudaStream_t stream) {
     using C = Prefill2Cfg<D>;
-    cudaError_t e = cudaFuncSetAttribute(prefill2_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    auto kern = p.window > 0 ? prefill2_kernel<D, true> : prefill2_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(((p.nQ + 1) / 2) * p.B * p.Hq));
-    prefill2_kernel<D><<<grid, 384, C::SMEM, stream>>>(tq, tk, tv, p);
+    kern<<<grid, 384, C::SMEM, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 

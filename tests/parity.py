@@ -61,7 +61,7 @@ def _decisions(gpu_map, ora_map, ora_margin, lam, what):
     return int(diff.sum())
 
 
-def prefill_units_check(a, res, lam, units, log=None):
+def prefill_units_check(a, res, lam, units, log=None, window=0):
     """Compare the GPU prefill result on the given (b, h, qtile) units.
 
     a: workloads.Attn on the GPU; res: dict from blasst.prefill(..., want_map=True).
@@ -80,10 +80,11 @@ def prefill_units_check(a, res, lam, units, log=None):
         k = a.k[b:b + 1, hk:hk + 1].float().cpu()
         v = a.v[b:b + 1, hk:hk + 1].float().cpu()
         uu = [(0, 0, t) for t in tiles]
-        own = orc.prefill_tiled(q, k, v, a.causal, a.scale, lam, units=uu, precision="f32")
+        own = orc.prefill_tiled(q, k, v, a.causal, a.scale, lam, units=uu, precision="f32", window=window)
         forced_map = np.full(own["map"].shape, 0, np.uint8)
         forced_map[0, 0] = gmap[b, h]
-        ref = orc.prefill_tiled(q, k, v, a.causal, a.scale, lam, units=uu, forced=forced_map, precision="f32")
+        ref = orc.prefill_tiled(q, k, v, a.causal, a.scale, lam, units=uu, forced=forced_map, precision="f32",
+                                window=window)
         for t in tiles:
             what = f"{a.name} lam={lam:g} b={b} h={h} qtile={t}"
             band_total += _decisions(gmap[b, h, t], own["map"][0, 0, t], own["margin"][0, 0, t], lam, what)
@@ -96,10 +97,10 @@ def prefill_units_check(a, res, lam, units, log=None):
     return band_total, max(e[0] for e in errs), float(np.mean([e[1] for e in errs]))
 
 
-def prefill_full_check(a, res, lam, log=None):
+def prefill_full_check(a, res, lam, log=None, window=0):
     """Whole-problem comparison (small problems): decisions, exact count, O, lse."""
     own = orc.prefill_tiled(a.q.float().cpu(), a.k.float().cpu(), a.v.float().cpu(), a.causal, a.scale, lam,
-                            precision="f32")
+                            precision="f32", window=window)
     gmap = res["map"].cpu().numpy()
     band = _decisions(gmap, own["map"], own["margin"], lam, f"{a.name} lam={lam:g}")
     n_gpu = int(res["skipped"].item())
@@ -108,7 +109,7 @@ def prefill_full_check(a, res, lam, log=None):
     if band == 0:
         assert n_gpu == own["skipped"]
     ref = orc.prefill_tiled(a.q.float().cpu(), a.k.float().cpu(), a.v.float().cpu(), a.causal, a.scale, lam,
-                            forced=gmap, precision="f32")
+                            forced=gmap, precision="f32", window=window)
     mx, mean = _check_rows(res["o"].float().cpu().numpy(), res["lse"].cpu().numpy(), ref["o"], ref["lse"],
                            f"{a.name} lam={lam:g}")
     if log is not None and band:
@@ -157,7 +158,7 @@ def decode_full_check(a, res, lam, S, log=None):
     return band, mx, mean, n_gpu
 
 
-def decode_paged_check(a, res, lam, S, seqs=None, log=None):
+def decode_paged_check(a, res, lam, S, seqs=None, log=None, window=0):
     """A paged decode (workloads.paged_decode) against the oracle run on each
     sequence alone: its own key count, the call's lambda and split count.  Tiles
     past a sequence's end must stay "not visited"."""
@@ -170,8 +171,10 @@ def decode_paged_check(a, res, lam, S, seqs=None, log=None):
     for b in (range(B) if seqs is None else seqs):
         L = lens[b]
         nt = -(-L // 128)
-        what = f"{a.name} seq {b} (L={L}) lam={lam:g} S={S}"
+        lo = (L - window) // 128 if 0 < window < L else 0  # first tile holding a key in the window
+        what = f"{a.name} seq {b} (L={L}) lam={lam:g} S={S} window={window}"
         assert (gmap[b, :, nt:] == 2).all(), f"{what}: tiles past the end visited"
+        assert (gmap[b, :, :lo] == 2).all(), f"{what}: tiles before the window visited"
         if L == 0:
             assert (o_gpu[b] == 0).all() and np.isneginf(lse_gpu[b]).all(), what
             continue
@@ -181,10 +184,11 @@ def decode_paged_check(a, res, lam, S, seqs=None, log=None):
         # With more splits than tiles, split s = [floor(s*nt/S), floor((s+1)*nt/S)) puts
         # every tile in a split of its own and leaves the rest empty (no contribution):
         # the same partition as nt splits.
-        Sb = min(S, nt)
-        own = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=Sb, precision="f32")
+        Sb = min(S, nt - lo)
+        own = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=Sb, precision="f32", window=window)
         band = _decisions(gmap[b:b + 1, :, :nt], own["map"], own["margin"], lam, what)
-        ref = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=Sb, forced=gmap[b:b + 1, :, :nt], precision="f32")
+        ref = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=Sb, forced=gmap[b:b + 1, :, :nt], precision="f32",
+                               window=window)
         _check_rows(o_gpu[b:b + 1], lse_gpu[b:b + 1], ref["o"], ref["lse"], what)
         if log is not None and band:
             log.append(f"{what}: {band} tiles inside the 1e-3 margin band")

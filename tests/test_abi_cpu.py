@@ -138,12 +138,29 @@ def test_decode_validation(kw, code):
     (dict(d=64), K.BLASST_ERR_UNSUPPORTED),
     (dict(table=FAKE + 2), K.BLASST_ERR_UNSUPPORTED),
     (dict(S=2, wsb=16), K.BLASST_ERR_WORKSPACE_TOO_SMALL),
+    (dict(win=-1), K.BLASST_ERR_INVALID_ARG),
 ])
 def test_decode_paged_validation(kw, code):
     a = dict(q=FAKE, kp=FAKE, vp=FAKE, table=FAKE, lens=None, o=FAKE, B=2, Hq=8, Hkv=2, L=1000, d=128, npg=200,
-             ps=16, mp=63, tm=1, scale=0.1, lam=0.01, S=1, ws=FAKE, wsb=1 << 30)
+             ps=16, mp=63, tm=1, scale=0.1, lam=0.01, S=1, ws=FAKE, wsb=1 << 30, win=0)
     a.update(kw)
     rc = K.blasst_decode_paged(a["q"], a["kp"], a["vp"], a["table"], a["lens"], a["o"], None, a["B"], a["Hq"],
-                               a["Hkv"], a["L"], a["d"], a["npg"], a["ps"], a["mp"], a["tm"], a["scale"], a["lam"],
-                               a["S"], a["ws"], a["wsb"], None, None, None, stream=0)
+                               a["Hkv"], a["L"], a["win"], a["d"], a["npg"], a["ps"], a["mp"], a["tm"], a["scale"],
+                               a["lam"], a["S"], a["ws"], a["wsb"], None, None, None, stream=0)
+    assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(window=0), K.BLASST_ERR_INVALID_ARG),
+    (dict(window=-5), K.BLASST_ERR_INVALID_ARG),
+    (dict(flags=K.BLASST_PREFILL_WIDE), K.BLASST_ERR_UNSUPPORTED),
+    (dict(flags=K.BLASST_PREFILL_ONE_QTILE), K.BLASST_ERR_UNSUPPORTED),
+    (dict(q=None), K.BLASST_ERR_INVALID_ARG),
+    (dict(lam=2.0), K.BLASST_ERR_INVALID_ARG),
+])
+def test_prefill_window_validation(kw, code):
+    a = dict(q=FAKE, window=64, flags=0, lam=0.01)
+    a.update(kw)
+    rc = K.blasst_prefill_window(a["q"], FAKE, FAKE, FAKE, None, 1, 4, 2, 100, 100, 128, a["window"], 0.1, a["lam"],
+                                 None, None, None, a["flags"], stream=0)
     assert rc == code

@@ -75,6 +75,15 @@ def test_paged_full_length_equals_contiguous_bitwise(page_size, token_major):
         assert int(got["skipped"].item()) == int(ref["skipped"].item())
 
 
+@pytest.mark.parametrize("window", [1, 100, 128, 300, 2000])
+@pytest.mark.parametrize("page_size", [16, 128])
+def test_paged_sliding_window(window, page_size):
+    a = W.paged_decode(seed=9, B=len(LENS), Hq=8, Hkv=2, max_len=1000, page_size=page_size, lens=LENS, device="cuda")
+    for lam, S in ((0.0, 1), (0.3, 2), (0.0, 3)):
+        res = _run(a, lam, S, window=window)
+        parity.decode_paged_check(a, res, lam, S, window=window)
+
+
 def test_paged_zero_length_sequence():
     a = W.paged_decode(seed=6, B=3, Hq=8, Hkv=2, max_len=600, page_size=64, lens=[600, 0, 5], device="cuda")
     for S in (1, 2):

@@ -174,6 +174,49 @@ def test_elide_v_is_bitwise_identical_at_full_size(workload):
         assert int(ref["skipped"].item()) > 0
 
 
+WINDOW_SHAPES = [(1, 4, 2, 1000, 1000, 128), (1, 4, 1, 257, 1000, 128), (2, 2, 2, 300, 300, 64),
+                 (1, 2, 2, 1000, 700, 128)]
+
+
+@pytest.mark.parametrize("shape", WINDOW_SHAPES, ids=[str(s) for s in WINDOW_SHAPES])
+@pytest.mark.parametrize("window", [1, 64, 128, 129, 300, 5000])
+@pytest.mark.parametrize("flags", [0, K.BLASST_PREFILL_ELIDE_V], ids=["two-qtiles", "two-qtiles-elide-V"])
+def test_sliding_window_matches_oracle(shape, window, flags):
+    B, Hq, Hkv, Lq, Lkv, d = shape
+    a = parity.to_gpu(W.small_random(31 + window, B, Hq, Hkv, Lq, Lkv, d, True))
+    for lam in (0.0, 0.05, 0.5):
+        res = K.prefill(a.q, a.k, a.v, True, a.scale, lam, want_map=True, flags=flags, window=window)
+        torch.cuda.synchronize()
+        parity.prefill_full_check(a, res, lam, window=window)
+
+
+def test_sliding_window_covering_all_keys_equals_causal_bitwise():
+    a = parity.to_gpu(W.small_random(77, 1, 4, 2, 900, 1100, 128, True))
+    for lam in (0.0, 0.3):
+        ref = K.prefill(a.q, a.k, a.v, True, a.scale, lam, want_map=True)
+        got = K.prefill(a.q, a.k, a.v, True, a.scale, lam, want_map=True, window=1100)
+        torch.cuda.synchronize()
+        assert torch.equal(got["map"], ref["map"]) and torch.equal(got["o"], ref["o"])
+        assert torch.equal(got["lse"], ref["lse"])
+
+
+def test_sliding_window_llm_full_size_sampled():
+    """LLM prefill at 16k keys with a 4096-key window: sampled query tiles."""
+    L, Wn = 16384, 4096
+    a = parity.to_gpu(W.llm(seed=0, L=L, device="cuda"))
+    rng = np.random.default_rng(5)
+    nQ = L // 128
+    units = parity.sample_units(rng, 1, a.Hq, nQ, 4, always=[(0, 0, 0), (0, 31, nQ - 1), (0, 3, 40)])
+    for lam in (0.0, 40 / Wn, 0.3):
+        res = K.prefill(a.q, a.k, a.v, True, a.scale, lam, want_map=True, window=Wn)
+        torch.cuda.synchronize()
+        mp = res["map"]
+        assert int(res["skipped"].item()) == int((mp == 1).sum().item())
+        # a query tile visits at most ceil(W/128) + 1 key tiles
+        assert int((mp != 2).sum(dim=-1).max().item()) <= Wn // 128 + 1
+        parity.prefill_units_check(a, res, lam, units, window=Wn)
+
+
 def test_short_watchdog_reports_timeout_and_context_survives():
     """Waits with a ~1 us limit give up; the kernel records a timeout, drains its
     copies, frees its tensor memory and exits; the next normal call is correct."""
