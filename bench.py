@@ -35,9 +35,9 @@ PREFILL = dict(B=1, Hq=32, Hkv=8, L=16384, d=128)
 DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the current kernels; None until captured for this version of the kernels.
-# prefill: not yet captured for the current prefill2_kernel<128> (last capture, an earlier version: 367.7 MB read + 102.5 MB written).
+# prefill: prefill2_kernel<128, false> capture (369.3 MB read + 100.8 MB written).
 # decode: decode_kernel<4, false> B=8 capture (1074.0 MB read + 4.3 MB written) x 8 for the B=64 launch.
-TRAFFIC_BYTES = {"prefill": None, "decode": 8 * (1073967000 + 4270336)}
+TRAFFIC_BYTES = {"prefill": 369254400 + 100825600, "decode": 8 * (1073967000 + 4270336)}
 
 
 def load_peaks():
@@ -411,11 +411,11 @@ def run_ours(args):
                          f"{secs:.1f} s of fp32 oracle time"}
 
     ach = exec_flop / (p_max * 1e-3) / 1e12
-    roof = {"bound": "tensor", "kernel": "prefill2_kernel<128> (two query tiles per CTA)", "achieved": ach,
+    roof = {"bound": "tensor", "kernel": "prefill2_kernel<128, false> (two query tiles per CTA)", "achieved": ach,
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
             "peak_source": peaks["source"] + " burst bf16",
             "traffic": TRAFFIC_BYTES["prefill"]}
-    roof_d = {"bound": "hbm", "kernel": "decode_kernel<4> + combine", "achieved": dec_gbs,
+    roof_d = {"bound": "hbm", "kernel": "decode_kernel<4, false> + combine", "achieved": dec_gbs,
               "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
               "peak_source": peaks["source"] + " HBM copy", "traffic": TRAFFIC_BYTES["decode"]}
     line = {
