@@ -2,7 +2,8 @@
 // eight softmax warps per query tile (selected with BLASST_PREFILL_WIDE).
 //
 // Same pipeline as the two-tile kernel in prefill.cu (one TMA producer, one MMA
-// issuer per query tile taking turns, P in TMEM), but each query row is handled by
+// issuer per query tile taking turns and committing once per key tile, P in TMEM),
+// but each query row is handled by
 // two threads: warps 0-3 own key columns 0..63 of the rows of tile A, warps 4-7
 // columns 64..127; warps 8-15 do the same for tile B.  Each thread therefore takes
 // the max and the exponentials of 64 scores instead of 128, which halves the
@@ -37,11 +38,14 @@ static_assert(4 * 128 * kRegsSoftmax + 128 * kRegsProducer <= kThreads * kRegsLa
 
 template <int NK, int NV>
 struct WideCtrl {
+    // commit c of issuer w (after QK_w(c) and PV_w(c-1)) arrives on rel[w][c % NR]:
+    // S ready for the softmax, K/V slots free for the producer (as in prefill.cu)
+    static constexpr int NR = (NK > NV ? NK : NV) + 1;
     uint64_t q_full;
     uint64_t k_full[NK], v_full[NV];
-    uint64_t k_empty[2][NK], v_empty[2][NV];
-    uint64_t s_full[2], p_full[2][2], o_done[2];
-    uint64_t drain[2], never;
+    uint64_t rel[2][NR];
+    uint64_t p_full[2][2];
+    uint64_t never;
     uint32_t tmem_base;
     int vote[2][3];
     int dec[2];
@@ -123,22 +127,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (tid == 0) {
         mbar_init(&ctrl->q_full, 1);
-        for (int i = 0; i < C::NK; ++i) {
-            mbar_init(&ctrl->k_full[i], 1);
-            mbar_init(&ctrl->k_empty[0][i], 1);
-            mbar_init(&ctrl->k_empty[1][i], 1);
-        }
-        for (int i = 0; i < C::NV; ++i) {
-            mbar_init(&ctrl->v_full[i], 1);
-            mbar_init(&ctrl->v_empty[0][i], 1);
-            mbar_init(&ctrl->v_empty[1][i], 1);
-        }
+        for (int i = 0; i < C::NK; ++i) mbar_init(&ctrl->k_full[i], 1);
+        for (int i = 0; i < C::NV; ++i) mbar_init(&ctrl->v_full[i], 1);
         for (int w = 0; w < 2; ++w) {
-            mbar_init(&ctrl->s_full[w], 1);
+            for (int i = 0; i < Ctrl::NR; ++i) mbar_init(&ctrl->rel[w][i], 1);
             mbar_init(&ctrl->p_full[w][0], 4);
             mbar_init(&ctrl->p_full[w][1], 4);
-            mbar_init(&ctrl->o_done[w], 1);
-            mbar_init(&ctrl->drain[w], 1);
             ctrl->vote[w][0] = ctrl->vote[w][1] = ctrl->vote[w][2] = 1;
         }
         mbar_init(&ctrl->never, 1);
@@ -178,7 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(smem + C::OFF_Q + w * C::TILE_BYTES + x * C::BOX_BYTES, &tq, &ctrl->q_full,
                                     x * 64, (2 * pi + w) * kTile, zq);
                 }
-                // a slot is reused once every query tile that read its previous occupant released it
+                // a slot is reused once every query tile that read its previous occupant is done
+                // with it: K_m by QK_w(m) (commit m), V_m by PV_w(m) (commit m+1)
+                constexpr int NR = Ctrl::NR;
                 int issued_k = 0, issued_v = 0;
                 for (int j = 0; j < N; ++j) {
                     const int ks = j % C::NK;
@@ -186,7 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (j >= C::NK) {
                         const int prev = j - C::NK;
                         for (int w = 0; w < 2 && okk; ++w)
-                            if (prev < nvis[w]) okk = mbar_wait(&ctrl->k_empty[w][ks], (prev / C::NK) & 1, wd);
+                            if (prev < nvis[w]) okk = mbar_wait(&ctrl->rel[w][(unsigned)prev % NR], ((unsigned)prev / NR) & 1u, wd);
                     }
                     if (!okk) break;
                     mbar_arrive_expect_tx(&ctrl->k_full[ks], C::TILE_BYTES);
@@ -200,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (j >= C::NV) {
                         const int prev = j - C::NV;
                         for (int w = 0; w < 2 && okv; ++w)
-                            if (prev < nvis[w]) okv = mbar_wait(&ctrl->v_empty[w][vs], (prev / C::NV) & 1, wd);
+                            if (prev < nvis[w])
+                                okv = mbar_wait(&ctrl->rel[w][(unsigned)(prev + 1) % NR], ((unsigned)(prev + 1) / NR) & 1u, wd);
                     }
                     if (!okv) break;
                     mbar_arrive_expect_tx(&ctrl->v_full[vs], C::TILE_BYTES);
@@ -236,8 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t o = ((kk >> 2) * C::BOX_BYTES + (kk & 3) * 32) >> 4;
                         mma_ss_split(s_t, qlo + o, b0 + o, kIdescS, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(&ctrl->s_full[w]);
-                    mma_commit(&ctrl->k_empty[w][j % C::NK]);
+                };
+                int ncommit = 0;
+                auto commit = [&]() {
+                    mma_commit(&ctrl->rel[w][(unsigned)ncommit % Ctrl::NR]);
+                    ++ncommit;
                 };
                 auto issue_pv_half = [&](int vs, int half, bool first) {
                     const uint32_t b0 = vlo + (uint32_t)vs * kTileLo;
@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) {
                     tc_fence_after();
                     issue_qk(0);
+                    commit();
                 }
                 int npv = 0;
                 for (int j = 0; j < n && ok; ++j) {
@@ -290,17 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     if (!skip) {
                         issue_pv_half(vs, 1, npv == 0);
-                        mma_commit(&ctrl->o_done[w]);
                         ++npv;
                     }
-                    mma_commit(&ctrl->v_empty[w][vs]);
                     if (j + 1 < n) issue_qk(j + 1);
+                    commit();  // commit j+1: PV_w(j) and QK_w(j+1)
                     *turn = 1 - w;
                 }
                 active[w] = 0;
                 *turn = 1 - w;
-                mma_commit(&ctrl->drain[w]);
-                mbar_wait_drain(&ctrl->drain[w], 0, kDrainNs);
+                if (ncommit > 0)  // the last commit covers every MMA of this thread
+                    mbar_wait_drain(&ctrl->rel[w][(unsigned)(ncommit - 1) % Ctrl::NR],
+                                    ((unsigned)(ncommit - 1) / Ctrl::NR) & 1u, kDrainNs);
             }
         }
     } else {
@@ -326,7 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int* vote = ctrl->vote[w];
 
         for (int j = 0; j < n; ++j) {
-            mbar_wait(&ctrl->s_full[w], j & 1, wd);
+            // commit j: S_j is in TMEM and O holds PV_w(j-1)
+            mbar_wait(&ctrl->rel[w][(unsigned)j % Ctrl::NR], ((unsigned)j / Ctrl::NR) & 1u, wd);
             tc_fence_after();
             uint32_t xr[64];
             tmem_ld32(tl + s_col, xr);
@@ -387,8 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // rescale this half-row of O to the new reference before its PV is issued
                 if (__any_sync(0xffffffffu, move) && npv > 0) {
-                    mbar_wait(&ctrl->o_done[w], (npv - 1) & 1, wd);
-                    tc_fence_after();
 #pragma unroll
                     for (int cc = 0; cc < D / 2; cc += 16) {
                         uint32_t ov[16];
@@ -406,12 +406,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->p_full[w][half]);
+            mbar_arrive_if(&ctrl->p_full[w][half], lane == 0);
         }
 
         // ---------------------------------------------------------------- epilogue
-        if (npv > 0) {
-            mbar_wait(&ctrl->o_done[w], (npv - 1) & 1, wd);
+        if (n > 0) {  // commit n covers the last PV
+            mbar_wait(&ctrl->rel[w][(unsigned)n % Ctrl::NR], ((unsigned)n / Ctrl::NR) & 1u, wd);
             tc_fence_after();
         }
         ctrl->mx[w][half ^ 1][r] = l;
