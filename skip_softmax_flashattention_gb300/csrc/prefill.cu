@@ -39,10 +39,6 @@
 #include "kernels.cuh"
 #include "ptx.cuh"
 
-// 2^x of the two-query-tile kernel: 0 = fp32 ex2 per element, 1 = bf16x2 ex2 per pair.
-#ifndef BLASST_EXP_BF16X2
-#define BLASST_EXP_BF16X2 0
-#endif
 
 namespace blasst {
 namespace {
@@ -859,11 +855,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t pk[16];
-#if BLASST_EXP_BF16X2
-                    rs += exp_pack32_bf16(xr + ch * 32, p.c_log2, mc, pk);
-#else
                     rs += exp_pack32(xr + ch * 32, p.c_log2, mc, pk);
-#endif
                     tmem_st16(tl + s_col + ch * 16, pk);
                     if (ch == 1) {  // first half of P (keys 0..63) is in TMEM: let PV start on it
                         tmem_st_wait();

@@ -385,13 +385,6 @@ __device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float 
         : "f"(a0), "f"(a1));
 }
 
-// 2^x for two values at once on the special-function unit, bf16 in and out.
-__device__ __forceinline__ uint32_t ex2_bf16x2(uint32_t x) {
-    uint32_t y;
-    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(y) : "r"(x));
-    return y;
-}
-
 // Maximum of 128 fp32 values held as raw bits, as a shallow tree of 3-input maxima.
 __device__ __forceinline__ float row_max128(const uint32_t* x) {
     float m[16];
@@ -438,24 +431,4 @@ __device__ __forceinline__ float exp_pack16(const uint32_t* x, float c, float mc
     }
     return (s0 + s1) + (s2 + s3);
 }
-// As exp_pack32, with the exponent argument rounded to bf16 and 2^x taken two at a
-// time in bf16 (half the special-function instructions); the sum adds the bf16
-// values that the P.V product will use.
-__device__ __forceinline__ float exp_pack32_bf16(const uint32_t* x, float c, float mc, uint32_t* pk) {
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        float a0, a1;
-        ffma2(a0, a1, __uint_as_float(x[2 * i]), __uint_as_float(x[2 * i + 1]), c, -mc);
-        const uint32_t e = ex2_bf16x2(pack_bf16x2(a0, a1));
-        pk[i] = e;
-        const float p0 = __uint_as_float(e << 16), p1 = __uint_as_float(e & 0xffff0000u);
-        if (i & 1)
-            fadd2_acc(s2, s3, p0, p1);
-        else
-            fadd2_acc(s0, s1, p0, p1);
-    }
-    return (s0 + s1) + (s2 + s3);
-}
-
 }  // namespace blasst
