@@ -35,9 +35,9 @@ PREFILL = dict(B=1, Hq=32, Hkv=8, L=16384, d=128)
 DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the current kernels; None until captured for this version of the kernels.
-# prefill: not yet captured for the current prefill2_kernel<128, false> (last capture, an earlier version: 369.3 MB read + 100.8 MB written).
+# prefill: prefill2_kernel<128, false> capture (365.6 MB read + 100.3 MB written).
 # decode: decode_kernel<4, false> B=8 capture (1074.0 MB read + 4.3 MB written) x 8 for the B=64 launch.
-TRAFFIC_BYTES = {"prefill": None, "decode": 8 * (1073967000 + 4270336)}
+TRAFFIC_BYTES = {"prefill": 365569024 + 100312832, "decode": 8 * (1073967000 + 4270336)}
 
 
 def load_peaks():
@@ -362,37 +362,65 @@ def run_ours(args):
     dec_gbs = (kv_bytes + other_bytes) / (d_max * 1e-3) / 1e9
     dec_dense_gbs = (tile_bytes * 2 * tiles_d) / (d_max * 1e-3) / 1e9
 
-    # ---- end to end through the C ABI with host buffers (prefill, the headline metric)
+    # ---- end to end through the C ABI with host buffers (prefill, the headline metric).
+    # Every step copies its own Q, K, V from pinned host memory and reads its own O and
+    # lse back.  Steps are pipelined over two device buffer sets and three streams, as a
+    # serving loop would run them: step i+1's inputs go in and step i-1's results come
+    # out while step i's kernel runs.
     qh = a.q.cpu().pin_memory()
     kh = a.k.cpu().pin_memory()
     vh = a.v.cpu().pin_memory()
-    oh = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    lseh = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
-    qd, kd, vd = torch.empty_like(a.q), torch.empty_like(a.k), torch.empty_like(a.v)
+    oh = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for _ in range(2)]
+    lseh = [torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True) for _ in range(2)]
+    qd = [torch.empty_like(a.q) for _ in range(2)]
+    kd = [torch.empty_like(a.k) for _ in range(2)]
+    vd = [torch.empty_like(a.v) for _ in range(2)]
+    od = [torch.empty_like(o) for _ in range(2)]
+    lsed = [torch.empty_like(lse) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    s_comp = torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_done = [ev(), ev()]     # inputs of set x copied
+    comp_done = [ev(), ev()]   # kernel of set x finished (inputs free, outputs ready)
+    out_done = [ev(), ev()]    # outputs of set x read back (outputs free)
+    for x in range(2):
+        comp_done[x].record(s_comp)
+        out_done[x].record(s_out)
 
-    def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        rc = K.blasst_prefill(qd, kd, vd, o, lse, P["B"], P["Hq"], P["Hkv"], L, L, P["d"], 1, a.scale, lam_p(),
-                              skipped_p, stream)
+    def e2e_step(i):
+        x = i & 1
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(comp_done[x])
+            qd[x].copy_(qh, non_blocking=True)
+            kd[x].copy_(kh, non_blocking=True)
+            vd[x].copy_(vh, non_blocking=True)
+            in_done[x].record(s_in)
+        s_comp.wait_event(in_done[x])
+        s_comp.wait_event(out_done[x])
+        rc = K.blasst_prefill(qd[x], kd[x], vd[x], od[x], lsed[x], P["B"], P["Hq"], P["Hkv"], L, L, P["d"], 1,
+                              a.scale, lam_p(), skipped_p, s_comp.cuda_stream)
         assert rc == 0
-        oh.copy_(o, non_blocking=True)
-        lseh.copy_(lse, non_blocking=True)
+        comp_done[x].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(comp_done[x])
+            oh[x].copy_(od[x], non_blocking=True)
+            lseh[x].copy_(lsed[x], non_blocking=True)
+            out_done[x].record(s_out)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    for i in range(max(1, args.warmup)):
+        e2e_step(i)
     torch.cuda.synchronize()
     e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_s.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e_e.record(stream)
+    e_s.record(s_in)
+    for i in range(args.steps):
+        e2e_step(i)
+    s_out.wait_event(comp_done[(args.steps - 1) & 1])
+    e_e.record(s_out)  # after the last step's read-back (s_out runs its copies in step order)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(pg, e_s.elapsed_time(e_e) / args.steps)
     e2e_value = sum_over_ranks(pg, dense_flop / (e2e_ms * 1e-3) / 1e12)
     h2d = qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2
-    d2h = oh.numel() * 2 + lseh.numel() * 4
+    d2h = oh[0].numel() * 2 + lseh[0].numel() * 4
 
     # ---- CPU baseline: the oracle on a bounded sample of the same prefill workload
     cpu = None
