@@ -53,6 +53,20 @@
  *    split is an independent pass (m restarts at -inf) and the splits are merged by
  *    lse weighting: lse = ln(sum_s exp(lse_s)), O = sum_s exp(lse_s - lse) O_s.
  *
+ *  oracle_mla_decode_tiled
+ *                 decode for multi-head latent attention in its absorbed form (the
+ *                 pages name MLA as the decode case where the skipped compute
+ *                 pays: Skip-Softmax design doc, "Kernel", and BLASST talk notes,
+ *                 "Abstract"; the pages give no formula for it).  Reading: every
+ *                 cached token holds ONE row of dk values shared by all query heads;
+ *                 the score of head h is scale * (q_h . row) over all dk values and
+ *                 the value vector is the row's first dv values.  All query heads
+ *                 read the same cached rows, so (as with the heads of a GQA group)
+ *                 one skip decision covers every head x 128 keys.  A sequence b
+ *                 holds seq_lens[b] keys (the whole cache when seq_lens is null);
+ *                 its splits cover its own tiles, and a split with no tile gives
+ *                 O = 0, lse = -inf.
+ *
  * Plain loops, no blocking or fusion beyond the tiling the method itself states;
  * OpenMP only splits independent (batch, head, query-tile) units across cores.
  */
@@ -90,7 +104,7 @@ static int visible(int causal, long window, long r, long c, long Lq, long Lkv) {
     return window <= 0 || c > rr - window;
 }
 
-/* s = scale * (q . k), accumulated in `real` in index order */
+/* s = scale * (q . k) over d values, accumulated in `real` in index order */
 static real score(const real* q, const real* k, int d, real scale) {
     real acc = 0;
     for (int i = 0; i < d; ++i) acc += q[i] * k[i];
@@ -160,14 +174,17 @@ int FN(oracle_dense)(const real* q, const real* k, const real* v, real* o, real*
 /* map/margin:  per-tile outputs indexed by tile number (non-null)              */
 /* O, l, m:     per-row state, n_rows x d / n_rows / n_rows (output: O/l, lse)  */
 /* ------------------------------------------------------------------------- */
+/* kb/vb:       key c is kb + c*kstride (d values), its value vb + c*vstride   */
+/*              (dv values; O rows hold dv values)                            */
 typedef struct {
     int n_rows;
     const real* const* qrow;
     const long* rpos;
     const real* kb;
     const real* vb;
+    long kstride, vstride;
     long Lq, Lkv;
-    int d, Bc, causal;
+    int d, dv, Bc, causal;
     long window;
     real scale;
     real lnlam;
@@ -176,7 +193,7 @@ typedef struct {
 static long run_pass(const pass_args* a, int t0, int t1, const uint8_t* forced,
                      uint8_t* map, real* margin, real* O, real* l, real* m,
                      real* S /* n_rows*Bc scratch */, real* mt /* n_rows */, real* mnew /* n_rows */) {
-    const int n = a->n_rows, d = a->d, Bc = a->Bc;
+    const int n = a->n_rows, d = a->dv, Bc = a->Bc;
     long skipped = 0;
     for (int i = 0; i < n; ++i) {
         m[i] = NEG_INF;
@@ -202,7 +219,7 @@ static long run_pass(const pass_args* a, int t0, int t1, const uint8_t* forced,
                 long c = c0 + cc;
                 real sv = NEG_INF;
                 if (visible(a->causal, a->window, a->rpos[i], c, a->Lq, a->Lkv))
-                    sv = score(a->qrow[i], a->kb + c * d, d, a->scale);
+                    sv = score(a->qrow[i], a->kb + c * a->kstride, a->d, a->scale);
                 S[(long)i * Bc + cc] = sv;
                 if (sv > best) best = sv;
             }
@@ -248,7 +265,7 @@ static long run_pass(const pass_args* a, int t0, int t1, const uint8_t* forced,
                 if (sv == NEG_INF) continue;
                 real p = R_EXP(sv - mnew[i]);
                 rowsum += p;
-                const real* vr = a->vb + (c0 + cc) * d;
+                const real* vr = a->vb + (c0 + cc) * a->vstride;
                 for (int x = 0; x < d; ++x) Oi[x] += p * vr[x];
             }
             l[i] = alpha * l[i] + rowsum;
@@ -334,9 +351,10 @@ long long FN(oracle_prefill_tiled)(const real* q, const real* k, const real* v, 
             a.rpos = rpos;
             a.kb = k + ((b * Hkv + hk) * (long)Lkv) * d;
             a.vb = v + ((b * Hkv + hk) * (long)Lkv) * d;
+            a.kstride = a.vstride = d;
             a.Lq = Lq;
             a.Lkv = Lkv;
-            a.d = d;
+            a.d = a.dv = d;
             a.Bc = Bc;
             a.causal = causal;
             a.window = window;
@@ -418,9 +436,10 @@ long long FN(oracle_decode_tiled)(const real* q, const real* k, const real* v, r
             a.rpos = rpos;
             a.kb = k + ((b * Hkv + hk) * (long)Lkv) * d;
             a.vb = v + ((b * Hkv + hk) * (long)Lkv) * d;
+            a.kstride = a.vstride = d;
             a.Lq = 1;
             a.Lkv = Lkv;
-            a.d = d;
+            a.d = a.dv = d;
             a.Bc = Bc;
             a.causal = window > 0;  /* the query row sits at Lkv - 1 */
             a.window = window;
@@ -464,6 +483,122 @@ long long FN(oracle_decode_tiled)(const real* q, const real* k, const real* v, r
                         memcpy(o_part + (((long)s * B + b) * Hq + hq) * d, Op + ((long)s * G + i) * d,
                                sizeof(real) * d);
                         lse_part[((long)s * B + b) * Hq + hq] = lp[(long)s * G + i];
+                    }
+                }
+            }
+            if (map) memcpy(map + base, lmap, nK);
+            if (margin) memcpy(margin + base, lmargin, sizeof(real) * nK);
+        }
+        free(qrow); free(rpos); free(O); free(l); free(m); free(Sb); free(mt); free(mn);
+        free(lmap); free(lmargin); free(Op); free(lp);
+    }
+    return skipped_total;
+}
+
+/* ------------------------------------------------------------------------- */
+/* MLA decode (absorbed form): one latent row per cached token, shared by all  */
+/* Hq query heads; the Hq heads form the rows of every tile.                  */
+/*                                                                           */
+/* q [B,Hq,dk], kv [B,Lmax,dk] (value = first dv entries of a row)             */
+/* seq_lens: nullable [B], keys of sequence b (clamped to [0, Lmax])           */
+/* o [B,Hq,dv], lse [B,Hq]                                                     */
+/* units:   nullable list of batch indices; all splits of a sequence are run   */
+/* forced/map/margin: nullable [B, nK], nK = ceil(Lmax / Bc); tiles past a     */
+/*          sequence's end are not visited (map 2, margin NaN)                 */
+/* o_part/lse_part: nullable [S,B,Hq,dv] / [S,B,Hq] per-split results          */
+/* returns the number of skipped tiles, or -1 on bad arguments                 */
+/* ------------------------------------------------------------------------- */
+long long FN(oracle_mla_decode_tiled)(const real* q, const real* kv, const int32_t* seq_lens, real* o,
+                                      real* lse, int B, int Hq, int Lmax, int dk, int dv, double scale,
+                                      double lambda, int Bc, int num_splits, const int32_t* units,
+                                      int n_units, const uint8_t* forced, uint8_t* map, real* margin,
+                                      real* o_part, real* lse_part) {
+    if (B <= 0 || Hq <= 0 || Lmax <= 0 || dk <= 0 || dv <= 0 || dv > dk || Bc <= 0 || num_splits < 1)
+        return -1;
+    const int nK = (Lmax + Bc - 1) / Bc;
+    const int S = num_splits;
+    const long nu = units ? n_units : (long)B;
+    long long skipped_total = 0;
+#pragma omp parallel reduction(+ : skipped_total)
+    {
+        const real** qrow = (const real**)malloc(sizeof(real*) * Hq);
+        long* rpos = (long*)malloc(sizeof(long) * Hq);
+        real* O = (real*)malloc(sizeof(real) * (size_t)Hq * dv);
+        real* l = (real*)malloc(sizeof(real) * Hq);
+        real* m = (real*)malloc(sizeof(real) * Hq);
+        real* Sb = (real*)malloc(sizeof(real) * (size_t)Hq * Bc);
+        real* mt = (real*)malloc(sizeof(real) * Hq);
+        real* mn = (real*)malloc(sizeof(real) * Hq);
+        uint8_t* lmap = (uint8_t*)malloc(nK);
+        real* lmargin = (real*)malloc(sizeof(real) * nK);
+        real* Op = (real*)malloc(sizeof(real) * (size_t)S * Hq * dv);
+        real* lp = (real*)malloc(sizeof(real) * (size_t)S * Hq);
+#pragma omp for schedule(dynamic, 1)
+        for (long u = 0; u < nu; ++u) {
+            const long b = units ? units[u] : u;
+            long Lb = Lmax;
+            if (seq_lens) {
+                Lb = seq_lens[b];
+                if (Lb < 0) Lb = 0;
+                if (Lb > Lmax) Lb = Lmax;
+            }
+            const int nT = (int)((Lb + Bc - 1) / Bc);
+            for (int i = 0; i < Hq; ++i) {
+                qrow[i] = q + (b * Hq + i) * (long)dk;
+                rpos[i] = 0;
+            }
+            pass_args a;
+            a.n_rows = Hq;
+            a.qrow = qrow;
+            a.rpos = rpos;
+            a.kb = kv + b * (long)Lmax * dk;
+            a.vb = a.kb; /* the value is the leading dv entries of the same row */
+            a.kstride = a.vstride = dk;
+            a.Lq = 1;
+            a.Lkv = Lb;
+            a.d = dk;
+            a.dv = dv;
+            a.Bc = Bc;
+            a.causal = 0;
+            a.window = 0;
+            a.scale = (real)scale;
+            a.lnlam = ln_lambda(lambda);
+            const long base = b * (long)nK;
+            for (int t = 0; t < nK; ++t) { /* past the sequence's end: not visited */
+                lmap[t] = 2;
+                lmargin[t] = (real)NAN;
+            }
+            for (int s = 0; s < S; ++s) {
+                int t0 = (int)(((long)s * nT) / S), t1 = (int)(((long)(s + 1) * nT) / S);
+                skipped_total += run_pass(&a, t0, t1, forced ? forced + base : NULL, lmap, lmargin, O, l,
+                                          m, Sb, mt, mn);
+                memcpy(Op + (long)s * Hq * dv, O, sizeof(real) * (size_t)Hq * dv);
+                memcpy(lp + (long)s * Hq, m, sizeof(real) * Hq);
+            }
+            for (int i = 0; i < Hq; ++i) {
+                real M = NEG_INF;
+                for (int s = 0; s < S; ++s)
+                    if (lp[(long)s * Hq + i] > M) M = lp[(long)s * Hq + i];
+                real* orow = o + (b * Hq + i) * (long)dv;
+                for (int x = 0; x < dv; ++x) orow[x] = 0;
+                if (M == NEG_INF) {
+                    lse[b * Hq + i] = NEG_INF;
+                } else {
+                    real tot = 0;
+                    for (int s = 0; s < S; ++s) tot += R_EXP(lp[(long)s * Hq + i] - M);
+                    real L = M + R_LOG(tot);
+                    for (int s = 0; s < S; ++s) {
+                        real w = R_EXP(lp[(long)s * Hq + i] - L);
+                        const real* os = Op + ((long)s * Hq + i) * dv;
+                        for (int x = 0; x < dv; ++x) orow[x] += w * os[x];
+                    }
+                    lse[b * Hq + i] = L;
+                }
+                if (o_part && lse_part) {
+                    for (int s = 0; s < S; ++s) {
+                        memcpy(o_part + (((long)s * B + b) * Hq + i) * dv, Op + ((long)s * Hq + i) * dv,
+                               sizeof(real) * dv);
+                        lse_part[((long)s * B + b) * Hq + i] = lp[(long)s * Hq + i];
                     }
                 }
             }

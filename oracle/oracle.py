@@ -45,6 +45,12 @@ def _configure(lib):
                       ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
                       ctypes.c_void_p, ctypes.c_int])
+        f = getattr(lib, "oracle_mla_decode_tiled" + suf)
+        f.restype = ctypes.c_longlong
+        f.argtypes = ([P, P, ctypes.c_void_p, P, P] + [ctypes.c_int] * 5 +
+                      [ctypes.c_double, ctypes.c_double, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                       ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                       ctypes.c_void_p, ctypes.c_void_p])
     return lib
 
 
@@ -167,6 +173,55 @@ def decode_tiled(q, k, v, scale: float, lam: float, num_splits: int = 1, Bc: int
         _vp(op), _vp(lp), int(window))
     if sk < 0:
         raise ValueError("oracle_decode_tiled: bad arguments")
+    return {"o": o, "lse": lse, "map": m, "margin": g, "skipped": int(sk), "o_part": op,
+            "lse_part": lp}
+
+
+def mla_decode_tiled(q, kv, dv: int, scale: float, lam: float, num_splits: int = 1, seq_lens=None,
+                     Bc: int = 128, units=None, forced=None, precision: str = "f32"):
+    """Tiled skip-softmax pass for MLA decode in its absorbed form.
+
+    q [B,Hq,dk]; kv [B,Lmax,dk], one latent row per cached token shared by every
+    query head; the value of a token is the first `dv` entries of its row.  One
+    decision covers all Hq heads x Bc keys.  seq_lens: optional [B] key counts.
+    units: optional iterable of batch indices; forced: optional uint8 [B,nK].
+    Returns dict(o [B,Hq,dv], lse [B,Hq], map [B,nK], margin [B,nK], skipped,
+    o_part [S,B,Hq,dv], lse_part [S,B,Hq]).
+    """
+    dt, ct, suf = _types(precision)
+    q = _np(q, dt)
+    if q.ndim == 4:
+        q = np.ascontiguousarray(q[:, :, 0, :])
+    kv = _np(kv, dt)
+    B, Hq, dk = q.shape
+    Lmax = kv.shape[1]
+    if kv.shape != (B, Lmax, dk):
+        raise ValueError("kv must be [B, Lmax, dk]")
+    nK = -(-Lmax // Bc)
+    S = int(num_splits)
+    o = np.zeros((B, Hq, dv), dt)
+    lse = np.full((B, Hq), np.nan, dt)
+    m = np.full((B, nK), 255, np.uint8)
+    g = np.full((B, nK), np.nan, dt)
+    op = np.zeros((S, B, Hq, dv), dt)
+    lp = np.full((S, B, Hq), np.nan, dt)
+    sl = None
+    if seq_lens is not None:
+        sl = np.ascontiguousarray(np.asarray(seq_lens, dtype=np.int32).reshape(B))
+    u = None
+    nu = 0
+    if units is not None:
+        u = np.ascontiguousarray(np.asarray(list(units), dtype=np.int32).reshape(-1))
+        nu = u.shape[0]
+    f = None
+    if forced is not None:
+        f = np.ascontiguousarray(np.asarray(forced, dtype=np.uint8).reshape(B, nK))
+    sk = getattr(_load(), "oracle_mla_decode_tiled" + suf)(
+        _ptr(q, ct), _ptr(kv, ct), _vp(sl), _ptr(o, ct), _ptr(lse, ct),
+        B, Hq, Lmax, dk, int(dv), float(scale), float(lam), Bc, S, _vp(u), nu, _vp(f), _vp(m), _vp(g),
+        _vp(op), _vp(lp))
+    if sk < 0:
+        raise ValueError("oracle_mla_decode_tiled: bad arguments")
     return {"o": o, "lse": lse, "map": m, "margin": g, "skipped": int(sk), "o_part": op,
             "lse_part": lp}
 

@@ -31,8 +31,13 @@ MUTANTS = {
     "lse-missing-max": ("m[i] = m[i] + R_LOG(l[i]);", "m[i] = R_LOG(l[i]);"),
     "split-bounds-truncated": ("int t0 = lo + (int)(((long)s * (nK - lo)) / S), t1 = lo + (int)(((long)(s + 1) * (nK - lo)) / S);",
                                "int t0 = lo + s * ((nK - lo) / S), t1 = (s == S - 1) ? nK : lo + (s + 1) * ((nK - lo) / S);"),
-    "transposed-score-index": ("sv = score(a->qrow[i], a->kb + c * d, d, a->scale);",
-                               "sv = score(a->qrow[i], a->kb + (c0 + (Bc - 1 - cc < a->Lkv - c0 ? Bc - 1 - cc : cc)) * d, d, a->scale);"),
+    "transposed-score-index": ("sv = score(a->qrow[i], a->kb + c * a->kstride, a->d, a->scale);",
+                               "sv = score(a->qrow[i], a->kb + (c0 + (Bc - 1 - cc < a->Lkv - c0 ? Bc - 1 - cc : cc)) * a->kstride, a->d, a->scale);"),
+    "mla-value-from-the-row-tail": ("a.vb = a.kb; /* the value is", "a.vb = a.kb + (dk - dv); /* the value is"),
+    "mla-score-over-value-width": ("a.d = dk;\n            a.dv = dv;", "a.d = dv;\n            a.dv = dv;"),
+    "mla-sequence-length-ignored": ("if (Lb > Lmax) Lb = Lmax;\n            }", "if (Lb > Lmax) Lb = Lmax;\n                Lb = Lmax;\n            }"),
+    "mla-splits-over-the-whole-cache": ("int t0 = (int)(((long)s * nT) / S), t1 = (int)(((long)(s + 1) * nT) / S);",
+                                        "int t0 = (int)(((long)s * nK) / S), t1 = (int)(((long)(s + 1) * nK) / S);"),
 }
 
 PINS = [
@@ -46,6 +51,9 @@ PINS = [
     lambda: pins.test_skipped_contribution_closed_form(0.1),
     lambda: pins.test_window_of_one_key_returns_that_keys_value(20, 29),
     lambda: pins.test_decode_window_splits_cover_the_window(),
+    lambda: pins.test_mla_lambda0_equals_textbook_latent_attention(2),
+    lambda: pins.test_mla_skip_set_closed_form_and_masked_dense(),
+    lambda: pins.test_mla_sequence_lengths_truncate_the_cache(),
 ]
 
 

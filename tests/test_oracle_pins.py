@@ -481,6 +481,122 @@ def test_decode_partials_merge_by_lse():
     np.testing.assert_allclose(one["o_part"][0], one["o"], atol=0)
 
 
+# --------------------------------------------------------- MLA decode ---
+def np_latent_attention(q, kv, dv, scale, seq_lens=None, keep=None):
+    """Textbook attention over a latent cache with library matmuls (float64): for
+    head h of sequence b, softmax(scale * kv[:Lb] q_h) kv[:Lb, :dv].  ``keep``
+    optionally masks keys ([B, Lmax] bool).  Returns (o [B,Hq,dv], lse [B,Hq])."""
+    q = np.asarray(q, np.float64)
+    kv = np.asarray(kv, np.float64)
+    B, Hq, dk = q.shape
+    Lmax = kv.shape[1]
+    o = np.zeros((B, Hq, dv))
+    lse = np.full((B, Hq), -np.inf)
+    for b in range(B):
+        Lb = Lmax if seq_lens is None else min(max(int(seq_lens[b]), 0), Lmax)
+        if Lb == 0:
+            continue
+        s = scale * q[b] @ kv[b, :Lb].T  # [Hq, Lb]
+        if keep is not None:
+            s = np.where(keep[b, :Lb][None, :], s, -np.inf)
+        M = s.max(axis=1, keepdims=True)
+        p = np.exp(s - M)
+        o[b] = p @ kv[b, :Lb, :dv] / p.sum(axis=1, keepdims=True)
+        lse[b] = M[:, 0] + np.log(p.sum(axis=1))
+    return o, lse
+
+
+@pytest.mark.parametrize("S", [1, 2, 5])
+def test_mla_lambda0_equals_textbook_latent_attention(S):
+    """lambda = 0 skips nothing, and the latent form is plain attention whose keys
+    are the cached rows and whose values are their leading dv entries."""
+    B, Hq, L, dk, dv = 3, 4, 700, 24, 16
+    q, kv = rnd(90, B, Hq, dk), rnd(91, B, L, dk)
+    lens = [700, 333, 129]
+    res = orc.mla_decode_tiled(q, kv, dv, 0.5, 0.0, num_splits=S, seq_lens=lens, precision="f64")
+    assert res["skipped"] == 0
+    o, lse = np_latent_attention(q, kv, dv, 0.5, lens)
+    np.testing.assert_allclose(res["o"], o, atol=1e-12)
+    np.testing.assert_allclose(res["lse"], lse, atol=1e-12)
+
+
+def test_mla_skip_set_closed_form_and_masked_dense():
+    """One decision covers every query head x 128 keys; each split restarts the
+    running max; the merged result equals latent attention with the skipped key
+    tiles masked out."""
+    B, Hq, L, dk, dv = 2, 8, 1500, 24, 16
+    u = rnd(98, dk)
+    u /= np.linalg.norm(u)
+    q, kv = rnd(92, B, Hq, dk) + 3.0 * u, rnd(93, B, L, dk)
+    kv[:, :4] = 20.0 * u  # sink keys every head attends to
+    scale, lam = 0.3, 0.05
+    lens = [1500, 900]
+    for S in (1, 3):
+        res = orc.mla_decode_tiled(q, kv, dv, scale, lam, num_splits=S, seq_lens=lens, precision="f64")
+        assert res["skipped"] >= 3
+        keep = np.ones((B, L), bool)
+        for b in range(B):
+            nT = -(-lens[b] // 128)
+            s = scale * q[b] @ kv[b, :lens[b]].T
+            for sp in range(S):
+                t0, t1 = sp * nT // S, (sp + 1) * nT // S
+                run = np.full(Hq, -np.inf)
+                for t in range(t0, t1):
+                    mt = s[:, t * 128:(t + 1) * 128].max(axis=1)
+                    run = np.maximum(run, mt)
+                    sk = bool(np.all(mt - run < math.log(lam)))
+                    assert res["map"][b, t] == (1 if sk else 0)
+                    assert res["margin"][b, t] == pytest.approx(np.max(mt - run), abs=1e-12)
+                    if sk:
+                        keep[b, t * 128:(t + 1) * 128] = False
+            assert (res["map"][b, nT:] == 2).all() and np.isnan(res["margin"][b, nT:]).all()
+        o, lse = np_latent_attention(q, kv, dv, scale, lens, keep)
+        np.testing.assert_allclose(res["o"], o, atol=1e-12)
+        np.testing.assert_allclose(res["lse"], lse, atol=1e-12)
+
+
+def test_mla_equals_gqa_decode_with_one_kv_head_and_the_value_prefix():
+    """The latent form is GQA decode with one KV head holding the rows as keys and
+    their first dv entries (zero-padded) as values: same map, margins and output."""
+    B, Hq, L, dk, dv = 2, 4, 600, 16, 12
+    q, kv = rnd(94, B, Hq, dk), rnd(95, B, L, dk)
+    v = np.concatenate([kv[..., :dv], np.zeros((B, L, dk - dv))], axis=-1)
+    for lam in (0.0, 0.3):
+        a = orc.mla_decode_tiled(q, kv, dv, 1.1, lam, num_splits=2, precision="f64")
+        g = orc.decode_tiled(q, kv[:, None], v[:, None], 1.1, lam, num_splits=2, precision="f64")
+        assert a["skipped"] == g["skipped"]
+        np.testing.assert_array_equal(a["map"], g["map"][:, 0])
+        np.testing.assert_allclose(a["o"], g["o"][..., :dv], atol=1e-12)
+        assert np.all(g["o"][..., dv:] == 0)
+        np.testing.assert_allclose(a["lse"], g["lse"], atol=1e-12)
+
+
+def test_mla_sequence_lengths_truncate_the_cache():
+    """A sequence of length Lb gives what a cache of exactly Lb rows gives; a
+    sequence of length 0 gives O = 0 and lse = -inf; splits beyond a short
+    sequence's tiles are empty and change nothing."""
+    B, Hq, L, dk, dv = 3, 2, 520, 16, 8
+    q, kv = rnd(96, B, Hq, dk), rnd(97, B, L, dk)
+    lens = [520, 200, 0]
+    res = orc.mla_decode_tiled(q, kv, dv, 0.7, 0.2, num_splits=4, seq_lens=lens, precision="f64")
+    for b in range(2):
+        Lb = lens[b]
+        nT = -(-Lb // 128)
+        one = orc.mla_decode_tiled(q[b:b + 1], kv[b:b + 1, :Lb], dv, 0.7, 0.2, num_splits=min(4, nT),
+                                   precision="f64")
+        if nT >= 4:
+            np.testing.assert_array_equal(res["map"][b, :nT], one["map"][0])
+            np.testing.assert_allclose(res["o"][b], one["o"][0], atol=1e-12)
+        assert (res["map"][b, nT:] == 2).all()
+    assert np.all(res["o"][2] == 0) and np.all(np.isneginf(res["lse"][2]))
+    # two tiles over four splits: two splits are empty and the merge ignores them
+    short = orc.mla_decode_tiled(q, kv, dv, 0.7, 0.0, num_splits=4, seq_lens=[200, 200, 200], precision="f64")
+    ref, lref = np_latent_attention(q, kv, dv, 0.7, [200, 200, 200])
+    np.testing.assert_allclose(short["o"], ref, atol=1e-12)
+    np.testing.assert_allclose(short["lse"], lref, atol=1e-12)
+    assert np.all(np.isneginf(short["lse_part"][0])) and np.all(short["o_part"][0] == 0)
+
+
 # ---------------------------------------------------- lambda resolution ---
 def test_lambda_threshold_is_length_independent():
     for t in (0.0, 1e-4, 0.3, 0.99):
