@@ -221,6 +221,56 @@ int blasst_decode_noalloc(const void* q, const void* k_cache, const void* v_cach
 size_t blasst_decode_noalloc_scratch_bytes(void);
 
 /*
+ * Decode for multi-head latent attention in its absorbed form (the pages name MLA
+ * decode as the case where the skipped exponentials and P.V products pay, since it
+ * can be compute-bound: Skip-Softmax design doc, "Kernel"; they give no formula).
+ * Every cached token holds one row of dk = 576 bf16 values (a 512-value latent
+ * vector followed by a 64-value rotary key) shared by all query heads: head h
+ * scores it as scale * (q_h . row) over all dk values, and the token's value is the
+ * row's first dv = 512 values.  One skip decision covers all Hq heads x 128 keys.
+ *   q [B, Hq, dk], o [B, Hq, dv] bf16; lse nullable fp32 [B, Hq].
+ *   Hq           1, 2, 4, 8 or 16 query heads (else BLASST_ERR_UNSUPPORTED);
+ *                dk must be 576 and dv 512 (else BLASST_ERR_UNSUPPORTED).
+ *   kv           page_table NULL: contiguous bf16 [B][max_kv_len][dk];
+ *                page_table set: a pool of num_pages pages of page_size rows,
+ *                bf16 [num_pages][page_size][dk], row i of sequence b at row
+ *                i mod page_size of page page_table[b][i / page_size] (The
+ *                Hitchhiker's Guide, Phase 08, Section 3, "Paged Attention");
+ *                page_size 8, 16, 32, 64 or a multiple of 128, and
+ *                max_pages_per_seq * page_size >= max_kv_len.  16-byte aligned.
+ *                (num_pages, page_size, max_pages_per_seq are ignored without a
+ *                page table.)
+ *   seq_lens     nullable device int32 [B]: rows of sequence b (NULL: max_kv_len
+ *                each); a sequence of length 0 gives o = 0, lse = -inf.  Rows past
+ *                seq_lens[b] in the sequence's last 128-row tile (or page) are read
+ *                but get zero weight: they must hold finite values.
+ *   num_splits   1 .. ceil(max_kv_len / 128); blasst_mla_decode_num_splits plans one.
+ *                Split s of sequence b covers its tiles [floor(s*nT_b/S),
+ *                floor((s+1)*nT_b/S)), nT_b = ceil(seq_lens[b]/128); each split is an
+ *                independent pass and the splits are merged by log-sum-exp.
+ *   workspace    device memory of blasst_mla_decode_workspace_size bytes when
+ *                num_splits > 1 (16-byte aligned), else may be NULL.
+ *   skipped_tiles_out  nullable, zeroed then accumulated on the stream.
+ *   skip_map / margins nullable [B, ceil(max_kv_len/128)] (0 computed, 1 skipped,
+ *                2 not visited / the tile's max over heads of m~ - m, NaN if not
+ *                visited).
+ *   Out-of-range page indices and lengths are handled as for blasst_decode_paged.
+ */
+int blasst_mla_decode(const void* q, const void* kv, const int* page_table, const int* seq_lens, void* o,
+                      float* lse, int B, int Hq, int max_kv_len, int dk, int dv, int num_pages, int page_size,
+                      int max_pages_per_seq, float scale, float lambda, int num_splits, void* workspace,
+                      size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
+                      float* margins, void* stream);
+
+/* Split count for blasst_mla_decode: `requested` (1 .. ceil(max_kv_len/128)) if
+ * positive, else the fewest splits whose B * splits CTAs fill the last wave of the
+ * GPU's SMs to at least 90 %. */
+int blasst_mla_decode_num_splits(int B, int Hq, int max_kv_len, int requested, int* out);
+
+/* Workspace bytes blasst_mla_decode needs for num_splits splits (0 when 1). */
+size_t blasst_mla_decode_workspace_size(int B, int Hq, int max_kv_len, int num_splits);
+
+/*
  * Threshold resolution (Skip-Softmax design doc, "From configuration to the
  * kernel threshold"; BLASST talk notes, "threshold calibration", Eq. 3):
  *   mode 0 (threshold):        lambda = threshold           (any Lkv)

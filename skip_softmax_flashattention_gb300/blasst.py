@@ -77,6 +77,13 @@ def load(build_if_missing: bool = True):
     lib.blasst_decode_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, F, F, I, P, P, P, P]
     lib.blasst_decode_noalloc_scratch_bytes.restype = ctypes.c_size_t
     lib.blasst_decode_noalloc_scratch_bytes.argtypes = []
+    lib.blasst_mla_decode.restype = I
+    lib.blasst_mla_decode.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, I, I, F, F, I, P, ctypes.c_size_t,
+                                      P, P, P, P]
+    lib.blasst_mla_decode_num_splits.restype = I
+    lib.blasst_mla_decode_num_splits.argtypes = [I, I, I, I, ctypes.POINTER(I)]
+    lib.blasst_mla_decode_workspace_size.restype = ctypes.c_size_t
+    lib.blasst_mla_decode_workspace_size.argtypes = [I, I, I, I]
     lib.blasst_lambda.restype = I
     lib.blasst_lambda.argtypes = [I, ctypes.c_double, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                                   ctypes.c_longlong, ctypes.POINTER(ctypes.c_double)]
@@ -167,6 +174,25 @@ def blasst_decode_noalloc(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Lkv, d, scale
 
 def blasst_decode_noalloc_scratch_bytes() -> int:
     return int(load().blasst_decode_noalloc_scratch_bytes())
+
+
+def blasst_mla_decode(q, kv, page_table, seq_lens, o, lse, B, Hq, max_kv_len, dk, dv, num_pages, page_size,
+                      max_pages_per_seq, scale, lambda_, num_splits, workspace, workspace_bytes,
+                      skipped_tiles_out=None, skip_map=None, margins=None, stream=None) -> int:
+    return load().blasst_mla_decode(_ptr(q), _ptr(kv), _ptr(page_table), _ptr(seq_lens), _ptr(o), _ptr(lse), B, Hq,
+                                    max_kv_len, dk, dv, num_pages, page_size, max_pages_per_seq, float(scale),
+                                    float(lambda_), int(num_splits), _ptr(workspace), int(workspace_bytes),
+                                    _ptr(skipped_tiles_out), _ptr(skip_map), _ptr(margins), _stream(stream))
+
+
+def blasst_mla_decode_num_splits(B, Hq, max_kv_len, requested=0) -> tuple:
+    out = ctypes.c_int(0)
+    rc = load().blasst_mla_decode_num_splits(B, Hq, max_kv_len, requested, ctypes.byref(out))
+    return rc, out.value
+
+
+def blasst_mla_decode_workspace_size(B, Hq, max_kv_len, num_splits) -> int:
+    return int(load().blasst_mla_decode_workspace_size(B, Hq, max_kv_len, num_splits))
 
 
 def blasst_lambda(mode, threshold=0.0, a=math.nan, b=math.nan, target_sparsity=0.0, Lkv=1) -> tuple:
@@ -271,4 +297,42 @@ def decode_paged(q, k_pages, v_pages, page_table, seq_lens, max_kv_len: int, pag
                              num_pages, page_size, page_table.shape[1], token_major, scale, lam, S, ws, ws_bytes,
                              skipped, mp, mg, stream)
     _check(rc, "blasst_decode_paged")
+    return {"o": o, "lse": lse, "skipped": skipped, "map": mp, "margins": mg, "num_splits": S}
+
+
+MLA_DK, MLA_DV = 576, 512
+
+
+def mla_decode(q, kv, scale: float, lam: float, num_splits: int = 0, *, seq_lens=None, page_table=None,
+               page_size: int = 0, max_kv_len: int = 0, dv: int = MLA_DV, want_map=False, want_margins=False,
+               stream=None):
+    """Run blasst_mla_decode on torch tensors.  q [B,Hq,576] (or [B,Hq,1,576]); kv the
+    latent cache: [B, L, 576] without a page table, else a page pool [P, page_size, 576]
+    with page_table int32 [B, max_pages] (max_kv_len then required).  seq_lens int32 [B]
+    or None.  Returns dict(o [B,Hq,512], lse, skipped, map [B,nK], margins, num_splits)."""
+    import torch
+
+    q3 = q.reshape(q.shape[0], q.shape[1], q.shape[-1])
+    B, Hq, dk = q3.shape
+    if page_table is None:
+        max_kv_len = kv.shape[1]
+        num_pages = mpp = 0
+    else:
+        if max_kv_len < 1:
+            raise ValueError("max_kv_len is required with a page table")
+        num_pages, mpp = kv.shape[0], page_table.shape[1]
+    nK = -(-max_kv_len // TILE)
+    rc, S = blasst_mla_decode_num_splits(B, Hq, max_kv_len, num_splits)
+    _check(rc, "blasst_mla_decode_num_splits")
+    dev = q.device
+    ws_bytes = blasst_mla_decode_workspace_size(B, Hq, max_kv_len, S)
+    ws = torch.empty(max(ws_bytes, 16), device=dev, dtype=torch.uint8) if ws_bytes else None
+    o = torch.empty(B, Hq, dv, device=dev, dtype=q.dtype)
+    lse = torch.empty(B, Hq, device=dev, dtype=torch.float32)
+    skipped = torch.zeros(1, device=dev, dtype=torch.int64)
+    mp = torch.empty(B, nK, device=dev, dtype=torch.uint8) if want_map else None
+    mg = torch.empty(B, nK, device=dev, dtype=torch.float32) if want_margins else None
+    rc = blasst_mla_decode(q3, kv, page_table, seq_lens, o, lse, B, Hq, max_kv_len, dk, dv, num_pages, page_size,
+                           mpp, scale, lam, S, ws, ws_bytes, skipped, mp, mg, stream)
+    _check(rc, "blasst_mla_decode")
     return {"o": o, "lse": lse, "skipped": skipped, "map": mp, "margins": mg, "num_splits": S}

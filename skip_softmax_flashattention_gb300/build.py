@@ -1,6 +1,6 @@
 """Build the CUDA library (libblasst.so) in-tree for sm_103a with nvcc.
 
-The three translation units are compiled in parallel and linked into
+The translation units are compiled in parallel and linked into
 skip_softmax_flashattention_gb300/_build/libblasst.so (the CUDA runtime is linked
 statically; the driver is reached through the runtime at call time).
 """
@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libblasst.so")
-SOURCES = ["api.cu", "prefill.cu", "prefill_wide.cu", "decode.cu", "decode_noalloc.cu"]
+SOURCES = ["api.cu", "prefill.cu", "prefill_wide.cu", "decode.cu", "decode_noalloc.cu", "mla_decode.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -113,6 +113,38 @@ Thresholds thresholds(float scale, float lambda) {
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? BLASST_OK : BLASST_ERR_CUDA; }
 
+// One decode CTA fits per SM.  Take the fewest splits whose `units` x splits CTAs
+// fill the last wave to at least 90%; more splits restart the running max more often.
+int plan_splits(long long units, int nT, int* out) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return BLASST_ERR_CUDA;
+    int best = 1;
+    double best_eff = 0.0;
+    for (int S = 1; S <= nT && S <= 64; ++S) {
+        const double waves = (double)(units * S) / sms;
+        const double eff = waves / std::ceil(waves);
+        if (eff >= 0.9) {
+            best = S;
+            best_eff = eff;
+            break;
+        }
+        if (eff > best_eff + 1e-9) {
+            best_eff = eff;
+            best = S;
+        }
+    }
+    *out = best;
+    return BLASST_OK;
+}
+
+bool page_size_ok(int page_size) {
+    // a 128-key tile is whole pages or lies inside one page
+    return page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64 ||
+           (page_size > 0 && page_size % kTile == 0);
+}
+
 }  // namespace
 
 extern "C" {
@@ -232,30 +264,7 @@ int blasst_decode_num_splits(int B, int Hq, int Hkv, int Lkv, int d, int request
         *out = requested;
         return BLASST_OK;
     }
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
-        return BLASST_ERR_CUDA;
-    // One decode CTA fits per SM.  Take the fewest splits whose CTA count fills the
-    // last wave to at least 90%; more splits restart the running max more often.
-    const long long units = (long long)B * Hkv;
-    int best = 1;
-    double best_eff = 0.0;
-    for (int S = 1; S <= nT && S <= 64; ++S) {
-        const double waves = (double)(units * S) / sms;
-        const double eff = waves / std::ceil(waves);
-        if (eff >= 0.9) {
-            best = S;
-            best_eff = eff;
-            break;
-        }
-        if (eff > best_eff + 1e-9) {
-            best_eff = eff;
-            best = S;
-        }
-    }
-    *out = best;
-    return BLASST_OK;
+    return plan_splits((long long)B * Hkv, nT, out);
 }
 
 size_t blasst_decode_workspace_size(int B, int Hq, int Hkv, int Lkv, int d, int num_splits) {
@@ -373,9 +382,7 @@ int blasst_decode_paged(const void* q, const void* k_pages, const void* v_pages,
     const int G = Hq / Hkv;
     if (d != 128) return BLASST_ERR_UNSUPPORTED;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BLASST_ERR_UNSUPPORTED;
-    // a 128-key tile is whole pages (8, 16, 32 or 64 keys each) or lies inside one page
-    if (!(page_size == 8 || page_size == 16 || page_size == 32 || page_size == 64 || page_size % kTile == 0))
-        return BLASST_ERR_UNSUPPORTED;
+    if (!page_size_ok(page_size)) return BLASST_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
         (reinterpret_cast<uintptr_t>(page_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
@@ -404,6 +411,107 @@ int blasst_decode_paged(const void* q, const void* k_pages, const void* v_pages,
     p.window = window;
     return run_decode(tk, tv, p, q, o, lse, B, Hq, Hkv, max_kv_len, d, scale, lambda, num_splits, workspace,
                       skipped_tiles_out, skip_map, margins, stream);
+}
+
+int blasst_mla_decode_num_splits(int B, int Hq, int max_kv_len, int requested, int* out) {
+    if (!out || B < 1 || Hq < 1 || max_kv_len < 1 || requested < 0) return BLASST_ERR_INVALID_ARG;
+    const int nT = (max_kv_len + kTile - 1) / kTile;
+    if (requested > 0) {
+        if (requested > nT) return BLASST_ERR_INVALID_ARG;
+        *out = requested;
+        return BLASST_OK;
+    }
+    return plan_splits((long long)B, nT, out);  // one CTA per (sequence, split)
+}
+
+size_t blasst_mla_decode_workspace_size(int B, int Hq, int max_kv_len, int num_splits) {
+    return blasst_decode_workspace_size(B, Hq, 1, max_kv_len, blasst::kMlaDv, num_splits);
+}
+
+int blasst_mla_decode(const void* q, const void* kv, const int* page_table, const int* seq_lens, void* o,
+                      float* lse, int B, int Hq, int max_kv_len, int dk, int dv, int num_pages, int page_size,
+                      int max_pages_per_seq, float scale, float lambda, int num_splits, void* workspace,
+                      size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
+                      float* margins, void* stream) {
+    if (!q || !kv || !o) return BLASST_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || max_kv_len < 1 || dk < 1 || dv < 1) return BLASST_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || !lambda_ok(lambda)) return BLASST_ERR_INVALID_ARG;
+    if (page_table) {
+        if (num_pages < 1 || page_size < 1 || max_pages_per_seq < 1) return BLASST_ERR_INVALID_ARG;
+        if ((long long)max_pages_per_seq * page_size < max_kv_len) return BLASST_ERR_INVALID_ARG;
+    }
+    const int nT = (max_kv_len + kTile - 1) / kTile;
+    if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
+    if (dk != blasst::kMlaDk || dv != blasst::kMlaDv) return BLASST_ERR_UNSUPPORTED;
+    if (Hq != 1 && Hq != 2 && Hq != 4 && Hq != 8 && Hq != 16) return BLASST_ERR_UNSUPPORTED;
+    if (page_table && !page_size_ok(page_size)) return BLASST_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(kv) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
+        (reinterpret_cast<uintptr_t>(page_table) & 3u) || (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+        (reinterpret_cast<uintptr_t>(skipped_tiles_out) & 7u))
+        return BLASST_ERR_UNSUPPORTED;
+    if (B > 65535) return BLASST_ERR_UNSUPPORTED;
+    const size_t need = blasst_mla_decode_workspace_size(B, Hq, max_kv_len, num_splits);
+    if (num_splits > 1) {
+        if (!workspace) return BLASST_ERR_INVALID_ARG;
+        if (workspace_bytes < need) return BLASST_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned16(workspace)) return BLASST_ERR_UNSUPPORTED;
+    }
+    CUtensorMap tkv;
+    const int rows = page_size < kTile ? page_size : kTile;
+    if (page_table ? !encode_pages(&tkv, kv, dk, page_size, 1, num_pages, 1, rows)
+                   : !encode_3d(&tkv, kv, dk, max_kv_len, B))
+        return BLASST_ERR_CUDA;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* status = status_word();
+    if (!status) return BLASST_ERR_CUDA;
+    const long long map_n = (long long)B * nT;
+    if (skipped_tiles_out && cudaMemsetAsync(skipped_tiles_out, 0, sizeof(unsigned long long), st) != cudaSuccess)
+        return BLASST_ERR_CUDA;
+    if (skip_map && cudaMemsetAsync(skip_map, 2, (size_t)map_n, st) != cudaSuccess) return BLASST_ERR_CUDA;
+    if (margins && cudaMemsetAsync(margins, 0xFF, (size_t)map_n * sizeof(float), st) != cudaSuccess)
+        return BLASST_ERR_CUDA;
+
+    const Thresholds t = thresholds(scale, lambda);
+    blasst::DecodeParams p{};
+    p.q = static_cast<const uint16_t*>(q);
+    p.o = o;
+    p.lse = lse;
+    const size_t o_bytes = (size_t)num_splits * B * Hq * dv * sizeof(float);
+    p.o_part = num_splits > 1 ? static_cast<float*>(workspace) : nullptr;
+    p.lse_part = num_splits > 1
+                     ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) & ~size_t(255)))
+                     : nullptr;
+    p.B = B; p.Hq = Hq; p.Hkv = 1; p.Lkv = max_kv_len; p.G = Hq; p.nK = nT; p.S = num_splits;
+    p.c_log2 = t.c_log2;
+    p.scale = scale;
+    p.thr_raw = t.thr_raw;
+    p.lazy_raw = t.lazy_raw;
+    p.skipped = skipped_tiles_out;
+    p.skip_map = skip_map;
+    p.margins = margins;
+    p.status = status;
+    p.watchdog_ns = kWatchdogNs;
+    p.seq_lens = seq_lens;
+    p.page_table = page_table;
+    p.max_pages = max_pages_per_seq;
+    p.num_pages = num_pages;
+    p.page_size = page_size;
+    p.rows_per_box = rows;
+    p.token_major = 1;
+    cudaError_t e = blasst::launch_mla_decode(tkv, p, st);
+    if (e != cudaSuccess) return BLASST_ERR_CUDA;
+    if (num_splits > 1) {
+        blasst::CombineParams c{};
+        c.o_part = p.o_part;
+        c.lse_part = p.lse_part;
+        c.o = o;
+        c.lse = lse;
+        c.B = B; c.Hq = Hq; c.S = num_splits; c.d = dv;
+        e = blasst::launch_combine(c, st);
+    }
+    return cuda_status(e);
 }
 
 int blasst_lambda(int mode, double threshold, double a, double b, double target_sparsity, long long Lkv,

@@ -96,6 +96,10 @@ cudaError_t launch_prefill_wide(const CUtensorMap& tq, const CUtensorMap& tk, co
 cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p, int d,
                           cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
+// MLA decode (absorbed form): rows of kMlaDk values, values = their first kMlaDv.
+// DecodeParams carries Hq = G = the query heads (1, 2, 4, 8 or 16), Hkv = 1, d = kMlaDk.
+constexpr int kMlaDk = 576, kMlaDv = 512;
+cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream);
 
 
 }  // namespace blasst

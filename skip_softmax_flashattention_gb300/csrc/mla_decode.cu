@@ -1,0 +1,521 @@
+// mla_decode.cu -- skip-softmax (BLASST) decode for multi-head latent attention
+// (MLA) in its absorbed form, on sm_103a.
+//
+// Every cached token holds ONE row of DK = 576 values (a 512-value latent vector
+// followed by a 64-value rotary key) that all query heads read: the score of head
+// h is scale * (q_h . row) over the 576 values and the token's value vector is the
+// row's first DV = 512 values.  All heads read the same rows, as the heads of a
+// GQA group read their KV head, so the heads of a sequence form the rows of every
+// tile and one skip decision covers all of them x 128 keys.  The pages name MLA
+// decode as the case where skipping the exponentials and the P.V products pays,
+// because it can be compute-bound (Skip-Softmax design doc, "Kernel").
+//
+// One CTA runs one (sequence b, split s) pass over the split's key tiles in
+// ascending order.  Both products run with the key dimension on the 128 TMEM
+// lanes, as in the GQA decode kernel:
+//   S^T_j = K_j Q^T      M = 128 keys, N = 16 (heads, zero-padded), K = 576 (36 MMAs)
+//   O^T_j = V_j^T P_j^T  four M = 128 blocks of the 512 value columns, N = 16, K = 128 keys
+// A 576-wide key tile is 144 KB, more than a ring of whole tiles leaves room for,
+// so tiles stream through a ring of 64-column boxes (16 KB) and the S MMAs of a
+// tile are issued box by box as the boxes land.  A kept tile's value columns are
+// read a second time after its decision, in 128-column pairs of boxes: the key
+// stream never waits for a decision, the second read finds the rows in L2 (they
+// were read a few microseconds earlier), and a skipped tile's values are never
+// read again.  Each P.V result lands in a fresh TMEM slot and is folded into
+// per-thread registers a few tiles later (thread t owns value columns t, t+128,
+// t+256, t+384 of every head).
+//
+// Warp roles (224 threads): warps 0-3 softmax, warp 4 key loader, warp 5 MMA
+// issuer and TMEM owner, warp 6 value loader.
+//
+// Paged form: the cache is a pool of pages of page_size rows and a page table maps
+// each page-sized run of a sequence's keys to a page (The Hitchhiker's Guide, Phase
+// 08, Section 3, "Paged Attention").  A 128-key box is then fetched as 128 /
+// page_size boxes (page_size < 128) or as one box inside a page; boxes past the
+// end of the sequence, or with an out-of-range page index, read as zeros.
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "kernels.cuh"
+#include "ptx.cuh"
+
+namespace blasst {
+namespace {
+
+constexpr unsigned long long kDrainNs = 1000000000ull;
+
+constexpr int DK = kMlaDk;               // 576
+constexpr int DV = kMlaDv;               // 512
+constexpr int KBOX = DK / 64;            // 64-column boxes per key tile
+constexpr int VBLK = DV / 128;           // 128-column value blocks (box pairs) per key tile
+constexpr int NPAD = 16;                 // MMA N: the heads padded to 16
+constexpr int BOX_BYTES = kTile * 128;   // 128 keys x 64 columns
+constexpr int PAIR_BYTES = 2 * BOX_BYTES;
+constexpr int NKB = 6;                   // key box ring
+constexpr int NVP = 2;                   // value pair ring
+constexpr int NS = 4, NO = 4;            // TMEM S slots (16 columns) / O slots (64 columns)
+constexpr int NP = 4;                    // P staging buffers
+constexpr int ND = 8;                    // decision ring
+constexpr int NH = 8;                    // reference-max history ring
+constexpr int LOOKAHEAD = 3;             // S passes issued ahead of the P.V pass
+constexpr int LAG = 2;                   // P.V results folded this many computed tiles late
+constexpr int Q_BYTES = KBOX * NPAD * 128;
+constexpr int P_BYTES = 2 * NPAD * 128;  // [key half][16 rows][64 keys]
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + NKB * BOX_BYTES;
+constexpr int OFF_Q = OFF_V + NVP * PAIR_BYTES;
+constexpr int OFF_P = OFF_Q + Q_BYTES;
+constexpr int OFF_CTRL = OFF_P + NP * P_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t O_COL = NS * NPAD;
+constexpr int O_SLOT = VBLK * NPAD;      // block i of a slot: columns [16i, 16i + 16)
+static_assert(O_COL + NO * O_SLOT <= TMEM_COLS, "TMEM budget");
+static_assert(LAG <= NO && LOOKAHEAD + 1 <= NS && LOOKAHEAD + 2 <= ND, "ring sizes");
+static_assert(DK % 64 == 0 && DV % 128 == 0 && DV <= DK, "row layout");
+
+struct MlaCtrl {
+    uint64_t k_full[NKB], k_empty[NKB], v_full[NVP], v_empty[NVP];
+    uint64_t s_full[NS], s_free[NS], dec_full[ND], dec_free[ND];
+    uint64_t p_full[NP], p_free[NP], o_full[NO], o_free[NO];
+    uint64_t q_full, drain;
+    uint32_t tmem_base;
+    int dec[ND];
+    int abort;
+    float red[2][4][NPAD];
+    float mref_hist[NH][NPAD];
+    float lred[4][NPAD];
+};
+constexpr int SMEM = OFF_CTRL + (int)sizeof(MlaCtrl) + 1024;
+static_assert(SMEM <= 232448, "shared memory per CTA");
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+template <int G, bool PAGED>
+__global__ void __launch_bounds__(224, 1)
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const DecodeParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align1024(smem_raw);
+    MlaCtrl* ctrl = reinterpret_cast<MlaCtrl*>(smem + OFF_CTRL);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int s = blockIdx.x, b = blockIdx.z;
+    // This sequence's keys and this split's share of its tiles: [s*nT/S, (s+1)*nT/S).
+    int Lb = p.Lkv;
+    if (p.seq_lens) {
+        const int v = p.seq_lens[b];
+        Lb = min(max(v, 0), p.Lkv);
+        if (tid == 0 && s == 0 && v != Lb) atomicOr(p.status, kStatusPageTable);
+    }
+    const int nTb = (Lb + kTile - 1) / kTile;
+    const int t0 = (int)(((long long)s * nTb) / p.S);
+    const int t1 = (int)(((long long)(s + 1) * nTb) / p.S);
+    const int n = t1 - t0;
+
+    if (tid == 0) {
+        for (int i = 0; i < NKB; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
+        for (int i = 0; i < NVP; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
+        for (int i = 0; i < NS; ++i) { mbar_init(&ctrl->s_full[i], 1); mbar_init(&ctrl->s_free[i], 4); }
+        for (int i = 0; i < ND; ++i) {
+            mbar_init(&ctrl->dec_full[i], 1);
+            mbar_init(&ctrl->dec_free[i], 2);  // released by the MMA issuer and the value loader
+        }
+        for (int i = 0; i < NP; ++i) { mbar_init(&ctrl->p_full[i], 4); mbar_init(&ctrl->p_free[i], 1); }
+        for (int i = 0; i < NO; ++i) { mbar_init(&ctrl->o_full[i], 1); mbar_init(&ctrl->o_free[i], 4); }
+        mbar_init(&ctrl->q_full, 4);
+        mbar_init(&ctrl->drain, 1);
+        ctrl->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(&ctrl->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    __syncwarp();  // the set-up above diverged inside warps; bar.sync is warp-aligned
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctrl->tmem_base;
+    const Watchdog wd{&ctrl->abort, p.status, p.watchdog_ns};
+
+    // Paged form: sub-box i of a 64-column box covers keys [i*rows, (i+1)*rows) of
+    // the tile, one page run; lane i of a loader warp reads its page index once
+    // per tile and issues that sub-box of every column box.
+    const int nbox = PAGED ? kTile / p.rows_per_box : 1;
+    auto box_page = [&](int tile, int i) -> int {
+        int e = p.num_pages;  // out of range: the sub-box reads as zeros
+        const int key = tile * kTile + i * p.rows_per_box;
+        if (i < nbox && key < Lb) {
+            const int v = p.page_table[(long long)b * p.max_pages + key / p.page_size];
+            if (v >= 0 && v < p.num_pages)
+                e = v;
+            else
+                atomicOr(p.status, kStatusPageTable);
+        }
+        return e;
+    };
+    auto issue_sub_box = [&](uint8_t* dst, uint64_t* bar, int x, int tile, int i, int pg) {
+        const int off = (tile * kTile + i * p.rows_per_box) % p.page_size;
+        tma_load_4d(dst + i * p.rows_per_box * 128, &tkv, bar, x, 0, off, pg);
+    };
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ key loader
+        // box c of tile j is ring entry j*KBOX + c
+        if constexpr (!PAGED) {
+            if (lane == 0) {
+                tma_prefetch_desc(&tkv);
+                int issued = 0;
+                bool ok = true;
+                for (int j = 0; j < n && ok; ++j) {
+                    for (int c = 0; c < KBOX; ++c) {
+                        const int e = j * KBOX + c, ks = e % NKB;
+                        if (e >= NKB && !(ok = mbar_wait(&ctrl->k_empty[ks], ((e / NKB) - 1) & 1, wd))) break;
+                        mbar_arrive_expect_tx(&ctrl->k_full[ks], BOX_BYTES);
+                        tma_load_3d(smem + OFF_K + ks * BOX_BYTES, &tkv, &ctrl->k_full[ks], c * 64, (t0 + j) * kTile, b);
+                        issued = e + 1;
+                    }
+                }
+                for (int e = max(0, issued - NKB); e < issued; ++e)
+                    mbar_wait_drain(&ctrl->k_full[e % NKB], (e / NKB) & 1, kDrainNs);
+            }
+        } else {
+            if (lane == 0) tma_prefetch_desc(&tkv);
+            int issued = 0;
+            bool ok = true;
+            for (int j = 0; j < n && ok; ++j) {
+                const int pg = box_page(t0 + j, lane);
+                for (int c = 0; c < KBOX; ++c) {
+                    const int e = j * KBOX + c, ks = e % NKB;
+                    int go = 1;
+                    if (lane == 0) {
+                        if (e >= NKB && !mbar_wait(&ctrl->k_empty[ks], ((e / NKB) - 1) & 1, wd))
+                            go = 0;
+                        else
+                            mbar_arrive_expect_tx(&ctrl->k_full[ks], BOX_BYTES);
+                    }
+                    if (!(ok = __shfl_sync(0xffffffffu, go, 0) != 0)) break;
+                    if (lane < nbox) issue_sub_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, t0 + j, lane, pg);
+                    issued = e + 1;
+                }
+            }
+            if (lane == 0)
+                for (int e = max(0, issued - NKB); e < issued; ++e)
+                    mbar_wait_drain(&ctrl->k_full[e % NKB], (e / NKB) & 1, kDrainNs);
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ value loader
+        // pair i of the c-th computed tile is ring entry c*VBLK + i
+        int issued = 0;
+        bool ok = true;
+        for (int j = 0; j < n && ok; ++j) {
+            const int pg = PAGED ? box_page(t0 + j, lane) : 0;  // read while lane 0 waits for the decision
+            int go = 0;  // 0: stop, 1: load the tile's values, 2: tile skipped
+            if (lane == 0 && mbar_wait(&ctrl->dec_full[j % ND], (j / ND) & 1, wd)) {
+                const bool skipped = reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] != 0;
+                mbar_arrive(&ctrl->dec_free[j % ND]);
+                go = skipped ? 2 : 1;  // skipped: its values are not read again
+            }
+            go = __shfl_sync(0xffffffffu, go, 0);
+            if (go == 0) break;
+            if (go == 2) continue;
+            for (int i = 0; i < VBLK; ++i) {
+                const int e = issued, vs = e % NVP;
+                int gv = 1;
+                if (lane == 0) {
+                    if (e >= NVP && !mbar_wait(&ctrl->v_empty[vs], ((e / NVP) - 1) & 1, wd)) {
+                        gv = 0;
+                    } else {
+                        mbar_arrive_expect_tx(&ctrl->v_full[vs], PAIR_BYTES);
+                        if constexpr (!PAGED) {
+#pragma unroll
+                            for (int h = 0; h < 2; ++h)
+                                tma_load_3d(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &tkv, &ctrl->v_full[vs],
+                                            i * 128 + h * 64, (t0 + j) * kTile, b);
+                        }
+                    }
+                }
+                if (!(ok = __shfl_sync(0xffffffffu, gv, 0) != 0)) break;
+                if constexpr (PAGED) {
+                    if (lane < nbox) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            issue_sub_box(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
+                                          i * 128 + h * 64, t0 + j, lane, pg);
+                    }
+                }
+                issued = e + 1;
+            }
+        }
+        if (lane == 0)
+            for (int e = max(0, issued - NVP); e < issued; ++e)
+                mbar_wait_drain(&ctrl->v_full[e % NVP], (e / NVP) & 1, kDrainNs);
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescS = idesc_bf16(128, NPAD, false, false);
+            constexpr uint32_t kIdescO = idesc_bf16(128, NPAD, true, false);
+            const uint32_t sK = smem_u32(smem + OFF_K), sV = smem_u32(smem + OFF_V);
+            const uint32_t sQ = smem_u32(smem + OFF_Q), sP = smem_u32(smem + OFF_P);
+            // S^T_j, box by box as the key boxes land; each box's slot is released by a
+            // commit after its four MMAs
+            auto issue_s = [&](int j) -> bool {
+                const int ss = j % NS;
+                if (j >= NS && !mbar_wait(&ctrl->s_free[ss], ((j / NS) - 1) & 1, wd)) return false;
+                for (int c = 0; c < KBOX; ++c) {
+                    const int e = j * KBOX + c, ks = e % NKB;
+                    if (!mbar_wait(&ctrl->k_full[ks], (e / NKB) & 1, wd)) return false;
+                    tc_fence_after();
+                    const uint32_t kb = sK + ks * BOX_BYTES, qb = sQ + c * (NPAD * 128);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(tmem + ss * NPAD, desc_kmajor_sw128(kb + kk * 32), desc_kmajor_sw128(qb + kk * 32),
+                               kIdescS, (c > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit(&ctrl->k_empty[ks]);
+                }
+                mma_commit(&ctrl->s_full[ss]);
+                return true;
+            };
+            bool ok = mbar_wait(&ctrl->q_full, 0, wd);
+            for (int j = 0; j < min(LOOKAHEAD, n) && ok; ++j) ok = issue_s(j);
+            int comp = 0;
+            for (int j = 0; j < n && ok; ++j) {
+                if (j + LOOKAHEAD < n && !(ok = issue_s(j + LOOKAHEAD))) break;
+                if (!(ok = mbar_wait(&ctrl->dec_full[j % ND], (j / ND) & 1, wd))) break;
+                const bool skipped = reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] != 0;
+                mbar_arrive(&ctrl->dec_free[j % ND]);
+                if (skipped) continue;
+                const int pb = comp % NP, os = comp % NO;
+                if (!(ok = mbar_wait(&ctrl->p_full[pb], (comp / NP) & 1, wd))) break;
+                if (comp >= NO && !(ok = mbar_wait(&ctrl->o_free[os], ((comp / NO) - 1) & 1, wd))) break;
+                const uint32_t pbuf = sP + pb * P_BYTES;
+                for (int i = 0; i < VBLK && ok; ++i) {
+                    const int e = comp * VBLK + i, vs = e % NVP;
+                    if (!(ok = mbar_wait(&ctrl->v_full[vs], (e / NVP) & 1, wd))) break;
+                    tc_fence_after();
+                    const uint32_t vb = sV + vs * PAIR_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk) {
+                        const uint64_t adesc = desc_mnmajor_sw128(vb + kk * 2048, BOX_BYTES);
+                        const uint64_t bdesc = desc_kmajor_sw128(pbuf + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32);
+                        mma_ss(tmem + O_COL + os * O_SLOT + i * NPAD, adesc, bdesc, kIdescO, kk > 0 ? 1u : 0u);
+                    }
+                    mma_commit(&ctrl->v_empty[vs]);
+                }
+                if (!ok) break;
+                mma_commit(&ctrl->o_full[os]);
+                mma_commit(&ctrl->p_free[pb]);
+                ++comp;
+            }
+            mma_commit(&ctrl->drain);
+            mbar_wait_drain(&ctrl->drain, 0, kDrainNs);
+        }
+    } else {
+        // ------------------------------------------------------------ softmax (warps 0-3)
+        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        // Stage Q (rows = heads, zero-padded to 16) and clear the P buffers' padding rows.
+        {
+            uint8_t* sq = smem + OFF_Q;
+            for (int c = tid; c < NPAD * (DK / 8); c += 128) {
+                const int g = c / (DK / 8), ck = c % (DK / 8);
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (g < G) v = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + g) * DK + ck * 8);
+                const int box = ck >> 3, cw = ck & 7;
+                *reinterpret_cast<uint4*>(sq + box * (NPAD * 128) + g * 128 + ((cw ^ (g & 7)) << 4)) = v;
+            }
+            uint4* sp = reinterpret_cast<uint4*>(smem + OFF_P);
+            for (int c = tid; c < NP * P_BYTES / 16; c += 128) sp[c] = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->q_full);
+        }
+        const long long mapbase = (long long)b * p.nK;
+        const float cl = p.c_log2;
+        float m_exact[G], m_ref[G], lpart[G], oacc[VBLK][G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            m_exact[g] = -CUDART_INF_F;
+            m_ref[g] = -CUDART_INF_F;
+            lpart[g] = 0.f;
+#pragma unroll
+            for (int i = 0; i < VBLK; ++i) oacc[i][g] = 0.f;
+        }
+        int comp = 0, folded = 0;
+        unsigned long long nskip = 0;
+
+        auto fold = [&](int c) {
+            const int os = c % NO;
+            mbar_wait(&ctrl->o_full[os], (c / NO) & 1, wd);
+            tc_fence_after();
+            uint32_t yr[O_SLOT];
+            tmem_ld32(tl + O_COL + os * O_SLOT, yr);
+            tmem_ld32(tl + O_COL + os * O_SLOT + 32, yr + 32);
+            tmem_ld_wait();
+            fence_regs<O_SLOT>(yr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->o_free[os]);
+            const volatile float* mh = ctrl->mref_hist[c % NH];
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float f = (mh[g] == m_ref[g]) ? 1.f : ex2((mh[g] - m_ref[g]) * cl);
+#pragma unroll
+                for (int i = 0; i < VBLK; ++i) oacc[i][g] = fmaf(f, __uint_as_float(yr[i * NPAD + g]), oacc[i][g]);
+            }
+        };
+
+        for (int j = 0; j < n; ++j) {
+            const int ss = j % NS;
+            mbar_wait(&ctrl->s_full[ss], (j / NS) & 1, wd);
+            tc_fence_after();
+            uint32_t xr[16];
+            tmem_ld16(tl + ss * NPAD, xr);
+            tmem_ld_wait();
+            fence_regs<16>(xr);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->s_free[ss]);
+            const int key = (t0 + j) * kTile + tid;
+            const bool key_ok = key < Lb;
+            float x[G];
+#pragma unroll
+            for (int g = 0; g < G; ++g) x[g] = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
+            // per-head tile max over the 128 keys: warp shuffle, then across the 4 warps
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                float v = x[g];
+#pragma unroll
+                for (int sh = 16; sh > 0; sh >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, sh));
+                if (lane == 0) ctrl->red[j & 1][warp][g] = v;
+            }
+            named_bar_sync(1, 128);
+            float mnew[G];
+            bool skip = true;
+            float margin = -CUDART_INF_F;
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const volatile float* rd = &ctrl->red[j & 1][0][g];
+                const float mt = fmaxf(fmaxf(rd[0], rd[NPAD]), fmaxf(rd[2 * NPAD], rd[3 * NPAD]));
+                mnew[g] = fmaxf(m_exact[g], mt);
+                const float diff = mt - mnew[g];
+                skip = skip && (diff < p.thr_raw);
+                const float gm = (mt == -CUDART_INF_F && mnew[g] == -CUDART_INF_F) ? CUDART_INF_F : diff;
+                margin = fmaxf(margin, gm);
+                m_exact[g] = mnew[g];
+            }
+            if (tid == 0) {
+                // the slot is reused only after both readers of tile j - ND released it
+                if (j >= ND) mbar_wait(&ctrl->dec_free[j % ND], ((j / ND) - 1) & 1, wd);
+                reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] = skip ? 1 : 0;
+                mbar_arrive(&ctrl->dec_full[j % ND]);
+                if (p.skip_map) p.skip_map[mapbase + t0 + j] = skip ? 1 : 0;
+                if (p.margins) p.margins[mapbase + t0 + j] = margin * p.scale;
+                nskip += skip ? 1 : 0;
+            }
+            if (!skip) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    if (mnew[g] != -CUDART_INF_F && (m_ref[g] == -CUDART_INF_F || mnew[g] > m_ref[g] + p.lazy_raw)) {
+                        const float a = m_ref[g] == -CUDART_INF_F ? 0.f : ex2((m_ref[g] - mnew[g]) * cl);
+#pragma unroll
+                        for (int i = 0; i < VBLK; ++i) oacc[i][g] *= a;
+                        lpart[g] *= a;
+                        m_ref[g] = mnew[g];
+                    }
+                }
+                if (tid == 0) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) ctrl->mref_hist[comp % NH][g] = m_ref[g];
+                }
+                const int pb = comp % NP;
+                if (comp >= NP) mbar_wait(&ctrl->p_free[pb], ((comp / NP) - 1) & 1, wd);
+                uint8_t* pbuf = smem + OFF_P + pb * P_BYTES + (tid >> 6) * (NPAD * 128);
+                const int cw = (tid & 63) >> 3;
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float mr = m_ref[g] == -CUDART_INF_F ? 0.f : m_ref[g];
+                    const float pv = ex2(fmaf(x[g], cl, -mr * cl));
+                    lpart[g] += pv;
+                    *reinterpret_cast<unsigned short*>(pbuf + g * 128 + ((cw ^ (g & 7)) << 4) + (tid & 7) * 2) =
+                        (unsigned short)(pack_bf16x2(pv, 0.f) & 0xffffu);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
+                ++comp;
+            }
+            while (comp - folded > LAG) fold(folded++);
+        }
+        named_bar_sync(1, 128);
+        while (folded < comp) fold(folded++);
+
+        // l = sum over the 128 key lanes; O = oacc / l
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            float v = lpart[g];
+#pragma unroll
+            for (int sh = 16; sh > 0; sh >>= 1) v += __shfl_xor_sync(0xffffffffu, v, sh);
+            if (lane == 0) ctrl->lred[warp][g] = v;
+        }
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const volatile float* lr = &ctrl->lred[0][g];
+            const float l = lr[0] + lr[NPAD] + lr[2 * NPAD] + lr[3 * NPAD];
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+            const float lse = l > 0.f ? m_ref[g] * p.scale + __logf(l) : -CUDART_INF_F;
+            const long long hq = (long long)b * p.Hq + g;
+            if (p.S == 1) {
+#pragma unroll
+                for (int i = 0; i < VBLK; ++i)
+                    reinterpret_cast<unsigned short*>(p.o)[hq * DV + i * 128 + tid] =
+                        (unsigned short)(pack_bf16x2(oacc[i][g] * inv, 0.f) & 0xffffu);
+                if (tid == 0 && p.lse) p.lse[hq] = lse;
+            } else {
+                const long long ps = (long long)s * p.B * p.Hq + hq;
+#pragma unroll
+                for (int i = 0; i < VBLK; ++i) p.o_part[ps * DV + i * 128 + tid] = oacc[i][g] * inv;
+                if (tid == 0) p.lse_part[ps] = lse;
+            }
+        }
+        if (tid == 0 && p.skipped && nskip) atomicAdd(p.skipped, nskip);
+    }
+
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+template <int G, bool PAGED>
+cudaError_t launch_gp(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.S, 1, p.B);
+    mla_decode_kernel<G, PAGED><<<grid, 224, SMEM, stream>>>(tkv, p);
+    return cudaGetLastError();
+}
+template <int G>
+cudaError_t launch_g(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
+    return p.page_table ? launch_gp<G, true>(tkv, p, stream) : launch_gp<G, false>(tkv, p, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
+    switch (p.Hq) {
+        case 1: return launch_g<1>(tkv, p, stream);
+        case 2: return launch_g<2>(tkv, p, stream);
+        case 4: return launch_g<4>(tkv, p, stream);
+        case 8: return launch_g<8>(tkv, p, stream);
+        case 16: return launch_g<16>(tkv, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace blasst

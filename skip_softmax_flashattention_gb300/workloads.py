@@ -271,6 +271,57 @@ def paged_decode(seed: int = 0, B: int = 8, Hq: int = 32, Hkv: int = 8, max_len:
     return a
 
 
+def mla_decode(seed: int = 0, B: int = 64, Hq: int = 16, L: int = 32768, dk: int = 576, dv: int = 512,
+               device="cpu", sinks: int = 4, lens=None, min_len: int = 1, page_size: int = 0,
+               spare_pages: int = 7) -> Attn:
+    """MLA decode in absorbed form: q [B,Hq,1,dk]; one latent cache kv [B,L,dk]
+    whose rows are the keys of every head and whose first dv columns are the
+    values.  The decode recipe applied to the latent rows: q and kv N(0,1), scores
+    scaled by 2/sqrt(dk), and the first ``sinks`` rows of each sequence sink keys
+    along unit(mean of its queries), here with an ordinary row's norm sqrt(dk) (one
+    decision covers all Hq heads, so the weaker 3 * unit(...) sinks of the GQA recipe
+    would leave every tile computed).
+
+    extra: kv, dv, seq_lens (int32 [B], or None when ``lens`` is None and no pages
+    are asked for); with page_size > 0 also kv_pages [P, page_size, dk] and
+    page_table int32 [B, ceil(L/page_size)] (-1 past each sequence's last page),
+    the contiguous cache staying in ``kv`` (what the oracle reads).  k/v of the
+    returned object are views of the cache ([B,1,L,dk] and [B,1,L,dv])."""
+    g = _gen(seed, device)
+    q = torch.empty(B, Hq, 1, dk, device=device, dtype=torch.bfloat16)
+    kv = torch.empty(B, L, dk, device=device, dtype=torch.bfloat16)
+    q.copy_(_randn((B, Hq, 1, dk), g, device))
+    _fill_randn_bf16(kv, g)
+    if sinks:
+        u = _sink_direction(q, 1)  # [B, 1, dk]
+        kv[:, :sinks, :] = (math.sqrt(dk) * u).to(torch.bfloat16)
+    extra = {"kv": kv, "dv": dv, "seq_lens": None}
+    gl = torch.Generator(device="cpu")
+    gl.manual_seed(seed * 7919 + 13)
+    if lens is not None or page_size > 0:
+        if lens is None:
+            lens = torch.randint(min_len, L + 1, (B,), generator=gl)
+        lens = torch.as_tensor(lens, dtype=torch.int64).cpu()
+        extra["seq_lens"] = lens.to(torch.int32).to(device)
+    if page_size > 0:
+        npg_max = -(-L // page_size)
+        npg = (lens + page_size - 1) // page_size
+        used = int(npg.sum().item())
+        P = used + spare_pages
+        perm = torch.randperm(P, generator=gl)
+        table = torch.full((B, npg_max), -1, dtype=torch.int32)
+        valid = torch.arange(npg_max).unsqueeze(0) < npg.unsqueeze(1)
+        table[valid] = perm[:used].to(torch.int32)
+        pad = npg_max * page_size - L
+        x = kv if not pad else torch.cat([kv, torch.zeros(B, pad, dk, dtype=kv.dtype, device=device)], dim=1)
+        pool = torch.empty(P, page_size, dk, dtype=torch.bfloat16, device=device)
+        _fill_randn_bf16(pool, _gen(seed + 103, device))
+        pool[table[valid].to(torch.int64).to(device)] = x.reshape(B, npg_max, page_size, dk)[valid.to(device)]
+        extra.update(kv_pages=pool, page_table=table.to(device), page_size=page_size)
+    return Attn(q, kv.unsqueeze(1), kv[:, :, :dv].unsqueeze(1), causal=False, scale=2.0 / math.sqrt(dk),
+                name=f"mla-decode-B{B}-H{Hq}-L{L}" + (f"-ps{page_size}" if page_size else ""), extra=extra)
+
+
 def l2_flush_buffer(device, nbytes: int = 512 << 20) -> torch.Tensor:
     """A buffer larger than the 126 MB L2, written between timed iterations."""
     return torch.empty(nbytes // 4, dtype=torch.float32, device=device)

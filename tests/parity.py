@@ -194,6 +194,42 @@ def decode_paged_check(a, res, lam, S, seqs=None, log=None, window=0):
             log.append(f"{what}: {band} tiles inside the 1e-3 margin band")
 
 
+def mla_check(a, res, lam, S, seqs=None, log=None):
+    """An MLA decode (workloads.mla_decode) against the oracle run on each checked
+    sequence with its own key count, the call's lambda and split count: every tile
+    decision (outside the 1e-3 margin band), then O and lse with the GPU's decisions
+    forced.  Tiles past a sequence's end must stay "not visited"."""
+    kv = a.extra["kv"]
+    dv = a.extra["dv"]
+    Lmax = kv.shape[1]
+    sl = a.extra.get("seq_lens")
+    lens = [Lmax] * a.B if sl is None else sl.cpu().tolist()
+    gmap = res["map"].cpu().numpy()
+    o_gpu = res["o"].float().cpu().numpy()
+    lse_gpu = res["lse"].cpu().numpy()
+    assert int(res["skipped"].item()) == int((gmap == 1).sum())
+    band_total = 0
+    for b in (range(a.B) if seqs is None else seqs):
+        L = min(max(lens[b], 0), Lmax)
+        nt = -(-L // 128)
+        what = f"{a.name} seq {b} (L={L}) lam={lam:g} S={S}"
+        assert (gmap[b, nt:] == 2).all(), f"{what}: tiles past the end visited"
+        if L == 0:
+            assert (o_gpu[b] == 0).all() and np.isneginf(lse_gpu[b]).all(), what
+            continue
+        q = a.q[b:b + 1].float().cpu()
+        kvb = kv[b:b + 1].float().cpu()
+        own = orc.mla_decode_tiled(q, kvb, dv, a.scale, lam, num_splits=S, seq_lens=[L], precision="f32")
+        band = _decisions(gmap[b:b + 1], own["map"], own["margin"], lam, what)
+        ref = orc.mla_decode_tiled(q, kvb, dv, a.scale, lam, num_splits=S, seq_lens=[L], forced=gmap[b:b + 1],
+                                   precision="f32")
+        _check_rows(o_gpu[b:b + 1], lse_gpu[b:b + 1], ref["o"], ref["lse"], what)
+        band_total += band
+        if log is not None and band:
+            log.append(f"{what}: {band} tiles inside the 1e-3 margin band")
+    return band_total
+
+
 def sample_units(rng, B, H, nQ, k, always=()):
     """k random (b, h, qtile) units plus the listed ones (first/last tiles)."""
     units = set(always)

@@ -164,3 +164,40 @@ def test_prefill_window_validation(kw, code):
     rc = K.blasst_prefill_window(a["q"], FAKE, FAKE, FAKE, None, 1, 4, 2, 100, 100, 128, a["window"], 0.1, a["lam"],
                                  None, None, None, a["flags"], stream=0)
     assert rc == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=None), K.BLASST_ERR_INVALID_ARG),
+    (dict(kv=None), K.BLASST_ERR_INVALID_ARG),
+    (dict(Hq=32), K.BLASST_ERR_UNSUPPORTED),
+    (dict(Hq=3), K.BLASST_ERR_UNSUPPORTED),
+    (dict(dk=512), K.BLASST_ERR_UNSUPPORTED),
+    (dict(dv=256), K.BLASST_ERR_UNSUPPORTED),
+    (dict(S=0), K.BLASST_ERR_INVALID_ARG),
+    (dict(S=9), K.BLASST_ERR_INVALID_ARG),             # 1000 keys are 8 tiles
+    (dict(lam=2.0), K.BLASST_ERR_INVALID_ARG),
+    (dict(scale=0.0), K.BLASST_ERR_INVALID_ARG),
+    (dict(table=FAKE, mp=1), K.BLASST_ERR_INVALID_ARG),   # one 64-row page cannot hold 1000 rows
+    (dict(table=FAKE, npg=0), K.BLASST_ERR_INVALID_ARG),
+    (dict(table=FAKE, ps=24, mp=42), K.BLASST_ERR_UNSUPPORTED),
+    (dict(table=FAKE + 2), K.BLASST_ERR_UNSUPPORTED),
+    (dict(kv=FAKE + 2), K.BLASST_ERR_UNSUPPORTED),
+    (dict(S=2, ws=None), K.BLASST_ERR_INVALID_ARG),
+    (dict(S=2, wsb=16), K.BLASST_ERR_WORKSPACE_TOO_SMALL),
+])
+def test_mla_decode_validation(kw, code):
+    a = dict(q=FAKE, kv=FAKE, table=None, lens=None, B=2, Hq=16, L=1000, dk=576, dv=512, npg=40, ps=64, mp=16,
+             scale=0.1, lam=0.01, S=1, ws=FAKE, wsb=1 << 30)
+    a.update(kw)
+    rc = K.blasst_mla_decode(a["q"], a["kv"], a["table"], a["lens"], FAKE, None, a["B"], a["Hq"], a["L"], a["dk"],
+                             a["dv"], a["npg"], a["ps"], a["mp"], a["scale"], a["lam"], a["S"], a["ws"], a["wsb"],
+                             None, None, None, stream=0)
+    assert rc == code
+
+
+def test_mla_split_request_and_workspace_host_logic():
+    assert K.blasst_mla_decode_num_splits(4, 16, 1000, 8) == (K.BLASST_OK, 8)
+    assert K.blasst_mla_decode_num_splits(4, 16, 1000, 9)[0] == K.BLASST_ERR_INVALID_ARG
+    assert K.blasst_mla_decode_workspace_size(4, 16, 1000, 1) == 0
+    o_bytes = 3 * 4 * 16 * 512 * 4
+    assert K.blasst_mla_decode_workspace_size(4, 16, 1000, 3) == ((o_bytes + 255) & ~255) + 3 * 4 * 16 * 4

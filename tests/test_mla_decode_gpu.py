@@ -1,0 +1,116 @@
+"""MLA decode parity on the GPU: the CUDA kernel against the CPU oracle.
+
+The latent cache holds one 576-value row per token (keys of every head; values =
+the first 512 values).  Small problems are compared sequence by sequence in full
+(every tile decision, the exact skipped count, O and lse); the full-size problem
+(64 sequences x 32k rows, 16 heads) on sampled sequences in the launch
+configuration the benchmark times."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+from skip_softmax_flashattention_gb300 import blasst as K
+from skip_softmax_flashattention_gb300 import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    K.blasst_device_status(1)
+    yield
+    assert K.blasst_device_status(1) == K.BLASST_OK, "a kernel wait timed out or read a bad page index"
+
+
+def _run(a, lam, S, page=False):
+    ex = a.extra
+    if page:
+        return K.mla_decode(a.q, ex["kv_pages"], a.scale, lam, S, seq_lens=ex["seq_lens"],
+                            page_table=ex["page_table"], page_size=ex["page_size"], max_kv_len=ex["kv"].shape[1],
+                            want_map=True, want_margins=True)
+    return K.mla_decode(a.q, ex["kv"], a.scale, lam, S, seq_lens=ex["seq_lens"], want_map=True, want_margins=True)
+
+
+@pytest.mark.parametrize("Hq", [1, 8, 16])
+@pytest.mark.parametrize("L", [1, 127, 129, 700, 1500])
+@pytest.mark.parametrize("lam", [0.0, 0.03, 0.1])
+def test_contiguous_cache(Hq, L, lam):
+    a = W.mla_decode(seed=L + Hq, B=3, Hq=Hq, L=L, device="cuda")
+    nT = -(-L // 128)
+    for S in sorted({1, min(2, nT), min(5, nT)}):
+        res = _run(a, lam, S)
+        torch.cuda.synchronize()
+        parity.mla_check(a, res, lam, S)
+        if lam == 0.0:
+            assert int(res["skipped"].item()) == 0
+
+
+@pytest.mark.parametrize("Hq", [2, 4])
+def test_other_head_counts(Hq):
+    a = W.mla_decode(seed=3, B=2, Hq=Hq, L=1000, device="cuda")
+    for lam in (0.0, 0.05):
+        res = _run(a, lam, 3)
+        torch.cuda.synchronize()
+        parity.mla_check(a, res, lam, 3)
+
+
+def test_sequence_lengths_including_empty_and_tile_edges():
+    lens = [0, 1, 127, 128, 129, 1000, 2048, 2049]
+    a = W.mla_decode(seed=5, B=len(lens), Hq=16, L=2049, lens=lens, device="cuda")
+    for lam, S in ((0.0, 1), (0.03, 4), (0.1, 17)):
+        res = _run(a, lam, S)
+        torch.cuda.synchronize()
+        parity.mla_check(a, res, lam, S)
+
+
+@pytest.mark.parametrize("page_size", [8, 16, 64, 128, 256])
+def test_paged_cache_matches_contiguous_bitwise_and_oracle(page_size):
+    """The paged form reads the same rows through a page table: its map, O and lse
+    equal the contiguous form's bit for bit, and the oracle's."""
+    a = W.mla_decode(seed=page_size, B=6, Hq=16, L=1500, min_len=0, page_size=page_size, device="cuda")
+    for lam, S in ((0.0, 1), (0.05, 3)):
+        ref = _run(a, lam, S)
+        got = _run(a, lam, S, page=True)
+        torch.cuda.synchronize()
+        assert torch.equal(got["map"], ref["map"])
+        assert torch.equal(got["o"], ref["o"]) and torch.equal(got["lse"], ref["lse"])
+        assert int(got["skipped"].item()) == int(ref["skipped"].item())
+        parity.mla_check(a, got, lam, S)
+
+
+def test_margins_match_oracle():
+    from oracle import oracle as orc
+    import numpy as np
+
+    a = W.mla_decode(seed=9, B=2, Hq=16, L=2000, device="cuda")
+    res = _run(a, 0.0, 2)
+    torch.cuda.synchronize()
+    g = res["margins"].cpu().numpy()
+    for b in range(2):
+        own = orc.mla_decode_tiled(a.q[b:b + 1].float().cpu(), a.extra["kv"][b:b + 1].float().cpu(), 512, a.scale,
+                                   0.0, num_splits=2)
+        ref = own["margin"][0]
+        fin = np.isfinite(ref)
+        assert np.array_equal(np.isnan(g[b]), np.isnan(ref))
+        assert np.abs(g[b][fin] - ref[fin]).max() < 1e-3
+
+
+def test_full_size_sampled_sequences():
+    """64 sequences x 32768 rows x 16 heads, the split count the planner picks, at
+    lambda = 0 and at a threshold that skips part of the tiles: the first, the
+    last and two random sequences against the oracle."""
+    a = W.mla_decode(seed=0, B=64, Hq=16, L=32768, device="cuda")
+    for lam in (0.0, 0.03):
+        res = _run(a, lam, 0)
+        torch.cuda.synchronize()
+        S = res["num_splits"]
+        n = int(res["skipped"].item())
+        if lam == 0.0:
+            assert n == 0
+        else:
+            assert n > 0
+        parity.mla_check(a, res, lam, S, seqs=[0, 17, 40, 63])
+    del a, res
+    torch.cuda.empty_cache()
