@@ -479,6 +479,11 @@ def run_ours(args):
     return 0
 
 
+# MLA decode thresholds of the sweep, from none to moderate skipping (each split
+# restarts the running max, so more splits skip fewer tiles)
+MLA_LAMBDAS = (0.0, 0.01, 0.03, 0.1)
+
+
 def run_only(args):
     """One kernel on its own (`--only prefill|decode`), `--steps` launches after
     `--warmup`: the small case the ncu captures run (no timing is reported)."""
@@ -494,6 +499,11 @@ def run_only(args):
         lam = args.lam_a / a.Lkv
         for _ in range(args.warmup + args.steps):
             K.prefill(a.q, a.k, a.v, True, a.scale, lam)
+    elif args.only == "mla":
+        a = W.mla_decode(seed=0, B=args.decode_batch, device=dev)
+        lam = args.threshold if args.threshold is not None else MLA_LAMBDAS[2]
+        for _ in range(args.warmup + args.steps):
+            K.mla_decode(a.q, a.extra["kv"], a.scale, lam, args.splits)
     else:
         a = W.decode(seed=0, B=args.decode_batch, device=dev)
         lam = args.threshold if args.threshold is not None else args.lam_a / a.Lkv
@@ -642,6 +652,36 @@ def run_sweep(args):
         del a, e
         torch.cuda.empty_cache()
 
+    # MLA decode (absorbed form): 64 sequences x 32768 latent rows of 576 values, 16
+    # query heads; the cache is read once per row (values = the rows' first 512
+    # columns), so the algorithmic bytes are the cache's.  Contiguous, and paged with
+    # 64-row pages and 16k-32k rows per sequence.
+    for ps, Hq in ((0, 16), (0, 8), (64, 16)):
+        lens = None if ps == 0 else torch.randint(16384, 32769, (64,), generator=torch.Generator().manual_seed(3))
+        a = W.mla_decode(seed=0, B=64, Hq=Hq, L=32768, lens=lens, page_size=ps, device=dev)
+        e = a.extra
+        rows = 64 * 32768 if ps == 0 else int(lens.sum().item())
+        tiles = int(((e["seq_lens"].to(torch.int64) + 127) // 128).sum().item()) if ps else 64 * 256
+        call = (lambda lam, S: K.mla_decode(a.q, e["kv"], a.scale, lam, S)) if ps == 0 else \
+            (lambda lam, S: K.mla_decode(a.q, e["kv_pages"], a.scale, lam, S, seq_lens=e["seq_lens"],
+                                         page_table=e["page_table"], page_size=ps, max_kv_len=32768))
+        base = None
+        for lam in MLA_LAMBDAS if ps == 0 and Hq == 16 else (0.0, MLA_LAMBDAS[2]):
+            r = call(lam, 0)
+            torch.cuda.synchronize()
+            sk = int(r["skipped"].item())
+            Sx = r["num_splits"]
+            ms = _time_ms(lambda: call(lam, Sx), flush)
+            base = ms if lam == 0 else base
+            kv = rows * 576 * 2
+            emit({"sweep": f"mla-decode-B64-H{Hq}-L32768" + (f"-ps{ps}-16k-32k" if ps else ""), "kind": "mla-decode",
+                  "splits": Sx, "lambda": lam, "ms": ms, "skip_pct": 100.0 * sk / tiles,
+                  "kv_gbs": kv / (ms * 1e-3) / 1e9, "frac_of_measured_hbm": kv / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                  "executed_tflops": 2.0 * 128 * Hq * (576 * tiles + 512 * (tiles - sk)) / (ms * 1e-3) / 1e12,
+                  "speedup_vs_lambda0": base / ms})
+        del a, e
+        torch.cuda.empty_cache()
+
     # long-context sweep: calibrate on seed 1, evaluate targets on seed 2
     cands = [float(x) for x in np.logspace(-6, 0, 25)]
     margins = {}
@@ -689,7 +729,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-units", type=int, default=16)
-    ap.add_argument("--only", choices=["prefill", "decode"], default=None,
+    ap.add_argument("--only", choices=["prefill", "decode", "mla"], default=None,
                     help="launch one kernel only (profiling case); no JSON metric line")
     ap.add_argument("--prefill-len", type=int, default=16384)
     ap.add_argument("--decode-batch", type=int, default=64)

@@ -21,12 +21,19 @@
 // read a second time after its decision, in 128-column pairs of boxes: the key
 // stream never waits for a decision, the second read finds the rows in L2 (they
 // were read a few microseconds earlier), and a skipped tile's values are never
-// read again.  Each P.V result lands in a fresh TMEM slot and is folded into
+// read again.  (Keeping a tile's value columns in shared memory until its decision
+// instead leaves room to prefetch only one more pair, and every tile then waits a
+// full memory latency: measured 13 % slower on GB300.)  Shared memory: 64 KB of key
+// boxes, 128 KB of value pairs (one kept tile's four in flight at once), 18 KB of Q,
+// 8 KB of P; more value slots at the cost of key slots measured faster up to this
+// split.  Each P.V result lands in a fresh TMEM slot and is folded into
 // per-thread registers a few tiles later (thread t owns value columns t, t+128,
 // t+256, t+384 of every head).
 //
-// Warp roles (224 threads): warps 0-3 softmax, warp 4 key loader, warp 5 MMA
-// issuer and TMEM owner, warp 6 value loader.
+// Warp roles (256 threads): warps 0-3 softmax, warp 4 key loader, warp 5 issuer of
+// the S MMAs and TMEM owner, warp 6 value loader, warp 7 issuer of the P.V MMAs.
+// The two MMA streams have their own issuing threads, so a P.V pass waiting for a
+// decision or a value pair never holds up the S MMAs that drain the key ring.
 //
 // Paged form: the cache is a pool of pages of page_size rows and a page table maps
 // each page-sized run of a sequence's keys to a page (The Hitchhiker's Guide, Phase
@@ -53,13 +60,12 @@ constexpr int VBLK = DV / 128;           // 128-column value blocks (box pairs) 
 constexpr int NPAD = 16;                 // MMA N: the heads padded to 16
 constexpr int BOX_BYTES = kTile * 128;   // 128 keys x 64 columns
 constexpr int PAIR_BYTES = 2 * BOX_BYTES;
-constexpr int NKB = 6;                   // key box ring
-constexpr int NVP = 2;                   // value pair ring
+constexpr int NKB = 4;                   // key box ring
+constexpr int NVP = 4;                   // value pair ring (a kept tile's four pairs in flight at once)
 constexpr int NS = 4, NO = 4;            // TMEM S slots (16 columns) / O slots (64 columns)
-constexpr int NP = 4;                    // P staging buffers
+constexpr int NP = 2;                    // P staging buffers
 constexpr int ND = 8;                    // decision ring
 constexpr int NH = 8;                    // reference-max history ring
-constexpr int LOOKAHEAD = 3;             // S passes issued ahead of the P.V pass
 constexpr int LAG = 2;                   // P.V results folded this many computed tiles late
 constexpr int Q_BYTES = KBOX * NPAD * 128;
 constexpr int P_BYTES = 2 * NPAD * 128;  // [key half][16 rows][64 keys]
@@ -72,14 +78,14 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t O_COL = NS * NPAD;
 constexpr int O_SLOT = VBLK * NPAD;      // block i of a slot: columns [16i, 16i + 16)
 static_assert(O_COL + NO * O_SLOT <= TMEM_COLS, "TMEM budget");
-static_assert(LAG <= NO && LOOKAHEAD + 1 <= NS && LOOKAHEAD + 2 <= ND, "ring sizes");
+static_assert(LAG <= NO && NS + 2 <= ND, "ring sizes");
 static_assert(DK % 64 == 0 && DV % 128 == 0 && DV <= DK, "row layout");
 
 struct MlaCtrl {
     uint64_t k_full[NKB], k_empty[NKB], v_full[NVP], v_empty[NVP];
     uint64_t s_full[NS], s_free[NS], dec_full[ND], dec_free[ND];
     uint64_t p_full[NP], p_free[NP], o_full[NO], o_free[NO];
-    uint64_t q_full, drain;
+    uint64_t q_full, drain[2];
     uint32_t tmem_base;
     int dec[ND];
     int abort;
@@ -95,7 +101,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 template <int G, bool PAGED>
-__global__ void __launch_bounds__(224, 1)
+__global__ void __launch_bounds__(256, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const DecodeParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
@@ -120,12 +126,13 @@ __global__ void __launch_bounds__(224, 1)
         for (int i = 0; i < NS; ++i) { mbar_init(&ctrl->s_full[i], 1); mbar_init(&ctrl->s_free[i], 4); }
         for (int i = 0; i < ND; ++i) {
             mbar_init(&ctrl->dec_full[i], 1);
-            mbar_init(&ctrl->dec_free[i], 2);  // released by the MMA issuer and the value loader
+            mbar_init(&ctrl->dec_free[i], 2);  // released by the P.V issuer and the value loader
         }
         for (int i = 0; i < NP; ++i) { mbar_init(&ctrl->p_full[i], 4); mbar_init(&ctrl->p_free[i], 1); }
         for (int i = 0; i < NO; ++i) { mbar_init(&ctrl->o_full[i], 1); mbar_init(&ctrl->o_free[i], 4); }
         mbar_init(&ctrl->q_full, 4);
-        mbar_init(&ctrl->drain, 1);
+        mbar_init(&ctrl->drain[0], 1);
+        mbar_init(&ctrl->drain[1], 1);
         ctrl->abort = 0;
         fence_mbar_init();
     }
@@ -253,20 +260,19 @@ __global__ void __launch_bounds__(224, 1)
             for (int e = max(0, issued - NVP); e < issued; ++e)
                 mbar_wait_drain(&ctrl->v_full[e % NVP], (e / NVP) & 1, kDrainNs);
     } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ S issuer
+        // S^T_j, box by box as the key boxes land; each box's slot is released by a
+        // commit after its four MMAs.  S slot j % NS is reused once the softmax read it.
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(128, NPAD, false, false);
-            constexpr uint32_t kIdescO = idesc_bf16(128, NPAD, true, false);
-            const uint32_t sK = smem_u32(smem + OFF_K), sV = smem_u32(smem + OFF_V);
-            const uint32_t sQ = smem_u32(smem + OFF_Q), sP = smem_u32(smem + OFF_P);
-            // S^T_j, box by box as the key boxes land; each box's slot is released by a
-            // commit after its four MMAs
-            auto issue_s = [&](int j) -> bool {
+            const uint32_t sK = smem_u32(smem + OFF_K), sQ = smem_u32(smem + OFF_Q);
+            bool ok = mbar_wait(&ctrl->q_full, 0, wd);
+            for (int j = 0; j < n && ok; ++j) {
                 const int ss = j % NS;
-                if (j >= NS && !mbar_wait(&ctrl->s_free[ss], ((j / NS) - 1) & 1, wd)) return false;
+                if (j >= NS && !(ok = mbar_wait(&ctrl->s_free[ss], ((j / NS) - 1) & 1, wd))) break;
                 for (int c = 0; c < KBOX; ++c) {
                     const int e = j * KBOX + c, ks = e % NKB;
-                    if (!mbar_wait(&ctrl->k_full[ks], (e / NKB) & 1, wd)) return false;
+                    if (!(ok = mbar_wait(&ctrl->k_full[ks], (e / NKB) & 1, wd))) break;
                     tc_fence_after();
                     const uint32_t kb = sK + ks * BOX_BYTES, qb = sQ + c * (NPAD * 128);
 #pragma unroll
@@ -275,14 +281,20 @@ __global__ void __launch_bounds__(224, 1)
                                kIdescS, (c > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(&ctrl->k_empty[ks]);
                 }
+                if (!ok) break;
                 mma_commit(&ctrl->s_full[ss]);
-                return true;
-            };
-            bool ok = mbar_wait(&ctrl->q_full, 0, wd);
-            for (int j = 0; j < min(LOOKAHEAD, n) && ok; ++j) ok = issue_s(j);
+            }
+            mma_commit(&ctrl->drain[0]);
+            mbar_wait_drain(&ctrl->drain[0], 0, kDrainNs);
+        }
+    } else if (warp == 7) {
+        // ------------------------------------------------------------ P.V issuer
+        if (lane == 0) {
+            constexpr uint32_t kIdescO = idesc_bf16(128, NPAD, true, false);
+            const uint32_t sV = smem_u32(smem + OFF_V), sP = smem_u32(smem + OFF_P);
+            bool ok = true;
             int comp = 0;
             for (int j = 0; j < n && ok; ++j) {
-                if (j + LOOKAHEAD < n && !(ok = issue_s(j + LOOKAHEAD))) break;
                 if (!(ok = mbar_wait(&ctrl->dec_full[j % ND], (j / ND) & 1, wd))) break;
                 const bool skipped = reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] != 0;
                 mbar_arrive(&ctrl->dec_free[j % ND]);
@@ -309,8 +321,8 @@ __global__ void __launch_bounds__(224, 1)
                 mma_commit(&ctrl->p_free[pb]);
                 ++comp;
             }
-            mma_commit(&ctrl->drain);
-            mbar_wait_drain(&ctrl->drain, 0, kDrainNs);
+            mma_commit(&ctrl->drain[1]);
+            mbar_wait_drain(&ctrl->drain[1], 0, kDrainNs);
         }
     } else {
         // ------------------------------------------------------------ softmax (warps 0-3)
@@ -497,7 +509,7 @@ cudaError_t launch_gp(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_
     cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid(p.S, 1, p.B);
-    mla_decode_kernel<G, PAGED><<<grid, 224, SMEM, stream>>>(tkv, p);
+    mla_decode_kernel<G, PAGED><<<grid, 256, SMEM, stream>>>(tkv, p);
     return cudaGetLastError();
 }
 template <int G>
