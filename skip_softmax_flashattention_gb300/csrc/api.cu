@@ -421,7 +421,8 @@ int blasst_mla_decode_num_splits(int B, int Hq, int max_kv_len, int requested, i
         *out = requested;
         return BLASST_OK;
     }
-    return plan_splits((long long)B, nT, out);  // one CTA per (sequence, split)
+    // one CTA per (sequence, split), a cluster of Hq / 16 of them above 16 heads
+    return plan_splits((long long)B * (Hq > 16 ? Hq / 16 : 1), nT, out);
 }
 
 size_t blasst_mla_decode_workspace_size(int B, int Hq, int max_kv_len, int num_splits) {
@@ -443,7 +444,8 @@ int blasst_mla_decode(const void* q, const void* kv, const int* page_table, cons
     const int nT = (max_kv_len + kTile - 1) / kTile;
     if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
     if (dk != blasst::kMlaDk || dv != blasst::kMlaDv) return BLASST_ERR_UNSUPPORTED;
-    if (Hq != 1 && Hq != 2 && Hq != 4 && Hq != 8 && Hq != 16) return BLASST_ERR_UNSUPPORTED;
+    if (Hq != 1 && Hq != 2 && Hq != 4 && Hq != 8 && Hq != 16 && Hq != 32 && Hq != 64 && Hq != 128)
+        return BLASST_ERR_UNSUPPORTED;
     if (page_table && !page_size_ok(page_size)) return BLASST_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(kv) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||

@@ -35,6 +35,18 @@
 // The two MMA streams have their own issuing threads, so a P.V pass waiting for a
 // decision or a value pair never holds up the S MMAs that drain the key ring.
 //
+// More than 16 heads: a cluster of CG = Hq / 16 CTAs runs each (sequence, split),
+// CTA r holding heads [16r, 16r + 16).  The CTAs of a cluster read the same rows,
+// so each key box and value pair is loaded once and multicast to all of them (the
+// entries of ring slot k are issued by CTA k mod CG); a slot is refilled once every
+// CTA's MMAs have released it (each MMA commit arrives on the slot's barrier in
+// every CTA), and only onto barriers every CTA has armed: key slots are armed by
+// each CTA's S issuer one ring ahead, value slots by each CTA's value loader, which
+// tells the issuing CTA.  So every copy into a CTA is one it waits for before it
+// exits, also when a wait gives up.  The tile's decision covers all Hq heads: every CTA sends its vote
+// and margin to every other through distributed shared memory, and each takes the
+// AND of the CG votes.
+//
 // Paged form: the cache is a pool of pages of page_size rows and a page table maps
 // each page-sized run of a sequence's keys to a page (The Hitchhiker's Guide, Phase
 // 08, Section 3, "Paged Attention").  A 128-key box is then fetched as 128 /
@@ -92,6 +104,12 @@ struct MlaCtrl {
     float red[2][4][NPAD];
     float mref_hist[NH][NPAD];
     float lred[4][NPAD];
+    // clusters: per decision slot, the vote of every CTA (low word: 1 = all its heads
+    // skip; high word: its margin) and the barrier their arrivals complete
+    uint64_t votes[ND][8];
+    uint64_t vote_full[ND];
+    uint64_t v_armed[NVP];  // every CTA armed the slot's next entry (in the slot's issuing CTA)
+    int cl_skip;  // the cluster's decision on the current tile, for the softmax threads
 };
 constexpr int SMEM = OFF_CTRL + (int)sizeof(MlaCtrl) + 1024;
 static_assert(SMEM <= 232448, "shared memory per CTA");
@@ -100,14 +118,18 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int G, bool PAGED>
+template <int G, bool PAGED, int CG>
 __global__ void __launch_bounds__(256, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const DecodeParams p) {
+    static_assert(CG == 1 || G == NPAD, "a cluster's CTAs hold 16 heads each");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     MlaCtrl* ctrl = reinterpret_cast<MlaCtrl*>(smem + OFF_CTRL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int s = blockIdx.x, b = blockIdx.z;
+    const int s = blockIdx.x / CG, b = blockIdx.z;
+    const uint32_t rank = CG > 1 ? cluster_ctarank() : 0u;
+    const int h0 = (int)rank * NPAD;  // this CTA's first head (CG > 1)
+    constexpr uint16_t kAll = (uint16_t)((1u << CG) - 1u);
     // This sequence's keys and this split's share of its tiles: [s*nT/S, (s+1)*nT/S).
     int Lb = p.Lkv;
     if (p.seq_lens) {
@@ -121,8 +143,13 @@ __global__ void __launch_bounds__(256, 1)
     const int n = t1 - t0;
 
     if (tid == 0) {
-        for (int i = 0; i < NKB; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], 1); }
-        for (int i = 0; i < NVP; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
+        // a slot's release comes from the MMAs of every CTA of the cluster
+        for (int i = 0; i < NKB; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], CG); }
+        for (int i = 0; i < NVP; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], CG); }
+        for (int i = 0; i < ND; ++i) mbar_init(&ctrl->vote_full[i], CG);
+        for (int i = 0; i < NVP; ++i) mbar_init(&ctrl->v_armed[i], CG);
+        // the first NKB key entries are armed before any CTA of the cluster can copy
+        for (int i = 0; i < min(NKB, n * KBOX); ++i) mbar_arrive_expect_tx(&ctrl->k_full[i], BOX_BYTES);
         for (int i = 0; i < NS; ++i) { mbar_init(&ctrl->s_full[i], 1); mbar_init(&ctrl->s_free[i], 4); }
         for (int i = 0; i < ND; ++i) {
             mbar_init(&ctrl->dec_full[i], 1);
@@ -142,10 +169,29 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncwarp();  // the set-up above diverged inside warps; bar.sync is warp-aligned
     tc_fence_before();
-    __syncthreads();
+    if constexpr (CG > 1)
+        cluster_sync_all();  // every CTA's barriers exist before any remote arrival or copy
+    else
+        __syncthreads();
     tc_fence_after();
     const uint32_t tmem = ctrl->tmem_base;
     const Watchdog wd{&ctrl->abort, p.status, p.watchdog_ns};
+    // does this CTA issue the copies of ring slot k (with CG = 1: always)
+    auto issues = [&](int k) -> bool { return CG == 1 || (k % CG) == (int)rank; };
+    // a loaded box: this CTA alone, or multicast to the cluster
+    auto load_box = [&](uint8_t* dst, uint64_t* bar, int x, int y) {
+        if constexpr (CG == 1)
+            tma_load_3d(dst, &tkv, bar, x, y, b);
+        else
+            tma_load_3d_mc(dst, &tkv, bar, x, y, b, kAll);
+    };
+    // a slot's release: a commit arriving in this CTA, or in every CTA of the cluster
+    auto release = [&](uint64_t* bar) {
+        if constexpr (CG == 1)
+            mma_commit(bar);
+        else
+            mma_commit_mc(bar, kAll);
+    };
 
     // Paged form: sub-box i of a 64-column box covers keys [i*rows, (i+1)*rows) of
     // the tile, one page run; lane i of a loader warp reads its page index once
@@ -165,52 +211,45 @@ __global__ void __launch_bounds__(256, 1)
     };
     auto issue_sub_box = [&](uint8_t* dst, uint64_t* bar, int x, int tile, int i, int pg) {
         const int off = (tile * kTile + i * p.rows_per_box) % p.page_size;
-        tma_load_4d(dst + i * p.rows_per_box * 128, &tkv, bar, x, 0, off, pg);
+        if constexpr (CG == 1)
+            tma_load_4d(dst + i * p.rows_per_box * 128, &tkv, bar, x, 0, off, pg);
+        else
+            tma_load_4d_mc(dst + i * p.rows_per_box * 128, &tkv, bar, x, 0, off, pg, kAll);
     };
 
     if (warp == 4) {
         // ------------------------------------------------------------ key loader
-        // box c of tile j is ring entry j*KBOX + c
-        if constexpr (!PAGED) {
-            if (lane == 0) {
-                tma_prefetch_desc(&tkv);
-                int issued = 0;
-                bool ok = true;
-                for (int j = 0; j < n && ok; ++j) {
-                    for (int c = 0; c < KBOX; ++c) {
-                        const int e = j * KBOX + c, ks = e % NKB;
-                        if (e >= NKB && !(ok = mbar_wait(&ctrl->k_empty[ks], ((e / NKB) - 1) & 1, wd))) break;
-                        mbar_arrive_expect_tx(&ctrl->k_full[ks], BOX_BYTES);
-                        tma_load_3d(smem + OFF_K + ks * BOX_BYTES, &tkv, &ctrl->k_full[ks], c * 64, (t0 + j) * kTile, b);
-                        issued = e + 1;
-                    }
-                }
-                for (int e = max(0, issued - NKB); e < issued; ++e)
-                    mbar_wait_drain(&ctrl->k_full[e % NKB], (e / NKB) & 1, kDrainNs);
-            }
-        } else {
-            if (lane == 0) tma_prefetch_desc(&tkv);
-            int issued = 0;
-            bool ok = true;
-            for (int j = 0; j < n && ok; ++j) {
-                const int pg = box_page(t0 + j, lane);
-                for (int c = 0; c < KBOX; ++c) {
-                    const int e = j * KBOX + c, ks = e % NKB;
+        // Box c of tile j is ring entry e = j*KBOX + c, in slot e % NKB.  Its copy goes
+        // out once every CTA released the slot's previous entry; the entry's barrier was
+        // armed by the S issuer (by the set-up for the first NKB).
+        if (lane == 0) tma_prefetch_desc(&tkv);
+        int last = 0;  // entries passed
+        bool ok = true;
+        for (int j = 0; j < n && ok; ++j) {
+            const int pg = PAGED ? box_page(t0 + j, lane) : 0;
+            for (int c = 0; c < KBOX; ++c) {
+                const int e = j * KBOX + c, ks = e % NKB;
+                if (issues(ks)) {
                     int go = 1;
                     if (lane == 0) {
-                        if (e >= NKB && !mbar_wait(&ctrl->k_empty[ks], ((e / NKB) - 1) & 1, wd))
+                        if (e >= NKB && !mbar_wait_cluster(&ctrl->k_empty[ks], ((e / NKB) - 1) & 1, wd))
                             go = 0;
-                        else
-                            mbar_arrive_expect_tx(&ctrl->k_full[ks], BOX_BYTES);
+                        else if constexpr (!PAGED)
+                            load_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, (t0 + j) * kTile);
                     }
                     if (!(ok = __shfl_sync(0xffffffffu, go, 0) != 0)) break;
-                    if (lane < nbox) issue_sub_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, t0 + j, lane, pg);
-                    issued = e + 1;
+                    if constexpr (PAGED) {
+                        if (lane < nbox)
+                            issue_sub_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, t0 + j, lane, pg);
+                    }
                 }
+                last = e + 1;
             }
+        }
+        if constexpr (CG > 1) {  // the other CTAs' releases of the last entries arrive here
             if (lane == 0)
-                for (int e = max(0, issued - NKB); e < issued; ++e)
-                    mbar_wait_drain(&ctrl->k_full[e % NKB], (e / NKB) & 1, kDrainNs);
+                for (int e = max(0, last - NKB); e < last; ++e)
+                    mbar_wait_drain(&ctrl->k_empty[e % NKB], (e / NKB) & 1, kDrainNs);
         }
     } else if (warp == 6) {
         // ------------------------------------------------------------ value loader
@@ -232,21 +271,28 @@ __global__ void __launch_bounds__(256, 1)
                 const int e = issued, vs = e % NVP;
                 int gv = 1;
                 if (lane == 0) {
-                    if (e >= NVP && !mbar_wait(&ctrl->v_empty[vs], ((e / NVP) - 1) & 1, wd)) {
+                    if (e >= NVP && !mbar_wait_cluster(&ctrl->v_empty[vs], ((e / NVP) - 1) & 1, wd)) {
                         gv = 0;
                     } else {
                         mbar_arrive_expect_tx(&ctrl->v_full[vs], PAIR_BYTES);
+                        if constexpr (CG > 1) {
+                            mbar_arrive_cluster(cluster_addr(&ctrl->v_armed[vs], (uint32_t)(vs % CG)));
+                            // the issuing CTA copies once every CTA armed the entry
+                            if (issues(vs) && !mbar_wait_cluster(&ctrl->v_armed[vs], (e / NVP) & 1, wd)) gv = 0;
+                        }
                         if constexpr (!PAGED) {
+                            if (gv && issues(vs)) {
 #pragma unroll
-                            for (int h = 0; h < 2; ++h)
-                                tma_load_3d(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &tkv, &ctrl->v_full[vs],
-                                            i * 128 + h * 64, (t0 + j) * kTile, b);
+                                for (int h = 0; h < 2; ++h)
+                                    load_box(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
+                                             i * 128 + h * 64, (t0 + j) * kTile);
+                            }
                         }
                     }
                 }
                 if (!(ok = __shfl_sync(0xffffffffu, gv, 0) != 0)) break;
                 if constexpr (PAGED) {
-                    if (lane < nbox) {
+                    if (lane < nbox && issues(vs)) {
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
                             issue_sub_box(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
@@ -256,9 +302,13 @@ __global__ void __launch_bounds__(256, 1)
                 issued = e + 1;
             }
         }
-        if (lane == 0)
+        if (lane == 0) {
             for (int e = max(0, issued - NVP); e < issued; ++e)
                 mbar_wait_drain(&ctrl->v_full[e % NVP], (e / NVP) & 1, kDrainNs);
+            if constexpr (CG > 1)
+                for (int e = max(0, issued - NVP); e < issued; ++e)
+                    mbar_wait_drain(&ctrl->v_empty[e % NVP], (e / NVP) & 1, kDrainNs);
+        }
     } else if (warp == 5) {
         // ------------------------------------------------------------ S issuer
         // S^T_j, box by box as the key boxes land; each box's slot is released by a
@@ -266,6 +316,8 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) {
             constexpr uint32_t kIdescS = idesc_bf16(128, NPAD, false, false);
             const uint32_t sK = smem_u32(smem + OFF_K), sQ = smem_u32(smem + OFF_Q);
+            const int total = n * KBOX;
+            int armed = min(NKB, total), consumed = 0;
             bool ok = mbar_wait(&ctrl->q_full, 0, wd);
             for (int j = 0; j < n && ok; ++j) {
                 const int ss = j % NS;
@@ -273,19 +325,26 @@ __global__ void __launch_bounds__(256, 1)
                 for (int c = 0; c < KBOX; ++c) {
                     const int e = j * KBOX + c, ks = e % NKB;
                     if (!(ok = mbar_wait(&ctrl->k_full[ks], (e / NKB) & 1, wd))) break;
+                    consumed = e + 1;
+                    if (e + NKB < total) {  // arm the slot's next entry before releasing this one
+                        mbar_arrive_expect_tx(&ctrl->k_full[ks], BOX_BYTES);
+                        armed = e + NKB + 1;
+                    }
                     tc_fence_after();
                     const uint32_t kb = sK + ks * BOX_BYTES, qb = sQ + c * (NPAD * 128);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_ss(tmem + ss * NPAD, desc_kmajor_sw128(kb + kk * 32), desc_kmajor_sw128(qb + kk * 32),
                                kIdescS, (c > 0 || kk > 0) ? 1u : 0u);
-                    mma_commit(&ctrl->k_empty[ks]);
+                    release(&ctrl->k_empty[ks]);
                 }
                 if (!ok) break;
                 mma_commit(&ctrl->s_full[ss]);
             }
             mma_commit(&ctrl->drain[0]);
             mbar_wait_drain(&ctrl->drain[0], 0, kDrainNs);
+            // copies onto entries armed but not consumed (only after a wait gave up)
+            for (int e = consumed; e < armed; ++e) mbar_wait_drain(&ctrl->k_full[e % NKB], (e / NKB) & 1, kDrainNs);
         }
     } else if (warp == 7) {
         // ------------------------------------------------------------ P.V issuer
@@ -314,7 +373,7 @@ __global__ void __launch_bounds__(256, 1)
                         const uint64_t bdesc = desc_kmajor_sw128(pbuf + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32);
                         mma_ss(tmem + O_COL + os * O_SLOT + i * NPAD, adesc, bdesc, kIdescO, kk > 0 ? 1u : 0u);
                     }
-                    mma_commit(&ctrl->v_empty[vs]);
+                    release(&ctrl->v_empty[vs]);
                 }
                 if (!ok) break;
                 mma_commit(&ctrl->o_full[os]);
@@ -333,7 +392,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int c = tid; c < NPAD * (DK / 8); c += 128) {
                 const int g = c / (DK / 8), ck = c % (DK / 8);
                 uint4 v = make_uint4(0, 0, 0, 0);
-                if (g < G) v = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + g) * DK + ck * 8);
+                if (g < G) v = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + h0 + g) * DK + ck * 8);
                 const int box = ck >> 3, cw = ck & 7;
                 *reinterpret_cast<uint4*>(sq + box * (NPAD * 128) + g * 128 + ((cw ^ (g & 7)) << 4)) = v;
             }
@@ -417,14 +476,40 @@ __global__ void __launch_bounds__(256, 1)
                 margin = fmaxf(margin, gm);
                 m_exact[g] = mnew[g];
             }
+            if constexpr (CG > 1) {
+                // The decision covers the heads of every CTA of the cluster: send this
+                // CTA's vote and margin to all of them, wait for theirs, take the AND and
+                // the max.  A CTA runs less than a tile ahead of the slowest one in its S
+                // MMAs (a key slot is refilled only after every CTA released it), so a
+                // vote slot is never overwritten before it was read.
+                if (tid == 0) {
+                    const int slot = j % ND;
+                    const uint64_t word = ((uint64_t)__float_as_uint(margin) << 32) | (skip ? 1u : 0u);
+                    for (int r = 0; r < CG; ++r) st_cluster_u64(cluster_addr(&ctrl->votes[slot][rank], r), word);
+                    for (int r = 0; r < CG; ++r) mbar_arrive_cluster(cluster_addr(&ctrl->vote_full[slot], r));
+                    bool all = mbar_wait_cluster(&ctrl->vote_full[slot], (j / ND) & 1, wd);
+                    float mg = -CUDART_INF_F;
+                    for (int r = 0; r < CG; ++r) {
+                        const uint64_t w = reinterpret_cast<volatile uint64_t*>(ctrl->votes[slot])[r];
+                        all = all && (w & 1u) != 0;
+                        mg = fmaxf(mg, __uint_as_float((uint32_t)(w >> 32)));
+                    }
+                    margin = mg;
+                    reinterpret_cast<volatile int*>(&ctrl->cl_skip)[0] = all ? 1 : 0;
+                }
+                named_bar_sync(1, 128);
+                skip = reinterpret_cast<volatile int*>(&ctrl->cl_skip)[0] != 0;
+            }
             if (tid == 0) {
                 // the slot is reused only after both readers of tile j - ND released it
                 if (j >= ND) mbar_wait(&ctrl->dec_free[j % ND], ((j / ND) - 1) & 1, wd);
                 reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] = skip ? 1 : 0;
                 mbar_arrive(&ctrl->dec_full[j % ND]);
-                if (p.skip_map) p.skip_map[mapbase + t0 + j] = skip ? 1 : 0;
-                if (p.margins) p.margins[mapbase + t0 + j] = margin * p.scale;
-                nskip += skip ? 1 : 0;
+                if (rank == 0) {  // one record per tile for the whole cluster
+                    if (p.skip_map) p.skip_map[mapbase + t0 + j] = skip ? 1 : 0;
+                    if (p.margins) p.margins[mapbase + t0 + j] = margin * p.scale;
+                    nskip += skip ? 1 : 0;
+                }
             }
             if (!skip) {
 #pragma unroll
@@ -478,7 +563,7 @@ __global__ void __launch_bounds__(256, 1)
             const float l = lr[0] + lr[NPAD] + lr[2 * NPAD] + lr[3 * NPAD];
             const float inv = l > 0.f ? 1.f / l : 0.f;
             const float lse = l > 0.f ? m_ref[g] * p.scale + __logf(l) : -CUDART_INF_F;
-            const long long hq = (long long)b * p.Hq + g;
+            const long long hq = (long long)b * p.Hq + h0 + g;
             if (p.S == 1) {
 #pragma unroll
                 for (int i = 0; i < VBLK; ++i)
@@ -502,30 +587,52 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+    if constexpr (CG > 1) cluster_sync_all();  // no CTA leaves while another may still reach it
 }
 
-template <int G, bool PAGED>
+template <int G, bool PAGED, int CG>
 cudaError_t launch_gp(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<G, PAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    auto kern = mla_decode_kernel<G, PAGED, CG>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.S, 1, p.B);
-    mla_decode_kernel<G, PAGED><<<grid, 256, SMEM, stream>>>(tkv, p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.S * CG), 1, (unsigned)p.B);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.dynamicSmemBytes = SMEM;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CG;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = CG > 1 ? 1 : 0;
+    if constexpr (CG > 1) {  // a cluster of CG CTAs of this size must fit on the GPU
+        int nclusters = 0;
+        e = cudaOccupancyMaxActiveClusters(&nclusters, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (nclusters < 1) return cudaErrorInvalidConfiguration;
+    }
+    return cudaLaunchKernelEx(&cfg, kern, tkv, p);
 }
-template <int G>
+template <int G, int CG>
 cudaError_t launch_g(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
-    return p.page_table ? launch_gp<G, true>(tkv, p, stream) : launch_gp<G, false>(tkv, p, stream);
+    return p.page_table ? launch_gp<G, true, CG>(tkv, p, stream) : launch_gp<G, false, CG>(tkv, p, stream);
 }
 
 }  // namespace
 
+// Hq <= 16: one CTA per (sequence, split); 32, 64, 128: clusters of Hq / 16 CTAs.
 cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
     switch (p.Hq) {
-        case 1: return launch_g<1>(tkv, p, stream);
-        case 2: return launch_g<2>(tkv, p, stream);
-        case 4: return launch_g<4>(tkv, p, stream);
-        case 8: return launch_g<8>(tkv, p, stream);
-        case 16: return launch_g<16>(tkv, p, stream);
+        case 1: return launch_g<1, 1>(tkv, p, stream);
+        case 2: return launch_g<2, 1>(tkv, p, stream);
+        case 4: return launch_g<4, 1>(tkv, p, stream);
+        case 8: return launch_g<8, 1>(tkv, p, stream);
+        case 16: return launch_g<16, 1>(tkv, p, stream);
+        case 32: return launch_g<16, 2>(tkv, p, stream);
+        case 64: return launch_g<16, 4>(tkv, p, stream);
+        case 128: return launch_g<16, 8>(tkv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

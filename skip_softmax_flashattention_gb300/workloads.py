@@ -273,14 +273,17 @@ def paged_decode(seed: int = 0, B: int = 8, Hq: int = 32, Hkv: int = 8, max_len:
 
 def mla_decode(seed: int = 0, B: int = 64, Hq: int = 16, L: int = 32768, dk: int = 576, dv: int = 512,
                device="cpu", sinks: int = 4, lens=None, min_len: int = 1, page_size: int = 0,
-               spare_pages: int = 7) -> Attn:
+               spare_pages: int = 7, q_shared: float = 0.0, sink_norm: float = 0.0) -> Attn:
     """MLA decode in absorbed form: q [B,Hq,1,dk]; one latent cache kv [B,L,dk]
     whose rows are the keys of every head and whose first dv columns are the
     values.  The decode recipe applied to the latent rows: q and kv N(0,1), scores
     scaled by 2/sqrt(dk), and the first ``sinks`` rows of each sequence sink keys
     along unit(mean of its queries), here with an ordinary row's norm sqrt(dk) (one
     decision covers all Hq heads, so the weaker 3 * unit(...) sinks of the GQA recipe
-    would leave every tile computed).
+    would leave every tile computed).  With q_shared > 0 every query also gets
+    q_shared * u for one random unit vector u per sequence and the sinks point along
+    u with norm sink_norm (default sqrt(dk)): many heads then share strong sinks, as
+    the 64- and 128-head cases need for any tile to be skipped by all heads.
 
     extra: kv, dv, seq_lens (int32 [B], or None when ``lens`` is None and no pages
     are asked for); with page_size > 0 also kv_pages [P, page_size, dk] and
@@ -292,9 +295,15 @@ def mla_decode(seed: int = 0, B: int = 64, Hq: int = 16, L: int = 32768, dk: int
     kv = torch.empty(B, L, dk, device=device, dtype=torch.bfloat16)
     q.copy_(_randn((B, Hq, 1, dk), g, device))
     _fill_randn_bf16(kv, g)
+    norm = sink_norm if sink_norm > 0 else math.sqrt(dk)
+    if q_shared > 0:
+        u = _randn((B, 1, dk), g, device)
+        u = u / u.norm(dim=-1, keepdim=True)
+        q.copy_((q.float() + q_shared * u.unsqueeze(2)).to(torch.bfloat16))
     if sinks:
-        u = _sink_direction(q, 1)  # [B, 1, dk]
-        kv[:, :sinks, :] = (math.sqrt(dk) * u).to(torch.bfloat16)
+        if q_shared <= 0:
+            u = _sink_direction(q, 1)  # [B, 1, dk]
+        kv[:, :sinks, :] = (norm * u).to(torch.bfloat16)
     extra = {"kv": kv, "dv": dv, "seq_lens": None}
     gl = torch.Generator(device="cpu")
     gl.manual_seed(seed * 7919 + 13)

@@ -169,7 +169,8 @@ def test_prefill_window_validation(kw, code):
 @pytest.mark.parametrize("kw,code", [
     (dict(q=None), K.BLASST_ERR_INVALID_ARG),
     (dict(kv=None), K.BLASST_ERR_INVALID_ARG),
-    (dict(Hq=32), K.BLASST_ERR_UNSUPPORTED),
+    (dict(Hq=256), K.BLASST_ERR_UNSUPPORTED),
+    (dict(Hq=48), K.BLASST_ERR_UNSUPPORTED),
     (dict(Hq=3), K.BLASST_ERR_UNSUPPORTED),
     (dict(dk=512), K.BLASST_ERR_UNSUPPORTED),
     (dict(dv=256), K.BLASST_ERR_UNSUPPORTED),

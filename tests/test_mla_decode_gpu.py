@@ -114,3 +114,50 @@ def test_full_size_sampled_sequences():
         parity.mla_check(a, res, lam, S, seqs=[0, 17, 40, 63])
     del a, res
     torch.cuda.empty_cache()
+
+
+# Above 16 heads the heads are spread over a cluster of Hq / 16 CTAs that share every
+# load and exchange their votes.  The workload gives every head a shared query
+# component and matching sinks, so that tiles skipped by all heads exist.
+CLUSTER_KW = dict(q_shared=6.0, sink_norm=32.0)
+
+
+@pytest.mark.parametrize("Hq", [32, 64, 128])
+@pytest.mark.parametrize("L", [129, 1500])
+def test_cluster_head_counts(Hq, L):
+    a = W.mla_decode(seed=Hq + L, B=3, Hq=Hq, L=L, device="cuda", **CLUSTER_KW)
+    nT = -(-L // 128)
+    skipped = 0
+    for lam in (0.0, 0.03, 0.1):
+        for S in sorted({1, min(3, nT)}):
+            res = _run(a, lam, S)
+            torch.cuda.synchronize()
+            parity.mla_check(a, res, lam, S)
+            skipped += int(res["skipped"].item())
+    if L > 129:
+        assert skipped > 0
+
+
+def test_cluster_lengths_and_pages():
+    lens = [0, 1, 128, 129, 1000, 2049]
+    a = W.mla_decode(seed=7, B=len(lens), Hq=64, L=2049, lens=lens, page_size=64, device="cuda", **CLUSTER_KW)
+    for lam, S in ((0.0, 1), (0.1, 4)):
+        ref = _run(a, lam, S)
+        got = _run(a, lam, S, page=True)
+        torch.cuda.synchronize()
+        assert torch.equal(got["map"], ref["map"])
+        assert torch.equal(got["o"], ref["o"]) and torch.equal(got["lse"], ref["lse"])
+        parity.mla_check(a, got, lam, S)
+
+
+def test_cluster_full_size_sampled():
+    """64 sequences x 32768 rows x 128 heads (clusters of 8 CTAs), planner's splits."""
+    a = W.mla_decode(seed=0, B=64, Hq=128, L=32768, device="cuda", **CLUSTER_KW)
+    for lam in (0.0, 0.1):
+        res = _run(a, lam, 0)
+        torch.cuda.synchronize()
+        n = int(res["skipped"].item())
+        assert (n == 0) if lam == 0.0 else (n > 0)
+        parity.mla_check(a, res, lam, res["num_splits"], seqs=[0, 63])
+    del a, res
+    torch.cuda.empty_cache()
