@@ -421,8 +421,8 @@ int blasst_mla_decode_num_splits(int B, int Hq, int max_kv_len, int requested, i
         *out = requested;
         return BLASST_OK;
     }
-    // one CTA per (sequence, split), a cluster of Hq / 16 of them above 16 heads
-    return plan_splits((long long)B * (Hq > 16 ? Hq / 16 : 1), nT, out);
+    // one CTA per (sequence, split), a cluster of Hq / 32 of them above 32 heads
+    return plan_splits((long long)B * (Hq > 32 ? Hq / 32 : 1), nT, out);
 }
 
 size_t blasst_mla_decode_workspace_size(int B, int Hq, int max_kv_len, int num_splits) {

@@ -13,8 +13,8 @@
 // One CTA runs one (sequence b, split s) pass over the split's key tiles in
 // ascending order.  Both products run with the key dimension on the 128 TMEM
 // lanes, as in the GQA decode kernel:
-//   S^T_j = K_j Q^T      M = 128 keys, N = 16 (heads, zero-padded), K = 576 (36 MMAs)
-//   O^T_j = V_j^T P_j^T  four M = 128 blocks of the 512 value columns, N = 16, K = 128 keys
+//   S^T_j = K_j Q^T      M = 128 keys, N = 16 or 32 (heads, zero-padded), K = 576 (36 MMAs)
+//   O^T_j = V_j^T P_j^T  four M = 128 blocks of the 512 value columns, N = 16 or 32, K = 128 keys
 // A 576-wide key tile is 144 KB, more than a ring of whole tiles leaves room for,
 // so tiles stream through a ring of 64-column boxes (16 KB) and the S MMAs of a
 // tile are issued box by box as the boxes land.  A kept tile's value columns are
@@ -23,20 +23,18 @@
 // were read a few microseconds earlier), and a skipped tile's values are never
 // read again.  (Keeping a tile's value columns in shared memory until its decision
 // instead leaves room to prefetch only one more pair, and every tile then waits a
-// full memory latency: measured 13 % slower on GB300.)  Shared memory: 64 KB of key
-// boxes, 128 KB of value pairs (one kept tile's four in flight at once), 18 KB of Q,
-// 8 KB of P; more value slots at the cost of key slots measured faster up to this
-// split.  Each P.V result lands in a fresh TMEM slot and is folded into
-// per-thread registers a few tiles later (thread t owns value columns t, t+128,
-// t+256, t+384 of every head).
+// full memory latency: measured 13 % slower on GB300.)  Each P.V result lands in a
+// fresh TMEM slot and is folded into per-thread registers a few tiles later (thread
+// t owns value columns t, t+128, t+256, t+384 of every head); the per-head maxima,
+// the same in every thread, live in shared memory.
 //
 // Warp roles (256 threads): warps 0-3 softmax, warp 4 key loader, warp 5 issuer of
 // the S MMAs and TMEM owner, warp 6 value loader, warp 7 issuer of the P.V MMAs.
 // The two MMA streams have their own issuing threads, so a P.V pass waiting for a
 // decision or a value pair never holds up the S MMAs that drain the key ring.
 //
-// More than 16 heads: a cluster of CG = Hq / 16 CTAs runs each (sequence, split),
-// CTA r holding heads [16r, 16r + 16).  The CTAs of a cluster read the same rows,
+// Up to 16 heads the MMA N is 16, up to 32 it is 32.  More than 32 heads: a cluster
+// of CG = Hq / 32 CTAs runs each (sequence, split), CTA r holding heads [32r, 32r + 32).  The CTAs of a cluster read the same rows,
 // so each key box and value pair is loaded once and multicast to all of them (the
 // entries of ring slot k are issued by CTA k mod CG); a slot is refilled once every
 // CTA's MMAs have released it (each MMA commit arrives on the slot's barrier in
@@ -69,50 +67,63 @@ constexpr int DK = kMlaDk;               // 576
 constexpr int DV = kMlaDv;               // 512
 constexpr int KBOX = DK / 64;            // 64-column boxes per key tile
 constexpr int VBLK = DV / 128;           // 128-column value blocks (box pairs) per key tile
-constexpr int NPAD = 16;                 // MMA N: the heads padded to 16
 constexpr int BOX_BYTES = kTile * 128;   // 128 keys x 64 columns
 constexpr int PAIR_BYTES = 2 * BOX_BYTES;
 constexpr int NKB = 4;                   // key box ring
-constexpr int NVP = 4;                   // value pair ring (a kept tile's four pairs in flight at once)
-constexpr int NS = 4, NO = 4;            // TMEM S slots (16 columns) / O slots (64 columns)
+constexpr int NS = 4;                    // TMEM S slots
 constexpr int NP = 2;                    // P staging buffers
 constexpr int ND = 8;                    // decision ring
 constexpr int NH = 8;                    // reference-max history ring
 constexpr int LAG = 2;                   // P.V results folded this many computed tiles late
-constexpr int Q_BYTES = KBOX * NPAD * 128;
-constexpr int P_BYTES = 2 * NPAD * 128;  // [key half][16 rows][64 keys]
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + NKB * BOX_BYTES;
-constexpr int OFF_Q = OFF_V + NVP * PAIR_BYTES;
-constexpr int OFF_P = OFF_Q + Q_BYTES;
-constexpr int OFF_CTRL = OFF_P + NP * P_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t O_COL = NS * NPAD;
-constexpr int O_SLOT = VBLK * NPAD;      // block i of a slot: columns [16i, 16i + 16)
-static_assert(O_COL + NO * O_SLOT <= TMEM_COLS, "TMEM budget");
-static_assert(LAG <= NO && NS + 2 <= ND, "ring sizes");
+static_assert(NS + 2 <= ND, "ring sizes");
 static_assert(DK % 64 == 0 && DV % 128 == 0 && DV <= DK, "row layout");
 
-struct MlaCtrl {
-    uint64_t k_full[NKB], k_empty[NKB], v_full[NVP], v_empty[NVP];
-    uint64_t s_full[NS], s_free[NS], dec_full[ND], dec_free[ND];
-    uint64_t p_full[NP], p_free[NP], o_full[NO], o_free[NO];
-    uint64_t q_full, drain[2];
-    uint32_t tmem_base;
-    int dec[ND];
-    int abort;
-    float red[2][4][NPAD];
-    float mref_hist[NH][NPAD];
-    float lred[4][NPAD];
-    // clusters: per decision slot, the vote of every CTA (low word: 1 = all its heads
-    // skip; high word: its margin) and the barrier their arrivals complete
-    uint64_t votes[ND][8];
-    uint64_t vote_full[ND];
-    uint64_t v_armed[NVP];  // every CTA armed the slot's next entry (in the slot's issuing CTA)
-    int cl_skip;  // the cluster's decision on the current tile, for the softmax threads
+// Layout for NPAD heads per CTA (the MMA N: 16, or 32 for 17-32 heads and clusters).
+// Shared memory: 64 KB of key boxes, NVP value pairs (128 KB / 96 KB), Q, P.  TMEM:
+// NS S slots of NPAD columns, NO O slots of VBLK * NPAD columns.  More value slots
+// at the cost of key slots measured faster, up to the split used for NPAD = 16.
+template <int NPAD_>
+struct MlaCfg {
+    static constexpr int NPAD = NPAD_;
+    static constexpr int NVP = NPAD == 16 ? 4 : 3;   // value pair ring
+    static constexpr int NO = NPAD == 16 ? 4 : 3;    // TMEM O slots
+    static constexpr int Q_BYTES = KBOX * NPAD * 128;
+    static constexpr int P_BYTES = 2 * NPAD * 128;   // [key half][NPAD rows][64 keys]
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + NKB * BOX_BYTES;
+    static constexpr int OFF_Q = OFF_V + NVP * PAIR_BYTES;
+    static constexpr int OFF_P = OFF_Q + Q_BYTES;
+    static constexpr int OFF_CTRL = OFF_P + NP * P_BYTES;
+    static constexpr uint32_t O_COL = NS * NPAD;
+    static constexpr int O_SLOT = VBLK * NPAD;       // block i of a slot: columns [i*NPAD, (i+1)*NPAD)
+    static_assert(O_COL + NO * O_SLOT <= TMEM_COLS, "TMEM budget");
+    static_assert(LAG <= NO, "fold lag");
+    struct Ctrl {
+        uint64_t k_full[NKB], k_empty[NKB], v_full[NVP], v_empty[NVP];
+        uint64_t s_full[NS], s_free[NS], dec_full[ND], dec_free[ND];
+        uint64_t p_full[NP], p_free[NP], o_full[NO], o_free[NO];
+        uint64_t q_full, drain[2];
+        uint32_t tmem_base;
+        int dec[ND];
+        int abort;
+        float red[2][4][NPAD];      // per-warp tile maxima, by tile parity
+        float mex[2][NPAD];         // exact running max per head, by tile parity
+        float mrf[2][NPAD];         // reference max per head, by tile parity
+        float alpha[NPAD];          // this tile's rescale factor per head
+        float gmar[NPAD];           // this tile's margin per head
+        float mref_hist[NH][NPAD];  // reference max at each computed tile's P
+        float lred[4][NPAD];
+        // clusters: per decision slot, the vote of every CTA (low word: 1 = all its
+        // heads skip; high word: its margin) and the barrier their arrivals complete
+        uint64_t votes[ND][8];
+        uint64_t vote_full[ND];
+        uint64_t v_armed[NVP];  // every CTA armed the slot's next entry (in the slot's issuing CTA)
+        int cl_skip;            // the cluster's decision on the current tile
+    };
+    static constexpr int SMEM = OFF_CTRL + (int)sizeof(Ctrl) + 1024;
+    static_assert(SMEM <= 232448, "shared memory per CTA");
 };
-constexpr int SMEM = OFF_CTRL + (int)sizeof(MlaCtrl) + 1024;
-static_assert(SMEM <= 232448, "shared memory per CTA");
 
 __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -121,10 +132,14 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 template <int G, bool PAGED, int CG>
 __global__ void __launch_bounds__(256, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const DecodeParams p) {
-    static_assert(CG == 1 || G == NPAD, "a cluster's CTAs hold 16 heads each");
+    using C = MlaCfg<(G <= 16 ? 16 : 32)>;
+    constexpr int NPAD = C::NPAD, NVP = C::NVP, NO = C::NO, P_BYTES = C::P_BYTES, O_SLOT = C::O_SLOT;
+    constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_Q = C::OFF_Q, OFF_P = C::OFF_P;
+    constexpr uint32_t O_COL = C::O_COL;
+    static_assert(CG == 1 || G == NPAD, "a cluster's CTAs hold NPAD heads each");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
-    MlaCtrl* ctrl = reinterpret_cast<MlaCtrl*>(smem + OFF_CTRL);
+    auto* ctrl = reinterpret_cast<typename C::Ctrl*>(smem + C::OFF_CTRL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int s = blockIdx.x / CG, b = blockIdx.z;
     const uint32_t rank = CG > 1 ? cluster_ctarank() : 0u;
@@ -157,6 +172,8 @@ __global__ void __launch_bounds__(256, 1)
         }
         for (int i = 0; i < NP; ++i) { mbar_init(&ctrl->p_full[i], 4); mbar_init(&ctrl->p_free[i], 1); }
         for (int i = 0; i < NO; ++i) { mbar_init(&ctrl->o_full[i], 1); mbar_init(&ctrl->o_free[i], 4); }
+        for (int g = 0; g < NPAD; ++g)
+            for (int q = 0; q < 2; ++q) ctrl->mex[q][g] = ctrl->mrf[q][g] = -CUDART_INF_F;
         mbar_init(&ctrl->q_full, 4);
         mbar_init(&ctrl->drain[0], 1);
         mbar_init(&ctrl->drain[1], 1);
@@ -404,78 +421,112 @@ __global__ void __launch_bounds__(256, 1)
         }
         const long long mapbase = (long long)b * p.nK;
         const float cl = p.c_log2;
-        float m_exact[G], m_ref[G], lpart[G], oacc[VBLK][G];
+        // Per-head running state common to all 128 threads lives in shared memory, by
+        // tile parity: mex (exact running max) and mrf (reference max) of tile j are
+        // written by thread g for head g and read by everyone from tile j+1 on (after
+        // that tile's first barrier).  Per thread: the scores of its key, its partial
+        // row sums and its four value columns of every head.
+        float lpart[G], oacc[VBLK][G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            m_exact[g] = -CUDART_INF_F;
-            m_ref[g] = -CUDART_INF_F;
             lpart[g] = 0.f;
 #pragma unroll
             for (int i = 0; i < VBLK; ++i) oacc[i][g] = 0.f;
         }
-        int comp = 0, folded = 0;
+        int comp = 0, folded = 0, cur = 1;  // mrf[cur]: the reference max as of the last tile
         unsigned long long nskip = 0;
 
         auto fold = [&](int c) {
             const int os = c % NO;
             mbar_wait(&ctrl->o_full[os], (c / NO) & 1, wd);
             tc_fence_after();
-            uint32_t yr[O_SLOT];
-            tmem_ld32(tl + O_COL + os * O_SLOT, yr);
-            tmem_ld32(tl + O_COL + os * O_SLOT + 32, yr + 32);
-            tmem_ld_wait();
-            fence_regs<O_SLOT>(yr);
+            const volatile float* mh = ctrl->mref_hist[c % NH];
+            const volatile float* mr = ctrl->mrf[cur];
+#pragma unroll
+            for (int i = 0; i < VBLK; ++i) {
+                uint32_t yr[NPAD];
+                if constexpr (NPAD == 16)
+                    tmem_ld16(tl + O_COL + os * O_SLOT + i * NPAD, yr);
+                else
+                    tmem_ld32(tl + O_COL + os * O_SLOT + i * NPAD, yr);
+                tmem_ld_wait();
+                fence_regs<NPAD>(yr);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float a = mh[g], m = mr[g];
+                    const float f = (a == m) ? 1.f : ex2((a - m) * cl);
+                    oacc[i][g] = fmaf(f, __uint_as_float(yr[g]), oacc[i][g]);
+                }
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->o_free[os]);
-            const volatile float* mh = ctrl->mref_hist[c % NH];
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float f = (mh[g] == m_ref[g]) ? 1.f : ex2((mh[g] - m_ref[g]) * cl);
-#pragma unroll
-                for (int i = 0; i < VBLK; ++i) oacc[i][g] = fmaf(f, __uint_as_float(yr[i * NPAD + g]), oacc[i][g]);
-            }
         };
 
         for (int j = 0; j < n; ++j) {
-            const int ss = j % NS;
+            const int ss = j % NS, q = j & 1, qp = q ^ 1;
             mbar_wait(&ctrl->s_full[ss], (j / NS) & 1, wd);
             tc_fence_after();
-            uint32_t xr[16];
-            tmem_ld16(tl + ss * NPAD, xr);
-            tmem_ld_wait();
-            fence_regs<16>(xr);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->s_free[ss]);
             const int key = (t0 + j) * kTile + tid;
             const bool key_ok = key < Lb;
-            float x[G];
+            // the scores of this thread's key, one per head; read again for P, so the
+            // slot is released after P (nothing stays live across the decision)
+            auto load_scores = [&](uint32_t* xr) {
+                if constexpr (NPAD == 16)
+                    tmem_ld16(tl + ss * NPAD, xr);
+                else
+                    tmem_ld32(tl + ss * NPAD, xr);
+                tmem_ld_wait();
+                fence_regs<NPAD>(xr);
+            };
+            {
+                // per-head max over the warp's 32 keys by a transposing butterfly: each
+                // step hands half of the remaining heads to the partner lane, so lane L
+                // ends with the max of head L >> (5 - log2 G) after G - 1 + (5 - log2 G)
+                // shuffles instead of 5 G
+                uint32_t xr[NPAD];
+                load_scores(xr);
+                float v[G];
 #pragma unroll
-            for (int g = 0; g < G; ++g) x[g] = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
-            // per-head tile max over the 128 keys: warp shuffle, then across the 4 warps
+                for (int g = 0; g < G; ++g) v[g] = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
+                int hl = 0;  // head index held by this lane
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float v = x[g];
+                for (int st = 0; st < 5; ++st) {
+                    const int o = 16 >> st;
+                    const int half = G >> (st + 1);  // heads handed over at this step (0: none left)
+                    if (half >= 1) {
+                        const bool up = (lane & o) != 0;
 #pragma unroll
-                for (int sh = 16; sh > 0; sh >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, sh));
-                if (lane == 0) ctrl->red[j & 1][warp][g] = v;
+                        for (int k = 0; k < half; ++k) {
+                            const float send = up ? v[k] : v[k + half];
+                            const float keep = up ? v[k + half] : v[k];
+                            v[k] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, o));
+                        }
+                        hl += up ? half : 0;
+                    } else {
+                        v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
+                    }
+                }
+                constexpr int kLow = 32 / G;  // lanes holding the same head
+                if ((lane & (kLow - 1)) == 0) ctrl->red[q][warp][hl] = v[0];
             }
             named_bar_sync(1, 128);
-            float mnew[G];
-            bool skip = true;
-            float margin = -CUDART_INF_F;
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const volatile float* rd = &ctrl->red[j & 1][0][g];
+            // the decision: thread g judges head g, the barrier takes the AND
+            float mn_own = -CUDART_INF_F;
+            bool vote = true;
+            if (tid < G) {
+                const volatile float* rd = &ctrl->red[q][0][tid];
                 const float mt = fmaxf(fmaxf(rd[0], rd[NPAD]), fmaxf(rd[2 * NPAD], rd[3 * NPAD]));
-                mnew[g] = fmaxf(m_exact[g], mt);
-                const float diff = mt - mnew[g];
-                skip = skip && (diff < p.thr_raw);
-                const float gm = (mt == -CUDART_INF_F && mnew[g] == -CUDART_INF_F) ? CUDART_INF_F : diff;
-                margin = fmaxf(margin, gm);
-                m_exact[g] = mnew[g];
+                mn_own = fmaxf(reinterpret_cast<volatile float*>(ctrl->mex[qp])[tid], mt);
+                const float diff = mt - mn_own;
+                vote = diff < p.thr_raw;
+                ctrl->gmar[tid] = (mt == -CUDART_INF_F && mn_own == -CUDART_INF_F) ? CUDART_INF_F : diff;
+                ctrl->mex[q][tid] = mn_own;
             }
+            bool skip = bar_red_and(1, 128, vote);
+            float margin = -CUDART_INF_F;
+            if (tid == 0)
+                for (int g = 0; g < G; ++g) margin = fmaxf(margin, reinterpret_cast<volatile float*>(ctrl->gmar)[g]);
             if constexpr (CG > 1) {
                 // The decision covers the heads of every CTA of the cluster: send this
                 // CTA's vote and margin to all of them, wait for theirs, take the AND and
@@ -511,29 +562,44 @@ __global__ void __launch_bounds__(256, 1)
                     nskip += skip ? 1 : 0;
                 }
             }
+            // thread g moves head g's reference max (computed tiles only) and carries it
+            // into this tile's buffer; the factor for O and l goes to alpha[g]
+            if (tid < G) {
+                const float mro = reinterpret_cast<volatile float*>(ctrl->mrf[qp])[tid];
+                float mr = mro, a = 1.f;
+                if (!skip && mn_own != -CUDART_INF_F && (mro == -CUDART_INF_F || mn_own > mro + p.lazy_raw)) {
+                    a = mro == -CUDART_INF_F ? 0.f : ex2((mro - mn_own) * cl);
+                    mr = mn_own;
+                }
+                ctrl->mrf[q][tid] = mr;
+                if (!skip) {
+                    ctrl->alpha[tid] = a;
+                    ctrl->mref_hist[comp % NH][tid] = mr;
+                }
+            }
             if (!skip) {
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    if (mnew[g] != -CUDART_INF_F && (m_ref[g] == -CUDART_INF_F || mnew[g] > m_ref[g] + p.lazy_raw)) {
-                        const float a = m_ref[g] == -CUDART_INF_F ? 0.f : ex2((m_ref[g] - mnew[g]) * cl);
-#pragma unroll
-                        for (int i = 0; i < VBLK; ++i) oacc[i][g] *= a;
-                        lpart[g] *= a;
-                        m_ref[g] = mnew[g];
-                    }
-                }
-                if (tid == 0) {
-#pragma unroll
-                    for (int g = 0; g < G; ++g) ctrl->mref_hist[comp % NH][g] = m_ref[g];
-                }
+                named_bar_sync(1, 128);  // alpha, mrf[q] and mref_hist visible
+                cur = q;
+                uint32_t xr[NPAD];
+                load_scores(xr);
+                const volatile float* al = ctrl->alpha;
+                const volatile float* mrv = ctrl->mrf[q];
                 const int pb = comp % NP;
                 if (comp >= NP) mbar_wait(&ctrl->p_free[pb], ((comp / NP) - 1) & 1, wd);
                 uint8_t* pbuf = smem + OFF_P + pb * P_BYTES + (tid >> 6) * (NPAD * 128);
                 const int cw = (tid & 63) >> 3;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float mr = m_ref[g] == -CUDART_INF_F ? 0.f : m_ref[g];
-                    const float pv = ex2(fmaf(x[g], cl, -mr * cl));
+                    const float a = al[g];
+                    if (a != 1.f) {
+#pragma unroll
+                        for (int i = 0; i < VBLK; ++i) oacc[i][g] *= a;
+                        lpart[g] *= a;
+                    }
+                    const float m = mrv[g];
+                    const float mr = m == -CUDART_INF_F ? 0.f : m;
+                    const float xg = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
+                    const float pv = ex2(fmaf(xg, cl, -mr * cl));
                     lpart[g] += pv;
                     *reinterpret_cast<unsigned short*>(pbuf + g * 128 + ((cw ^ (g & 7)) << 4) + (tid & 7) * 2) =
                         (unsigned short)(pack_bf16x2(pv, 0.f) & 0xffffu);
@@ -543,9 +609,13 @@ __global__ void __launch_bounds__(256, 1)
                 if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
                 ++comp;
             }
+            tc_fence_before();  // the S slot's last read is done
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ctrl->s_free[ss]);
             while (comp - folded > LAG) fold(folded++);
         }
         named_bar_sync(1, 128);
+        cur = (n - 1) & 1;  // the last tile's buffer holds every head's final reference max
         while (folded < comp) fold(folded++);
 
         // l = sum over the 128 key lanes; O = oacc / l
@@ -562,7 +632,8 @@ __global__ void __launch_bounds__(256, 1)
             const volatile float* lr = &ctrl->lred[0][g];
             const float l = lr[0] + lr[NPAD] + lr[2 * NPAD] + lr[3 * NPAD];
             const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float lse = l > 0.f ? m_ref[g] * p.scale + __logf(l) : -CUDART_INF_F;
+            const float mrg = reinterpret_cast<volatile float*>(ctrl->mrf[cur])[g];
+            const float lse = l > 0.f ? mrg * p.scale + __logf(l) : -CUDART_INF_F;
             const long long hq = (long long)b * p.Hq + h0 + g;
             if (p.S == 1) {
 #pragma unroll
@@ -593,6 +664,7 @@ __global__ void __launch_bounds__(256, 1)
 template <int G, bool PAGED, int CG>
 cudaError_t launch_gp(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
     auto kern = mla_decode_kernel<G, PAGED, CG>;
+    constexpr int SMEM = MlaCfg<(G <= 16 ? 16 : 32)>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -622,7 +694,7 @@ cudaError_t launch_g(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t
 
 }  // namespace
 
-// Hq <= 16: one CTA per (sequence, split); 32, 64, 128: clusters of Hq / 16 CTAs.
+// Hq <= 32: one CTA per (sequence, split); 64, 128: clusters of Hq / 32 CTAs.
 cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
     switch (p.Hq) {
         case 1: return launch_g<1, 1>(tkv, p, stream);
@@ -630,9 +702,9 @@ cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cud
         case 4: return launch_g<4, 1>(tkv, p, stream);
         case 8: return launch_g<8, 1>(tkv, p, stream);
         case 16: return launch_g<16, 1>(tkv, p, stream);
-        case 32: return launch_g<16, 2>(tkv, p, stream);
-        case 64: return launch_g<16, 4>(tkv, p, stream);
-        case 128: return launch_g<16, 8>(tkv, p, stream);
+        case 32: return launch_g<32, 1>(tkv, p, stream);
+        case 64: return launch_g<32, 2>(tkv, p, stream);
+        case 128: return launch_g<32, 4>(tkv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
