@@ -63,6 +63,21 @@ bool encode_3d(CUtensorMap* map, const void* base, int d, int L, long long Z) {
     return r == CUDA_SUCCESS;
 }
 
+// [Z][L][d] bf16 as a 3-D tensor with boxes of 64 columns x `rows` rows (the latent
+// page pool of MLA decode: Z = 1, L = num_pages * page_size rows of d values).
+bool encode_rows(CUtensorMap* map, const void* base, int d, long long L, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)L, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)L * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // 4-D map over a page pool of bf16 K or V, box = 64 columns x `rows` keys of one
 // head of one page.  Dimensions are ordered by stride:
 //   key-major pool [page][key][head][d]: (d, head, key, page)
@@ -461,7 +476,8 @@ int blasst_mla_decode(const void* q, const void* kv, const int* page_table, cons
     }
     CUtensorMap tkv;
     const int rows = page_size < kTile ? page_size : kTile;
-    if (page_table ? !encode_pages(&tkv, kv, dk, page_size, 1, num_pages, 1, rows)
+    if (page_table && (long long)num_pages * page_size > 0x7fffffffLL - kTile) return BLASST_ERR_UNSUPPORTED;
+    if (page_table ? !encode_rows(&tkv, kv, dk, (long long)num_pages * page_size, rows)
                    : !encode_3d(&tkv, kv, dk, max_kv_len, B))
         return BLASST_ERR_CUDA;
 

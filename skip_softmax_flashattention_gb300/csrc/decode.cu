@@ -186,9 +186,14 @@ __global__ void __launch_bounds__(224, 1)
         } else {
             if (lane == 0) tma_prefetch_desc(&tk);
             int issued = 0;
+            // each lane's page index is read two tiles ahead of its copy
+            int pg_next = n > 0 ? box_page(t0, lane) : 0;
+            int pg_next2 = n > 1 ? box_page(t0 + 1, lane) : 0;
             for (int j = 0; j < n; ++j) {
                 const int ks = j % NK;
-                const int pg = box_page(t0 + j, lane);  // read while lane 0 waits for the slot
+                const int pg = pg_next;
+                pg_next = pg_next2;
+                pg_next2 = j + 2 < n ? box_page(t0 + j + 2, lane) : 0;
                 int ok = 1;
                 if (lane == 0) {
                     if (j >= NK && !mbar_wait(&ctrl->k_empty[ks], ((j / NK) - 1) & 1, wd))

@@ -226,12 +226,15 @@ __global__ void __launch_bounds__(256, 1)
         }
         return e;
     };
+    // the pool is rows: page pg's row `off` is row pg * page_size + off (an out-of-range
+    // page lands past the last row and reads as zeros)
     auto issue_sub_box = [&](uint8_t* dst, uint64_t* bar, int x, int tile, int i, int pg) {
         const int off = (tile * kTile + i * p.rows_per_box) % p.page_size;
+        const int y = pg * p.page_size + off;
         if constexpr (CG == 1)
-            tma_load_4d(dst + i * p.rows_per_box * 128, &tkv, bar, x, 0, off, pg);
+            tma_load_3d(dst + i * p.rows_per_box * 128, &tkv, bar, x, y, 0);
         else
-            tma_load_4d_mc(dst + i * p.rows_per_box * 128, &tkv, bar, x, 0, off, pg, kAll);
+            tma_load_3d_mc(dst + i * p.rows_per_box * 128, &tkv, bar, x, y, 0, kAll);
     };
 
     if (warp == 4) {
@@ -242,8 +245,16 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) tma_prefetch_desc(&tkv);
         int last = 0;  // entries passed
         bool ok = true;
+        // paged: each lane's page index is read two tiles ahead, so the load's latency
+        // never sits between a freed slot and its copy
+        int pg_next = (PAGED && n > 0) ? box_page(t0, lane) : 0;
+        int pg_next2 = (PAGED && n > 1) ? box_page(t0 + 1, lane) : 0;
         for (int j = 0; j < n && ok; ++j) {
-            const int pg = PAGED ? box_page(t0 + j, lane) : 0;
+            const int pg = pg_next;
+            if constexpr (PAGED) {
+                pg_next = pg_next2;
+                pg_next2 = j + 2 < n ? box_page(t0 + j + 2, lane) : 0;
+            }
             for (int c = 0; c < KBOX; ++c) {
                 const int e = j * KBOX + c, ks = e % NKB;
                 if (issues(ks)) {
