@@ -52,7 +52,7 @@ extern "C" {
 #define BLASST_OK 0
 #define BLASST_WARN_LAMBDA_GE_1 1        /* blasst_lambda: curve gave lambda > 1 (value still returned) */
 #define BLASST_ERR_INVALID_ARG (-1)      /* null required pointer, bad size, lambda/scale out of range */
-#define BLASST_ERR_UNSUPPORTED (-2)      /* valid request this build does not run (d, G, alignment) */
+#define BLASST_ERR_UNSUPPORTED (-2)      /* valid request the library does not support (d, G, alignment) */
 #define BLASST_ERR_WORKSPACE_TOO_SMALL (-3)
 #define BLASST_ERR_CUDA (-4)             /* a CUDA runtime/driver call failed */
 #define BLASST_ERR_TIMEOUT (-5)          /* a device-side wait ran past its limit (see blasst_device_status) */

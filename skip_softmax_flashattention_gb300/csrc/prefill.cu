@@ -852,7 +852,6 @@ __global__ void __launch_bounds__(384, 1)
                 }
                 const float mc = (m_ref == -CUDART_INF_F ? 0.f : m_ref) * p.c_log2;
                 float rs = 0.f;
-#pragma unroll
                 // P in two 32-column stores (one per half; measured 1.6 % faster than four
                 // 16-column ones)
 #pragma unroll
