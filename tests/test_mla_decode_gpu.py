@@ -161,3 +161,34 @@ def test_cluster_full_size_sampled():
         parity.mla_check(a, res, lam, res["num_splits"], seqs=[0, 63])
     del a, res
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("Hq", [16, 64])
+def test_bad_page_index_and_length_are_contained_and_reported(Hq):
+    """Out-of-range page indices (too large, negative) are never dereferenced: those
+    rows read as zeros and the device status says so; a length above max_kv_len is
+    clamped and reported.  The next normal call is exact."""
+    kw = CLUSTER_KW if Hq > 16 else {}
+    a = W.mla_decode(seed=11, B=3, Hq=Hq, L=640, lens=[640, 300, 500], page_size=64, device="cuda", **kw)
+    ex = a.extra
+    table, lens = ex["page_table"].clone(), ex["seq_lens"].clone()
+    bad = table.clone()
+    bad[0, 1] = ex["kv_pages"].shape[0] + 1000
+    bad[1, 2] = -5
+    ex["page_table"] = bad
+    res = _run(a, 0.0, 2, page=True)
+    torch.cuda.synchronize()
+    assert K.blasst_device_status(1) == K.BLASST_ERR_PAGE_TABLE
+    assert torch.isfinite(res["o"].float()).all() and not torch.isnan(res["lse"]).any()
+    ex["page_table"] = table
+    long_lens = lens.clone()
+    long_lens[2] = 10 ** 6  # clamped to max_kv_len
+    ex["seq_lens"] = long_lens
+    res = _run(a, 0.0, 2, page=True)
+    torch.cuda.synchronize()
+    assert K.blasst_device_status(1) == K.BLASST_ERR_PAGE_TABLE
+    assert int((res["map"][2] != 2).sum().item()) == 5  # 640 rows = 5 tiles
+    ex["seq_lens"] = lens
+    res = _run(a, 0.03, 2, page=True)
+    torch.cuda.synchronize()
+    parity.mla_check(a, res, 0.03, 2)
