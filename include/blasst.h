@@ -230,8 +230,8 @@ size_t blasst_decode_noalloc_scratch_bytes(void);
  * row's first dv = 512 values.  One skip decision covers all Hq heads x 128 keys.
  *   q [B, Hq, dk], o [B, Hq, dv] bf16; lse nullable fp32 [B, Hq].
  *   Hq           1, 2, 4, 8, 16, 32, 64 or 128 query heads (else
- *                BLASST_ERR_UNSUPPORTED); above 32 the heads are spread over a cluster
- *                of Hq / 32 CTAs that share every load.  dk must be 576 and dv 512
+ *                BLASST_ERR_UNSUPPORTED); above 64 the heads are spread over a cluster
+ *                of Hq / 64 CTAs that share every load.  dk must be 576 and dv 512
  *                (else BLASST_ERR_UNSUPPORTED).
  *   kv           page_table NULL: contiguous bf16 [B][max_kv_len][dk];
  *                page_table set: a pool of num_pages pages of page_size rows,
@@ -265,7 +265,7 @@ int blasst_mla_decode(const void* q, const void* kv, const int* page_table, cons
                       float* margins, void* stream);
 
 /* Split count for blasst_mla_decode: `requested` (1 .. ceil(max_kv_len/128)) if
- * positive, else the fewest splits whose B * splits * max(1, Hq/32) CTAs fill the
+ * positive, else the fewest splits whose B * splits * max(1, Hq/64) CTAs fill the
  * last wave of the GPU's SMs to at least 90 %. */
 int blasst_mla_decode_num_splits(int B, int Hq, int max_kv_len, int requested, int* out);
 

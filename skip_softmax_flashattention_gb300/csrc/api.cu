@@ -436,8 +436,8 @@ int blasst_mla_decode_num_splits(int B, int Hq, int max_kv_len, int requested, i
         *out = requested;
         return BLASST_OK;
     }
-    // one CTA per (sequence, split), a cluster of Hq / 32 of them above 32 heads
-    return plan_splits((long long)B * (Hq > 32 ? Hq / 32 : 1), nT, out);
+    // one CTA per (sequence, split), a cluster of Hq / 64 of them above 64 heads
+    return plan_splits((long long)B * (Hq > 64 ? Hq / 64 : 1), nT, out);
 }
 
 size_t blasst_mla_decode_workspace_size(int B, int Hq, int max_kv_len, int num_splits) {

@@ -13,8 +13,8 @@
 // One CTA runs one (sequence b, split s) pass over the split's key tiles in
 // ascending order.  Both products run with the key dimension on the 128 TMEM
 // lanes, as in the GQA decode kernel:
-//   S^T_j = K_j Q^T      M = 128 keys, N = 16 or 32 (heads, zero-padded), K = 576 (36 MMAs)
-//   O^T_j = V_j^T P_j^T  four M = 128 blocks of the 512 value columns, N = 16 or 32, K = 128 keys
+//   S^T_j = K_j Q^T      M = 128 keys, N = 16, 32 or 64 (heads, zero-padded), K = 576 (36 MMAs)
+//   O^T_j = V_j^T P_j^T  four M = 128 blocks of the 512 value columns, N as above, K = 128 keys
 // A 576-wide key tile is 144 KB, more than a ring of whole tiles leaves room for,
 // so tiles stream through a ring of 64-column boxes (16 KB) and the S MMAs of a
 // tile are issued box by box as the boxes land.  A kept tile's value columns are
@@ -23,18 +23,20 @@
 // were read a few microseconds earlier), and a skipped tile's values are never
 // read again.  (Keeping a tile's value columns in shared memory until its decision
 // instead leaves room to prefetch only one more pair, and every tile then waits a
-// full memory latency: measured 13 % slower on GB300.)  Each P.V result lands in a
-// fresh TMEM slot and is folded into per-thread registers a few tiles later (thread
-// t owns value columns t, t+128, t+256, t+384 of every head); the per-head maxima,
-// the same in every thread, live in shared memory.
+// full memory latency: measured 13 % slower on GB300.)  O stays in TMEM as one
+// accumulator over the computed tiles; when a head's reference max moves, the
+// softmax threads wait for the newest P.V and rescale that head's columns in place
+// before the next P.V.  The per-head maxima, the same in every thread, live in
+// shared memory; each thread keeps its partial row sums.
 //
 // Warp roles (256 threads): warps 0-3 softmax, warp 4 key loader, warp 5 issuer of
 // the S MMAs and TMEM owner, warp 6 value loader, warp 7 issuer of the P.V MMAs.
 // The two MMA streams have their own issuing threads, so a P.V pass waiting for a
 // decision or a value pair never holds up the S MMAs that drain the key ring.
 //
-// Up to 16 heads the MMA N is 16, up to 32 it is 32.  More than 32 heads: a cluster
-// of CG = Hq / 32 CTAs runs each (sequence, split), CTA r holding heads [32r, 32r + 32).  The CTAs of a cluster read the same rows,
+// Up to 16 heads the MMA N is 16, up to 32 it is 32, up to 64 it is 64.  128 heads: a
+// cluster of CG = 2 CTAs runs each (sequence, split), CTA r holding heads
+// [64r, 64r + 64).  The CTAs of a cluster read the same rows,
 // so each key box and value pair is loaded once and multicast to all of them (the
 // entries of ring slot k are issued by CTA k mod CG); a slot is refilled once every
 // CTA's MMAs have released it (each MMA commit arrives on the slot's barrier in
@@ -69,25 +71,25 @@ constexpr int KBOX = DK / 64;            // 64-column boxes per key tile
 constexpr int VBLK = DV / 128;           // 128-column value blocks (box pairs) per key tile
 constexpr int BOX_BYTES = kTile * 128;   // 128 keys x 64 columns
 constexpr int PAIR_BYTES = 2 * BOX_BYTES;
-constexpr int NKB = 4;                   // key box ring
 constexpr int NS = 4;                    // TMEM S slots
 constexpr int NP = 2;                    // P staging buffers
 constexpr int ND = 8;                    // decision ring
-constexpr int NH = 8;                    // reference-max history ring
-constexpr int LAG = 2;                   // P.V results folded this many computed tiles late
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(NS + 2 <= ND, "ring sizes");
 static_assert(DK % 64 == 0 && DV % 128 == 0 && DV <= DK, "row layout");
 
-// Layout for NPAD heads per CTA (the MMA N: 16, or 32 for 17-32 heads and clusters).
-// Shared memory: 64 KB of key boxes, NVP value pairs (128 KB / 96 KB), Q, P.  TMEM:
-// NS S slots of NPAD columns, NO O slots of VBLK * NPAD columns.  More value slots
-// at the cost of key slots measured faster, up to the split used for NPAD = 16.
+// Layout for NPAD heads per CTA (the MMA N: 16, 32, or 64).  Shared memory: NKB key
+// boxes, NVP value pairs, Q, P.  TMEM: NS S slots of NPAD columns, then O (VBLK
+// blocks of NPAD columns), one accumulator over the computed tiles, rescaled in
+// place when a head's reference max moves.  (Landing each P.V in a fresh slot and
+// folding it into registers instead measured 4 % slower at 16 heads and 30 % at 32.)
+// More value slots at the cost of key slots measured faster, up to the split used
+// for NPAD = 16.
 template <int NPAD_>
 struct MlaCfg {
     static constexpr int NPAD = NPAD_;
-    static constexpr int NVP = NPAD == 16 ? 4 : 3;   // value pair ring
-    static constexpr int NO = NPAD == 16 ? 4 : 3;    // TMEM O slots
+    static constexpr int NKB = NPAD == 64 ? 3 : 4;   // key box ring
+    static constexpr int NVP = NPAD == 16 ? 4 : NPAD == 32 ? 3 : 2;  // value pair ring
     static constexpr int Q_BYTES = KBOX * NPAD * 128;
     static constexpr int P_BYTES = 2 * NPAD * 128;   // [key half][NPAD rows][64 keys]
     static constexpr int OFF_K = 0;
@@ -95,15 +97,14 @@ struct MlaCfg {
     static constexpr int OFF_Q = OFF_V + NVP * PAIR_BYTES;
     static constexpr int OFF_P = OFF_Q + Q_BYTES;
     static constexpr int OFF_CTRL = OFF_P + NP * P_BYTES;
-    static constexpr uint32_t O_COL = NS * NPAD;
-    static constexpr int O_SLOT = VBLK * NPAD;       // block i of a slot: columns [i*NPAD, (i+1)*NPAD)
-    static_assert(O_COL + NO * O_SLOT <= TMEM_COLS, "TMEM budget");
-    static_assert(LAG <= NO, "fold lag");
+    static constexpr uint32_t O_COL = NS * NPAD;     // O block i: columns O_COL + [i*NPAD, (i+1)*NPAD)
+    static_assert(O_COL + VBLK * NPAD <= TMEM_COLS, "TMEM budget");
     struct Ctrl {
         uint64_t k_full[NKB], k_empty[NKB], v_full[NVP], v_empty[NVP];
         uint64_t s_full[NS], s_free[NS], dec_full[ND], dec_free[ND];
-        uint64_t p_full[NP], p_free[NP], o_full[NO], o_free[NO];
+        uint64_t p_full[NP], p_free[NP];
         uint64_t q_full, drain[2];
+        uint64_t o_done[8];         // computed tile c's P.V is done (ring of 8, phase c / 8)
         uint32_t tmem_base;
         int dec[ND];
         int abort;
@@ -112,8 +113,8 @@ struct MlaCfg {
         float mrf[2][NPAD];         // reference max per head, by tile parity
         float alpha[NPAD];          // this tile's rescale factor per head
         float gmar[NPAD];           // this tile's margin per head
-        float mref_hist[NH][NPAD];  // reference max at each computed tile's P
         float lred[4][NPAD];
+        float inv_l[NPAD];          // 1 / l per head for the outputs
         // clusters: per decision slot, the vote of every CTA (low word: 1 = all its
         // heads skip; high word: its margin) and the barrier their arrivals complete
         uint64_t votes[ND][8];
@@ -132,8 +133,8 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 template <int G, bool PAGED, int CG>
 __global__ void __launch_bounds__(256, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const DecodeParams p) {
-    using C = MlaCfg<(G <= 16 ? 16 : 32)>;
-    constexpr int NPAD = C::NPAD, NVP = C::NVP, NO = C::NO, P_BYTES = C::P_BYTES, O_SLOT = C::O_SLOT;
+    using C = MlaCfg<(G <= 16 ? 16 : G <= 32 ? 32 : 64)>;
+    constexpr int NPAD = C::NPAD, NKB = C::NKB, NVP = C::NVP, P_BYTES = C::P_BYTES;
     constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_Q = C::OFF_Q, OFF_P = C::OFF_P;
     constexpr uint32_t O_COL = C::O_COL;
     static_assert(CG == 1 || G == NPAD, "a cluster's CTAs hold NPAD heads each");
@@ -171,7 +172,7 @@ __global__ void __launch_bounds__(256, 1)
             mbar_init(&ctrl->dec_free[i], 2);  // released by the P.V issuer and the value loader
         }
         for (int i = 0; i < NP; ++i) { mbar_init(&ctrl->p_full[i], 4); mbar_init(&ctrl->p_free[i], 1); }
-        for (int i = 0; i < NO; ++i) { mbar_init(&ctrl->o_full[i], 1); mbar_init(&ctrl->o_free[i], 4); }
+        for (int i = 0; i < 8; ++i) mbar_init(&ctrl->o_done[i], 1);
         for (int g = 0; g < NPAD; ++g)
             for (int q = 0; q < 2; ++q) ctrl->mex[q][g] = ctrl->mrf[q][g] = -CUDART_INF_F;
         mbar_init(&ctrl->q_full, 4);
@@ -386,9 +387,8 @@ __global__ void __launch_bounds__(256, 1)
                 const bool skipped = reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] != 0;
                 mbar_arrive(&ctrl->dec_free[j % ND]);
                 if (skipped) continue;
-                const int pb = comp % NP, os = comp % NO;
+                const int pb = comp % NP;
                 if (!(ok = mbar_wait(&ctrl->p_full[pb], (comp / NP) & 1, wd))) break;
-                if (comp >= NO && !(ok = mbar_wait(&ctrl->o_free[os], ((comp / NO) - 1) & 1, wd))) break;
                 const uint32_t pbuf = sP + pb * P_BYTES;
                 for (int i = 0; i < VBLK && ok; ++i) {
                     const int e = comp * VBLK + i, vs = e % NVP;
@@ -399,12 +399,14 @@ __global__ void __launch_bounds__(256, 1)
                     for (int kk = 0; kk < kTile / 16; ++kk) {
                         const uint64_t adesc = desc_mnmajor_sw128(vb + kk * 2048, BOX_BYTES);
                         const uint64_t bdesc = desc_kmajor_sw128(pbuf + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32);
-                        mma_ss(tmem + O_COL + os * O_SLOT + i * NPAD, adesc, bdesc, kIdescO, kk > 0 ? 1u : 0u);
+                        // O accumulates over the computed tiles
+                        const uint32_t acc = (kk > 0 || comp > 0) ? 1u : 0u;
+                        mma_ss(tmem + O_COL + i * NPAD, adesc, bdesc, kIdescO, acc);
                     }
                     release(&ctrl->v_empty[vs]);
                 }
                 if (!ok) break;
-                mma_commit(&ctrl->o_full[os]);
+                mma_commit(&ctrl->o_done[comp % 8]);
                 mma_commit(&ctrl->p_free[pb]);
                 ++comp;
             }
@@ -437,42 +439,27 @@ __global__ void __launch_bounds__(256, 1)
         // written by thread g for head g and read by everyone from tile j+1 on (after
         // that tile's first barrier).  Per thread: the scores of its key, its partial
         // row sums and its four value columns of every head.
-        float lpart[G], oacc[VBLK][G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            lpart[g] = 0.f;
-#pragma unroll
-            for (int i = 0; i < VBLK; ++i) oacc[i][g] = 0.f;
-        }
-        int comp = 0, folded = 0, cur = 1;  // mrf[cur]: the reference max as of the last tile
-        unsigned long long nskip = 0;
-
-        auto fold = [&](int c) {
-            const int os = c % NO;
-            mbar_wait(&ctrl->o_full[os], (c / NO) & 1, wd);
-            tc_fence_after();
-            const volatile float* mh = ctrl->mref_hist[c % NH];
-            const volatile float* mr = ctrl->mrf[cur];
-#pragma unroll
-            for (int i = 0; i < VBLK; ++i) {
-                uint32_t yr[NPAD];
-                if constexpr (NPAD == 16)
-                    tmem_ld16(tl + O_COL + os * O_SLOT + i * NPAD, yr);
-                else
-                    tmem_ld32(tl + O_COL + os * O_SLOT + i * NPAD, yr);
-                tmem_ld_wait();
-                fence_regs<NPAD>(yr);
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float a = mh[g], m = mr[g];
-                    const float f = (a == m) ? 1.f : ex2((a - m) * cl);
-                    oacc[i][g] = fmaf(f, __uint_as_float(yr[g]), oacc[i][g]);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->o_free[os]);
+        // O is read and written in chunks of OCH columns (heads)
+        constexpr int OCH = NPAD < 32 ? NPAD : 32;
+        auto o_ld = [&](uint32_t ta, uint32_t* r) {
+            if constexpr (OCH == 16)
+                tmem_ld16(ta, r);
+            else
+                tmem_ld32(ta, r);
+            tmem_ld_wait();
+            fence_regs<OCH>(r);
         };
+        auto o_st = [&](uint32_t ta, const uint32_t* r) {
+            if constexpr (OCH == 16)
+                tmem_st16(ta, r);
+            else
+                tmem_st32(ta, r);
+        };
+        float lpart[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) lpart[g] = 0.f;
+        int comp = 0, cur = 1;  // mrf[cur]: the reference max as of the last tile
+        unsigned long long nskip = 0;
 
         for (int j = 0; j < n; ++j) {
             const int ss = j % NS, q = j & 1, qp = q ^ 1;
@@ -485,8 +472,10 @@ __global__ void __launch_bounds__(256, 1)
             auto load_scores = [&](uint32_t* xr) {
                 if constexpr (NPAD == 16)
                     tmem_ld16(tl + ss * NPAD, xr);
-                else
+                else if constexpr (NPAD == 32)
                     tmem_ld32(tl + ss * NPAD, xr);
+                else
+                    tmem_ld64(tl + ss * NPAD, xr);
                 tmem_ld_wait();
                 fence_regs<NPAD>(xr);
             };
@@ -518,8 +507,12 @@ __global__ void __launch_bounds__(256, 1)
                         v[0] = fmaxf(v[0], __shfl_xor_sync(0xffffffffu, v[0], o));
                     }
                 }
-                constexpr int kLow = 32 / G;  // lanes holding the same head
-                if ((lane & (kLow - 1)) == 0) ctrl->red[q][warp][hl] = v[0];
+                constexpr int kLow = G >= 32 ? 1 : 32 / G;  // lanes holding the same head
+                constexpr int kPer = G > 32 ? G / 32 : 1;    // heads held by one lane
+                if ((lane & (kLow - 1)) == 0) {
+#pragma unroll
+                    for (int r = 0; r < kPer; ++r) ctrl->red[q][warp][hl + r] = v[r];
+                }
             }
             named_bar_sync(1, 128);
             // the decision: thread g judges head g, the barrier takes the AND
@@ -583,30 +576,51 @@ __global__ void __launch_bounds__(256, 1)
                     mr = mn_own;
                 }
                 ctrl->mrf[q][tid] = mr;
-                if (!skip) {
-                    ctrl->alpha[tid] = a;
-                    ctrl->mref_hist[comp % NH][tid] = mr;
-                }
+                if (!skip) ctrl->alpha[tid] = a;
             }
             if (!skip) {
-                named_bar_sync(1, 128);  // alpha, mrf[q] and mref_hist visible
                 cur = q;
-                uint32_t xr[NPAD];
-                load_scores(xr);
                 const volatile float* al = ctrl->alpha;
                 const volatile float* mrv = ctrl->mrf[q];
+                {
+                    // the barrier that publishes alpha, mrf[q] also tells whether any head moved;
+                    // then O (the P.V of the computed tiles so far) is rescaled in TMEM once
+                    // the newest P.V is done
+                    const bool moved = tid < G && reinterpret_cast<volatile float*>(ctrl->alpha)[tid] != 1.f;
+                    if (bar_red_or(1, 128, moved)) {
+#pragma unroll
+                        for (int g = 0; g < G; ++g) {
+                            const float a = al[g];
+                            if (a != 1.f) lpart[g] *= a;
+                        }
+                        if (comp > 0) {
+                            mbar_wait(&ctrl->o_done[(comp - 1) % 8], ((comp - 1) / 8) & 1, wd);
+                            tc_fence_after();
+#pragma unroll 1
+                            for (int i = 0; i < VBLK; ++i) {
+#pragma unroll
+                                for (int h = 0; h < NPAD / OCH; ++h) {
+                                    uint32_t tt[OCH];
+                                    const uint32_t ta = tl + O_COL + i * NPAD + h * OCH;
+                                    o_ld(ta, tt);
+#pragma unroll
+                                    for (int c2 = 0; c2 < OCH; ++c2)
+                                        tt[c2] = __float_as_uint(__uint_as_float(tt[c2]) * al[h * OCH + c2]);
+                                    o_st(ta, tt);
+                                }
+                            }
+                            tmem_st_wait();
+                        }
+                    }
+                }
+                uint32_t xr[NPAD];
+                load_scores(xr);
                 const int pb = comp % NP;
                 if (comp >= NP) mbar_wait(&ctrl->p_free[pb], ((comp / NP) - 1) & 1, wd);
                 uint8_t* pbuf = smem + OFF_P + pb * P_BYTES + (tid >> 6) * (NPAD * 128);
                 const int cw = (tid & 63) >> 3;
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
-                    const float a = al[g];
-                    if (a != 1.f) {
-#pragma unroll
-                        for (int i = 0; i < VBLK; ++i) oacc[i][g] *= a;
-                        lpart[g] *= a;
-                    }
                     const float m = mrv[g];
                     const float mr = m == -CUDART_INF_F ? 0.f : m;
                     const float xg = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
@@ -616,6 +630,7 @@ __global__ void __launch_bounds__(256, 1)
                         (unsigned short)(pack_bf16x2(pv, 0.f) & 0xffffu);
                 }
                 fence_proxy_async_smem();
+                tc_fence_before();  // TMEM-O: the rescaled O is stored before the next P.V
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&ctrl->p_full[pb]);
                 ++comp;
@@ -623,13 +638,11 @@ __global__ void __launch_bounds__(256, 1)
             tc_fence_before();  // the S slot's last read is done
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->s_free[ss]);
-            while (comp - folded > LAG) fold(folded++);
         }
         named_bar_sync(1, 128);
         cur = (n - 1) & 1;  // the last tile's buffer holds every head's final reference max
-        while (folded < comp) fold(folded++);
 
-        // l = sum over the 128 key lanes; O = oacc / l
+        // l = sum over the 128 key lanes; O = (TMEM accumulator) / l
 #pragma unroll
         for (int g = 0; g < G; ++g) {
             float v = lpart[g];
@@ -638,25 +651,52 @@ __global__ void __launch_bounds__(256, 1)
             if (lane == 0) ctrl->lred[warp][g] = v;
         }
         named_bar_sync(1, 128);
+        {
+            // thread g finishes head g (l, lse); then every thread writes its value
+            // columns of every head from the TMEM accumulator
+            if (tid < G) {
+                const volatile float* lr = &ctrl->lred[0][tid];
+                const float l = lr[0] + lr[NPAD] + lr[2 * NPAD] + lr[3 * NPAD];
+                const float mrg = reinterpret_cast<volatile float*>(ctrl->mrf[cur])[tid];
+                const float lse = l > 0.f ? mrg * p.scale + __logf(l) : -CUDART_INF_F;
+                ctrl->inv_l[tid] = l > 0.f ? 1.f / l : 0.f;
+                const long long hq = (long long)b * p.Hq + h0 + tid;
+                if (p.S == 1) {
+                    if (p.lse) p.lse[hq] = lse;
+                } else {
+                    p.lse_part[(long long)s * p.B * p.Hq + hq] = lse;
+                }
+            }
+            named_bar_sync(1, 128);
+            if (comp > 0) {
+                mbar_wait(&ctrl->o_done[(comp - 1) % 8], ((comp - 1) / 8) & 1, wd);
+                tc_fence_after();
+            }
+            const volatile float* il = ctrl->inv_l;
+#pragma unroll 1
+            for (int i = 0; i < VBLK; ++i) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const volatile float* lr = &ctrl->lred[0][g];
-            const float l = lr[0] + lr[NPAD] + lr[2 * NPAD] + lr[3 * NPAD];
-            const float inv = l > 0.f ? 1.f / l : 0.f;
-            const float mrg = reinterpret_cast<volatile float*>(ctrl->mrf[cur])[g];
-            const float lse = l > 0.f ? mrg * p.scale + __logf(l) : -CUDART_INF_F;
-            const long long hq = (long long)b * p.Hq + h0 + g;
-            if (p.S == 1) {
+                for (int h = 0; h < NPAD / OCH; ++h) {
+                    uint32_t tt[OCH];
+                    if (comp > 0) {
+                        o_ld(tl + O_COL + i * NPAD + h * OCH, tt);
+                    } else {
 #pragma unroll
-                for (int i = 0; i < VBLK; ++i)
-                    reinterpret_cast<unsigned short*>(p.o)[hq * DV + i * 128 + tid] =
-                        (unsigned short)(pack_bf16x2(oacc[i][g] * inv, 0.f) & 0xffffu);
-                if (tid == 0 && p.lse) p.lse[hq] = lse;
-            } else {
-                const long long ps = (long long)s * p.B * p.Hq + hq;
+                        for (int c2 = 0; c2 < OCH; ++c2) tt[c2] = 0u;
+                    }
 #pragma unroll
-                for (int i = 0; i < VBLK; ++i) p.o_part[ps * DV + i * 128 + tid] = oacc[i][g] * inv;
-                if (tid == 0) p.lse_part[ps] = lse;
+                    for (int c2 = 0; c2 < OCH; ++c2) {
+                        const int g = h * OCH + c2;
+                        if (g >= G) continue;
+                        const float v = __uint_as_float(tt[c2]) * il[g];
+                        const long long hq = (long long)b * p.Hq + h0 + g;
+                        if (p.S == 1)
+                            reinterpret_cast<unsigned short*>(p.o)[hq * DV + i * 128 + tid] =
+                                (unsigned short)(pack_bf16x2(v, 0.f) & 0xffffu);
+                        else
+                            p.o_part[((long long)s * p.B * p.Hq + hq) * DV + i * 128 + tid] = v;
+                    }
+                }
             }
         }
         if (tid == 0 && p.skipped && nskip) atomicAdd(p.skipped, nskip);
@@ -675,7 +715,7 @@ __global__ void __launch_bounds__(256, 1)
 template <int G, bool PAGED, int CG>
 cudaError_t launch_gp(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
     auto kern = mla_decode_kernel<G, PAGED, CG>;
-    constexpr int SMEM = MlaCfg<(G <= 16 ? 16 : 32)>::SMEM;
+    constexpr int SMEM = MlaCfg<(G <= 16 ? 16 : G <= 32 ? 32 : 64)>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -705,7 +745,7 @@ cudaError_t launch_g(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t
 
 }  // namespace
 
-// Hq <= 32: one CTA per (sequence, split); 64, 128: clusters of Hq / 32 CTAs.
+// Hq <= 64: one CTA per (sequence, split); 128: clusters of 2 CTAs of 64 heads.
 cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
     switch (p.Hq) {
         case 1: return launch_g<1, 1>(tkv, p, stream);
@@ -714,8 +754,8 @@ cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cud
         case 8: return launch_g<8, 1>(tkv, p, stream);
         case 16: return launch_g<16, 1>(tkv, p, stream);
         case 32: return launch_g<32, 1>(tkv, p, stream);
-        case 64: return launch_g<32, 2>(tkv, p, stream);
-        case 128: return launch_g<32, 4>(tkv, p, stream);
+        case 64: return launch_g<64, 1>(tkv, p, stream);
+        case 128: return launch_g<64, 2>(tkv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
