@@ -656,9 +656,9 @@ def run_sweep(args):
     # query heads; the cache is read once per row (values = the rows' first 512
     # columns), so the algorithmic bytes are the cache's.  Contiguous, and paged with
     # 64-row pages and 16k-32k rows per sequence.
-    # 32 and 128 heads (one CTA / clusters of 4): queries share a direction and the
+    # 32, 64 and 128 heads (one CTA, one CTA, a pair): queries share a direction and the
     # sinks follow it, so that tiles skipped by all heads exist
-    for ps, Hq in ((0, 16), (0, 8), (64, 16), (0, 32), (0, 128)):
+    for ps, Hq in ((0, 16), (0, 8), (64, 16), (0, 32), (0, 64), (0, 128)):
         lens = None if ps == 0 else torch.randint(16384, 32769, (64,), generator=torch.Generator().manual_seed(3))
         kw = dict(q_shared=6.0, sink_norm=32.0) if Hq > 16 else {}
         a = W.mla_decode(seed=0, B=64, Hq=Hq, L=32768, lens=lens, page_size=ps, device=dev, **kw)
@@ -669,7 +669,7 @@ def run_sweep(args):
             (lambda lam, S: K.mla_decode(a.q, e["kv_pages"], a.scale, lam, S, seq_lens=e["seq_lens"],
                                          page_table=e["page_table"], page_size=ps, max_kv_len=32768))
         base = None
-        for lam in MLA_LAMBDAS if ps == 0 and Hq in (16, 128) else (0.0, MLA_LAMBDAS[2]):
+        for lam in MLA_LAMBDAS if ps == 0 and Hq in (16, 64, 128) else (0.0, MLA_LAMBDAS[2]):
             r = call(lam, 0)
             torch.cuda.synchronize()
             sk = int(r["skipped"].item())
