@@ -141,8 +141,9 @@ size_t blasst_decode_workspace_size(int B, int Hq, int Hkv, int Lkv, int d, int 
 /*
  * Decode forward: one query token per sequence against a KV cache.
  *   q [B, Hq, d], k_cache/v_cache [B, Hkv, Lkv, d], o [B, Hq, d] bf16; lse nullable fp32 [B, Hq].
- *   The skip unit is the G = Hq/Hkv query heads that read one KV head x 128 keys;
- *   G must be <= 16.  V tiles of skipped key tiles are never loaded.
+ *   d is 64 or 128.  The skip unit is the G = Hq/Hkv query heads that read one KV
+ *   head x 128 keys; G must be 1, 2, 4, 8 or 16.  V tiles of skipped key tiles are
+ *   never loaded.
  *   num_splits   S from blasst_decode_num_splits (explicit: the split plan is part
  *                of the result).
  *   workspace    device memory of at least blasst_decode_workspace_size() bytes,

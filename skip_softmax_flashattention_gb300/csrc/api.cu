@@ -306,7 +306,7 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
     const int nT = (Lkv + kTile - 1) / kTile;
     if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
-    if (d != 128) return BLASST_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BLASST_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
@@ -356,7 +356,7 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, blasst::Deco
     p.lse_part = num_splits > 1
                      ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o_bytes + 255) & ~size_t(255)))
                      : nullptr;
-    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Lkv = Lkv; p.G = G; p.nK = nT; p.S = num_splits;
+    p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.Lkv = Lkv; p.G = G; p.nK = nT; p.S = num_splits; p.d = d;
     p.c_log2 = t.c_log2;
     p.scale = scale;
     p.thr_raw = t.thr_raw;
@@ -395,7 +395,7 @@ int blasst_decode_paged(const void* q, const void* k_pages, const void* v_pages,
     const int nT = (max_kv_len + kTile - 1) / kTile;
     if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
-    if (d != 128) return BLASST_ERR_UNSUPPORTED;
+    if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
     if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BLASST_ERR_UNSUPPORTED;
     if (!page_size_ok(page_size)) return BLASST_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_pages) || !aligned16(v_pages) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;

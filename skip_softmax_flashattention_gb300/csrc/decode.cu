@@ -20,6 +20,11 @@
 // Warp roles (224 threads): warps 0-3 softmax, warp 4 K loader, warp 5 MMA issuer
 // and TMEM owner, warp 6 V loader.
 //
+// Head dim 64: the kernel runs at width 128.  The tensor maps have 64 columns, so the
+// second 64-column box of every K and V tile lies outside the tensor and reads as
+// zeros without touching memory; Q is staged with zero padding; only the first 64
+// output columns are written.
+//
 // Paged form (blasst_decode_paged): K and V live in a pool of fixed-size pages and
 // a page table maps each page-sized run of a sequence's keys to a physical page
 // (The Hitchhiker's Guide, Phase 08, Section 3, "Paged Attention": key i of
@@ -311,7 +316,8 @@ __global__ void __launch_bounds__(224, 1)
             for (int c = tid; c < NPAD * (D / 8); c += 128) {
                 const int g = c / (D / 8), ck = c % (D / 8);
                 uint4 v = make_uint4(0, 0, 0, 0);
-                if (g < G) v = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + hk * G + g) * D + ck * 8);
+                if (g < G && ck * 8 < p.d)
+                    v = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + hk * G + g) * p.d + ck * 8);
                 const int half = ck >> 3, cw = ck & 7;
                 *reinterpret_cast<uint4*>(sq + half * (NPAD * 128) + g * 128 + ((cw ^ (g & 7)) << 4)) = v;
             }
@@ -454,12 +460,13 @@ __global__ void __launch_bounds__(224, 1)
             const float lse = l > 0.f ? m_ref[g] * p.scale + __logf(l) : -CUDART_INF_F;
             const long long hq = (long long)b * p.Hq + hk * G + g;
             if (p.S == 1) {
-                reinterpret_cast<unsigned short*>(p.o)[hq * D + tid] =
-                    (unsigned short)(pack_bf16x2(oacc[g] * inv, 0.f) & 0xffffu);
+                if (tid < p.d)
+                    reinterpret_cast<unsigned short*>(p.o)[hq * p.d + tid] =
+                        (unsigned short)(pack_bf16x2(oacc[g] * inv, 0.f) & 0xffffu);
                 if (tid == 0 && p.lse) p.lse[hq] = lse;
             } else {
                 const long long ps = (long long)s * p.B * p.Hq + hq;
-                p.o_part[ps * D + tid] = oacc[g] * inv;
+                if (tid < p.d) p.o_part[ps * p.d + tid] = oacc[g] * inv;
                 if (tid == 0) p.lse_part[ps] = lse;
             }
         }

@@ -58,6 +58,7 @@ struct DecodeParams {
     float* o_part;            // [S,B,Hq,d] (S > 1)
     float* lse_part;          // [S,B,Hq]   (S > 1)
     int B, Hq, Hkv, Lkv, G, nK, S;
+    int d;                    // head dim of q, k, v, o (GQA decode: 64 or 128; the kernel pads to 128)
     float c_log2, scale, thr_raw, lazy_raw;
     unsigned long long* skipped;
     unsigned char* skip_map;  // [B,Hkv,nK] or null

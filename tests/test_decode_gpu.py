@@ -62,3 +62,16 @@ def test_decode_full_size():
         if lam == 0.0:
             assert n == 0
         parity.decode_units_check(a, res, lam, S, units)
+
+
+@pytest.mark.parametrize("shape", [(2, 8, 2, 1000), (1, 16, 1, 777), (3, 4, 4, 129)], ids=str)
+@pytest.mark.parametrize("lam", [0.0, 0.3])
+def test_decode_head_dim_64(shape, lam):
+    """d = 64 runs the width-128 kernel with the upper 64 columns read as zeros."""
+    B, Hq, Hkv, L = shape
+    a = parity.to_gpu(W.decode(seed=23, B=B, Hq=Hq, Hkv=Hkv, Lkv=L, d=64))
+    for S in sorted({1, min(3, -(-L // 128))}):
+        res = K.decode(a.q, a.k, a.v, a.scale, lam, num_splits=S, want_map=True)
+        torch.cuda.synchronize()
+        assert res["o"].shape[-1] == 64
+        parity.decode_full_check(a, res, lam, S)

@@ -112,3 +112,12 @@ def test_paged_serving_batch_sampled():
     for lam in (0.0, 0.3):
         res = _run(a, lam, 0)
         parity.decode_paged_check(a, res, lam, res["num_splits"], seqs=[0, 1, 17, 40, 62, 63])
+
+
+@pytest.mark.parametrize("page_size,token_major", [(16, True), (128, False)])
+def test_paged_head_dim_64(page_size, token_major):
+    a = W.paged_decode(seed=12, B=4, Hq=8, Hkv=2, max_len=1000, d=64, page_size=page_size,
+                       token_major=token_major, lens=[1000, 1, 517, 300], device="cuda")
+    for lam, S in ((0.0, 1), (0.3, 3)):
+        res = _run(a, lam, S)
+        parity.decode_paged_check(a, res, lam, S)
