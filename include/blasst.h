@@ -142,8 +142,9 @@ size_t blasst_decode_workspace_size(int B, int Hq, int Hkv, int Lkv, int d, int 
  * Decode forward: one query token per sequence against a KV cache.
  *   q [B, Hq, d], k_cache/v_cache [B, Hkv, Lkv, d], o [B, Hq, d] bf16; lse nullable fp32 [B, Hq].
  *   d is 64 or 128.  The skip unit is the G = Hq/Hkv query heads that read one KV
- *   head x 128 keys; G must be 1, 2, 4, 8 or 16.  V tiles of skipped key tiles are
- *   never loaded.
+ *   head x 128 keys; G must be 1, 2, 4, 8, 16, 32, 64 or 128 (MQA: Hkv = 1).  Above
+ *   16 the group runs on a wide-group kernel (a cluster of G/64 CTAs at 128).  V tiles
+ *   of skipped key tiles are never loaded.
  *   num_splits   S from blasst_decode_num_splits (explicit: the split plan is part
  *                of the result).
  *   workspace    device memory of at least blasst_decode_workspace_size() bytes,
@@ -174,6 +175,7 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
  *                max_kv_len (NULL: every sequence has max_kv_len keys).  A sequence
  *                of length 0 gives o = 0, lse = -inf.
  *   page_size    8, 16, 32, 64, or a multiple of 128 (else BLASST_ERR_UNSUPPORTED).
+ *   G = Hq/Hkv   1, 2, 4, 8 or 16 in this form (else BLASST_ERR_UNSUPPORTED).
  *   window       0, or a sliding window: only the last `window` keys of each
  *                sequence are attended (keys c >= seq_lens[b] - window).
  *   num_splits   as for blasst_decode, planned on max_kv_len (or on the window when

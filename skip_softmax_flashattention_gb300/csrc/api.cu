@@ -279,7 +279,9 @@ int blasst_decode_num_splits(int B, int Hq, int Hkv, int Lkv, int d, int request
         *out = requested;
         return BLASST_OK;
     }
-    return plan_splits((long long)B * Hkv, nT, out);
+    // G > 64: a cluster of G / 64 CTAs per (sequence, KV head, split)
+    const int G = Hq / Hkv;
+    return plan_splits((long long)B * Hkv * (G > 64 ? G / 64 : 1), nT, out);
 }
 
 size_t blasst_decode_workspace_size(int B, int Hq, int Hkv, int Lkv, int d, int num_splits) {
@@ -307,7 +309,8 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
     if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
     const int G = Hq / Hkv;
     if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
-    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16) return BLASST_ERR_UNSUPPORTED;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16 && G != 32 && G != 64 && G != 128)
+        return BLASST_ERR_UNSUPPORTED;
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
         (reinterpret_cast<uintptr_t>(skipped_tiles_out) & 7u))
@@ -366,7 +369,9 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, blasst::Deco
     p.margins = margins;
     p.status = status;
     p.watchdog_ns = kWatchdogNs;
-    cudaError_t e = blasst::launch_decode(tk, tv, p, d, st);
+    // more than 16 query heads per KV head: the wide-group kernel (contiguous cache)
+    cudaError_t e = (G > 16 && !p.page_table) ? blasst::launch_wide_decode(tk, tv, p, st)
+                                              : blasst::launch_decode(tk, tv, p, d, st);
     if (e != cudaSuccess) return BLASST_ERR_CUDA;
     if (num_splits > 1) {
         blasst::CombineParams c{};

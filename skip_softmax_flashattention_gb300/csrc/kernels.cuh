@@ -101,6 +101,10 @@ cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 // DecodeParams carries Hq = G = the query heads (1, 2, 4, 8 or 16), Hkv = 1, d = kMlaDk.
 constexpr int kMlaDk = 576, kMlaDv = 512;
 cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream);
+// GQA/MQA decode with G = 32, 64 or 128 query heads per KV head (contiguous cache, d 64 or
+// 128), on the MLA kernel's wide-group machinery with separate K and V tensors.
+cudaError_t launch_wide_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                               cudaStream_t stream);
 
 
 }  // namespace blasst

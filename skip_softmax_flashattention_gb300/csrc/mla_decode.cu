@@ -65,10 +65,17 @@ namespace {
 
 constexpr unsigned long long kDrainNs = 1000000000ull;
 
-constexpr int DK = kMlaDk;               // 576
-constexpr int DV = kMlaDv;               // 512
-constexpr int KBOX = DK / 64;            // 64-column boxes per key tile
-constexpr int VBLK = DV / 128;           // 128-column value blocks (box pairs) per key tile
+// Row shapes: MLA reads 576-wide latent rows whose first 512 values are the values;
+// wide-group GQA/MQA reads separate K and V rows of d <= 128 values (run at width 128,
+// the columns past d reading as zeros).
+struct MlaShape {
+    static constexpr int DK = kMlaDk, DV = kMlaDv;
+    static constexpr bool SEPV = false;  // values are the rows' leading DV columns
+};
+struct WideShape {
+    static constexpr int DK = 128, DV = 128;
+    static constexpr bool SEPV = true;   // values come from their own tensor
+};
 constexpr int BOX_BYTES = kTile * 128;   // 128 keys x 64 columns
 constexpr int PAIR_BYTES = 2 * BOX_BYTES;
 constexpr int NS = 4;                    // TMEM S slots
@@ -76,7 +83,6 @@ constexpr int NP = 2;                    // P staging buffers
 constexpr int ND = 8;                    // decision ring
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(NS + 2 <= ND, "ring sizes");
-static_assert(DK % 64 == 0 && DV % 128 == 0 && DV <= DK, "row layout");
 
 // Layout for NPAD heads per CTA (the MMA N: 16, 32, or 64).  Shared memory: NKB key
 // boxes, NVP value pairs, Q, P.  TMEM: NS S slots of NPAD columns, then O (VBLK
@@ -85,11 +91,15 @@ static_assert(DK % 64 == 0 && DV % 128 == 0 && DV <= DK, "row layout");
 // folding it into registers instead measured 4 % slower at 16 heads and 30 % at 32.)
 // More value slots at the cost of key slots measured faster, up to the split used
 // for NPAD = 16.
-template <int NPAD_>
+template <class SH, int NPAD_>
 struct MlaCfg {
     static constexpr int NPAD = NPAD_;
-    static constexpr int NKB = NPAD == 64 ? 3 : 4;   // key box ring
-    static constexpr int NVP = NPAD == 16 ? 4 : NPAD == 32 ? 3 : 2;  // value pair ring
+    static constexpr int KBOX = SH::DK / 64;         // 64-column boxes per key tile
+    static constexpr int VBLK = SH::DV / 128;        // 128-column value blocks (box pairs) per key tile
+    static_assert(SH::DK % 64 == 0 && SH::DV % 128 == 0 && SH::DV <= SH::DK, "row layout");
+    // key box / value pair rings: MLA tiles are 9 boxes + 4 pairs, wide-group tiles 2 + 1
+    static constexpr int NKB = SH::SEPV ? 4 : NPAD == 64 ? 3 : 4;
+    static constexpr int NVP = SH::SEPV ? 3 : NPAD == 16 ? 4 : NPAD == 32 ? 3 : 2;
     static constexpr int Q_BYTES = KBOX * NPAD * 128;
     static constexpr int P_BYTES = 2 * NPAD * 128;   // [key half][NPAD rows][64 keys]
     static constexpr int OFF_K = 0;
@@ -130,11 +140,14 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-template <int G, bool PAGED, int CG>
+template <class SH, int G, bool PAGED, int CG>
 __global__ void __launch_bounds__(256, 1)
-    mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const DecodeParams p) {
-    using C = MlaCfg<(G <= 16 ? 16 : G <= 32 ? 32 : 64)>;
+    mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tv,
+                      const DecodeParams p) {
+    using C = MlaCfg<SH, (G <= 16 ? 16 : G <= 32 ? 32 : 64)>;
+    constexpr int DK = SH::DK, DV = SH::DV, KBOX = C::KBOX, VBLK = C::VBLK;
     constexpr int NPAD = C::NPAD, NKB = C::NKB, NVP = C::NVP, P_BYTES = C::P_BYTES;
+    static_assert(!(PAGED && SH::SEPV), "the paged form is built for latent rows only");
     constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_Q = C::OFF_Q, OFF_P = C::OFF_P;
     constexpr uint32_t O_COL = C::O_COL;
     static_assert(CG == 1 || G == NPAD, "a cluster's CTAs hold NPAD heads each");
@@ -142,9 +155,14 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* smem = align1024(smem_raw);
     auto* ctrl = reinterpret_cast<typename C::Ctrl*>(smem + C::OFF_CTRL);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int s = blockIdx.x / CG, b = blockIdx.z;
+    const int s = blockIdx.x / CG, hk = blockIdx.y, b = blockIdx.z;
+    const int zkv = b * p.Hkv + hk;      // K/V rows of this sequence's KV head
     const uint32_t rank = CG > 1 ? cluster_ctarank() : 0u;
-    const int h0 = (int)rank * NPAD;  // this CTA's first head (CG > 1)
+    // this CTA's first query head: the KV head's group of p.G heads, CTA r of a cluster
+    // holding [r*NPAD, (r+1)*NPAD) of it
+    const int qh0 = hk * p.G + (int)rank * NPAD;
+    const int dq = SH::SEPV ? p.d : DK;  // values per query / key row in memory
+    const int dout = SH::SEPV ? p.d : DV;  // values per output row
     constexpr uint16_t kAll = (uint16_t)((1u << CG) - 1u);
     // This sequence's keys and this split's share of its tiles: [s*nT/S, (s+1)*nT/S).
     int Lb = p.Lkv;
@@ -197,11 +215,11 @@ __global__ void __launch_bounds__(256, 1)
     // does this CTA issue the copies of ring slot k (with CG = 1: always)
     auto issues = [&](int k) -> bool { return CG == 1 || (k % CG) == (int)rank; };
     // a loaded box: this CTA alone, or multicast to the cluster
-    auto load_box = [&](uint8_t* dst, uint64_t* bar, int x, int y) {
+    auto load_box = [&](uint8_t* dst, uint64_t* bar, int x, int y, const CUtensorMap* map) {
         if constexpr (CG == 1)
-            tma_load_3d(dst, &tkv, bar, x, y, b);
+            tma_load_3d(dst, map, bar, x, y, zkv);
         else
-            tma_load_3d_mc(dst, &tkv, bar, x, y, b, kAll);
+            tma_load_3d_mc(dst, map, bar, x, y, zkv, kAll);
     };
     // a slot's release: a commit arriving in this CTA, or in every CTA of the cluster
     auto release = [&](uint64_t* bar) {
@@ -243,7 +261,10 @@ __global__ void __launch_bounds__(256, 1)
         // Box c of tile j is ring entry e = j*KBOX + c, in slot e % NKB.  Its copy goes
         // out once every CTA released the slot's previous entry; the entry's barrier was
         // armed by the S issuer (by the set-up for the first NKB).
-        if (lane == 0) tma_prefetch_desc(&tkv);
+        if (lane == 0) {
+            tma_prefetch_desc(&tkv);
+            if constexpr (SH::SEPV) tma_prefetch_desc(&tv);
+        }
         int last = 0;  // entries passed
         bool ok = true;
         // paged: each lane's page index is read two tiles ahead, so the load's latency
@@ -264,7 +285,7 @@ __global__ void __launch_bounds__(256, 1)
                         if (e >= NKB && !mbar_wait_cluster(&ctrl->k_empty[ks], ((e / NKB) - 1) & 1, wd))
                             go = 0;
                         else if constexpr (!PAGED)
-                            load_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, (t0 + j) * kTile);
+                            load_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, (t0 + j) * kTile, &tkv);
                     }
                     if (!(ok = __shfl_sync(0xffffffffu, go, 0) != 0)) break;
                     if constexpr (PAGED) {
@@ -314,7 +335,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                                 for (int h = 0; h < 2; ++h)
                                     load_box(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
-                                             i * 128 + h * 64, (t0 + j) * kTile);
+                                             i * 128 + h * 64, (t0 + j) * kTile, SH::SEPV ? &tv : &tkv);
                             }
                         }
                     }
@@ -422,7 +443,8 @@ __global__ void __launch_bounds__(256, 1)
             for (int c = tid; c < NPAD * (DK / 8); c += 128) {
                 const int g = c / (DK / 8), ck = c % (DK / 8);
                 uint4 v = make_uint4(0, 0, 0, 0);
-                if (g < G) v = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + h0 + g) * DK + ck * 8);
+                if (g < G && ck * 8 < dq)
+                    v = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + qh0 + g) * dq + ck * 8);
                 const int box = ck >> 3, cw = ck & 7;
                 *reinterpret_cast<uint4*>(sq + box * (NPAD * 128) + g * 128 + ((cw ^ (g & 7)) << 4)) = v;
             }
@@ -432,7 +454,7 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->q_full);
         }
-        const long long mapbase = (long long)b * p.nK;
+        const long long mapbase = (long long)zkv * p.nK;
         const float cl = p.c_log2;
         // Per-head running state common to all 128 threads lives in shared memory, by
         // tile parity: mex (exact running max) and mrf (reference max) of tile j are
@@ -660,7 +682,7 @@ __global__ void __launch_bounds__(256, 1)
                 const float mrg = reinterpret_cast<volatile float*>(ctrl->mrf[cur])[tid];
                 const float lse = l > 0.f ? mrg * p.scale + __logf(l) : -CUDART_INF_F;
                 ctrl->inv_l[tid] = l > 0.f ? 1.f / l : 0.f;
-                const long long hq = (long long)b * p.Hq + h0 + tid;
+                const long long hq = (long long)b * p.Hq + qh0 + tid;
                 if (p.S == 1) {
                     if (p.lse) p.lse[hq] = lse;
                 } else {
@@ -689,12 +711,14 @@ __global__ void __launch_bounds__(256, 1)
                         const int g = h * OCH + c2;
                         if (g >= G) continue;
                         const float v = __uint_as_float(tt[c2]) * il[g];
-                        const long long hq = (long long)b * p.Hq + h0 + g;
+                        const long long hq = (long long)b * p.Hq + qh0 + g;
+                        const int col = i * 128 + tid;
+                        if (col >= dout) continue;
                         if (p.S == 1)
-                            reinterpret_cast<unsigned short*>(p.o)[hq * DV + i * 128 + tid] =
+                            reinterpret_cast<unsigned short*>(p.o)[hq * dout + col] =
                                 (unsigned short)(pack_bf16x2(v, 0.f) & 0xffffu);
                         else
-                            p.o_part[((long long)s * p.B * p.Hq + hq) * DV + i * 128 + tid] = v;
+                            p.o_part[((long long)s * p.B * p.Hq + hq) * dout + col] = v;
                     }
                 }
             }
@@ -712,14 +736,14 @@ __global__ void __launch_bounds__(256, 1)
     if constexpr (CG > 1) cluster_sync_all();  // no CTA leaves while another may still reach it
 }
 
-template <int G, bool PAGED, int CG>
-cudaError_t launch_gp(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
-    auto kern = mla_decode_kernel<G, PAGED, CG>;
-    constexpr int SMEM = MlaCfg<(G <= 16 ? 16 : G <= 32 ? 32 : 64)>::SMEM;
+template <class SH, int G, bool PAGED, int CG>
+cudaError_t launch_gp(const CUtensorMap& tkv, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+    auto kern = mla_decode_kernel<SH, G, PAGED, CG>;
+    constexpr int SMEM = MlaCfg<SH, (G <= 16 ? 16 : G <= 32 ? 32 : 64)>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.S * CG), 1, (unsigned)p.B);
+    cfg.gridDim = dim3((unsigned)(p.S * CG), (unsigned)p.Hkv, (unsigned)p.B);
     cfg.blockDim = dim3(256, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = stream;
@@ -736,11 +760,12 @@ cudaError_t launch_gp(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_
         if (e != cudaSuccess) return e;
         if (nclusters < 1) return cudaErrorInvalidConfiguration;
     }
-    return cudaLaunchKernelEx(&cfg, kern, tkv, p);
+    return cudaLaunchKernelEx(&cfg, kern, tkv, tv, p);
 }
 template <int G, int CG>
 cudaError_t launch_g(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
-    return p.page_table ? launch_gp<G, true, CG>(tkv, p, stream) : launch_gp<G, false, CG>(tkv, p, stream);
+    return p.page_table ? launch_gp<MlaShape, G, true, CG>(tkv, tkv, p, stream)
+                        : launch_gp<MlaShape, G, false, CG>(tkv, tkv, p, stream);
 }
 
 }  // namespace
@@ -756,6 +781,17 @@ cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cud
         case 32: return launch_g<32, 1>(tkv, p, stream);
         case 64: return launch_g<64, 1>(tkv, p, stream);
         case 128: return launch_g<64, 2>(tkv, p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// GQA/MQA decode with G = 32, 64 or 128 query heads per KV head (contiguous cache).
+cudaError_t launch_wide_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
+                               cudaStream_t stream) {
+    switch (p.G) {
+        case 32: return launch_gp<WideShape, 32, false, 1>(tk, tv, p, stream);
+        case 64: return launch_gp<WideShape, 64, false, 1>(tk, tv, p, stream);
+        case 128: return launch_gp<WideShape, 64, false, 2>(tk, tv, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

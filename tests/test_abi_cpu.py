@@ -114,7 +114,8 @@ def test_prefill_validation(kw, code):
     (dict(lam=2.0), K.BLASST_ERR_INVALID_ARG),
     (dict(d=96), K.BLASST_ERR_UNSUPPORTED),
     (dict(Hq=24, Hkv=8), K.BLASST_ERR_UNSUPPORTED),
-    (dict(Hq=64, Hkv=2), K.BLASST_ERR_UNSUPPORTED),
+    (dict(Hq=96, Hkv=2), K.BLASST_ERR_UNSUPPORTED),   # G = 48
+    (dict(Hq=512, Hkv=2), K.BLASST_ERR_UNSUPPORTED),  # G = 256
     (dict(S=2, ws=None, wsb=0), K.BLASST_ERR_INVALID_ARG),
     (dict(S=2, wsb=16), K.BLASST_ERR_WORKSPACE_TOO_SMALL),
 ])
@@ -136,6 +137,7 @@ def test_decode_validation(kw, code):
     (dict(ps=24, mp=42), K.BLASST_ERR_UNSUPPORTED),  # neither a divisor nor a multiple of 128
     (dict(ps=200, mp=5), K.BLASST_ERR_UNSUPPORTED),
     (dict(d=96), K.BLASST_ERR_UNSUPPORTED),
+    (dict(Hq=64, Hkv=2), K.BLASST_ERR_UNSUPPORTED),  # G = 32: the paged form holds up to 16
     (dict(table=FAKE + 2), K.BLASST_ERR_UNSUPPORTED),
     (dict(S=2, wsb=16), K.BLASST_ERR_WORKSPACE_TOO_SMALL),
     (dict(win=-1), K.BLASST_ERR_INVALID_ARG),

@@ -75,3 +75,39 @@ def test_decode_head_dim_64(shape, lam):
         torch.cuda.synchronize()
         assert res["o"].shape[-1] == 64
         parity.decode_full_check(a, res, lam, S)
+
+
+# More than 16 query heads per KV head (MQA and wide GQA): the wide-group kernel,
+# 32 / 64 heads in one CTA, 128 in a cluster of two.
+WIDE = [
+    # B, Hq, Hkv, Lkv, d
+    (2, 32, 1, 1000, 128),
+    (1, 64, 1, 777, 64),
+    (2, 64, 2, 1500, 128),
+    (1, 128, 1, 600, 128),
+    (2, 128, 2, 300, 64),
+]
+
+
+@pytest.mark.parametrize("shape", WIDE, ids=[str(s) for s in WIDE])
+@pytest.mark.parametrize("lam", [0.0, 0.3])
+def test_decode_wide_groups(shape, lam):
+    B, Hq, Hkv, L, d = shape
+    a = parity.to_gpu(W.decode(seed=29, B=B, Hq=Hq, Hkv=Hkv, Lkv=L, d=d))
+    for S in sorted({1, min(3, -(-L // 128))}):
+        res = K.decode(a.q, a.k, a.v, a.scale, lam, num_splits=S, want_map=True)
+        torch.cuda.synchronize()
+        assert res["o"].shape == (B, Hq, d)
+        parity.decode_full_check(a, res, lam, S)
+
+
+def test_decode_wide_group_full_size_sampled():
+    """64 sequences x 32768 keys, one KV head read by 64 query heads (MQA), the
+    library's split plan: two sequences against the oracle."""
+    a = parity.to_gpu(W.decode(seed=30, B=64, Hq=64, Hkv=1, Lkv=32768, d=128))
+    for lam in (0.0, 0.3):
+        res = K.decode(a.q, a.k, a.v, a.scale, lam, want_map=True)
+        torch.cuda.synchronize()
+        parity.decode_units_check(a, res, lam, res["num_splits"], [(0, 0), (63, 0)])
+    del a, res
+    torch.cuda.empty_cache()
