@@ -36,16 +36,21 @@
 //
 // Up to 16 heads the MMA N is 16, up to 32 it is 32, up to 64 it is 64.  128 heads: a
 // cluster of CG = 2 CTAs runs each (sequence, split), CTA r holding heads
-// [64r, 64r + 64).  The CTAs of a cluster read the same rows,
-// so each key box and value pair is loaded once and multicast to all of them (the
-// entries of ring slot k are issued by CTA k mod CG); a slot is refilled once every
-// CTA's MMAs have released it (each MMA commit arrives on the slot's barrier in
-// every CTA), and only onto barriers every CTA has armed: key slots are armed by
-// each CTA's S issuer one ring ahead, value slots by each CTA's value loader, which
-// tells the issuing CTA.  So every copy into a CTA is one it waits for before it
-// exits, also when a wait gives up.  The tile's decision covers all Hq heads: every CTA sends its vote
-// and margin to every other through distributed shared memory, and each takes the
-// AND of the CG votes.
+// [64r, 64r + 64).  The CTAs of a cluster read the same rows, so each key box and
+// value pair is loaded once and multicast to all of them (the entries of ring slot k
+// are issued by CTA k mod CG); a slot is refilled once every CTA's MMAs have released
+// it (each MMA commit arrives on the slot's barrier in every CTA), and only onto
+// barriers every CTA has armed: key slots are armed by each CTA's S issuer one ring
+// ahead, value slots by each CTA's value loader, which tells the issuing CTA.  So
+// every copy into a CTA is one it waits for before it exits, also when a wait gives
+// up.  The tile's decision covers all the heads: every CTA sends its vote and margin
+// to every other through distributed shared memory, and each takes the AND of the CG
+// votes.
+//
+// The same kernel serves GQA/MQA decode with 32-128 query heads per KV head
+// (WideShape): K and V are separate tensors of d <= 128 values per row, run at width
+// 128 (a 64-wide tensor's second column box lies outside it and reads as zeros), one
+// CTA (or cluster) per (sequence, KV head, split).
 //
 // Paged form: the cache is a pool of pages of page_size rows and a page table maps
 // each page-sized run of a sequence's keys to a page (The Hitchhiker's Guide, Phase
@@ -79,7 +84,6 @@ struct WideShape {
 constexpr int BOX_BYTES = kTile * 128;   // 128 keys x 64 columns
 constexpr int PAIR_BYTES = 2 * BOX_BYTES;
 constexpr int NS = 4;                    // TMEM S slots
-constexpr int NP = 2;                    // P staging buffers
 constexpr int ND = 8;                    // decision ring
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(NS + 2 <= ND, "ring sizes");
@@ -100,6 +104,7 @@ struct MlaCfg {
     // key box / value pair rings: MLA tiles are 9 boxes + 4 pairs, wide-group tiles 2 + 1
     static constexpr int NKB = SH::SEPV ? 4 : NPAD == 64 ? 3 : 4;
     static constexpr int NVP = SH::SEPV ? 3 : NPAD == 16 ? 4 : NPAD == 32 ? 3 : 2;
+    static constexpr int NP = 2;                     // P staging buffers
     static constexpr int Q_BYTES = KBOX * NPAD * 128;
     static constexpr int P_BYTES = 2 * NPAD * 128;   // [key half][NPAD rows][64 keys]
     static constexpr int OFF_K = 0;
@@ -146,7 +151,7 @@ __global__ void __launch_bounds__(256, 1)
                       const DecodeParams p) {
     using C = MlaCfg<SH, (G <= 16 ? 16 : G <= 32 ? 32 : 64)>;
     constexpr int DK = SH::DK, DV = SH::DV, KBOX = C::KBOX, VBLK = C::VBLK;
-    constexpr int NPAD = C::NPAD, NKB = C::NKB, NVP = C::NVP, P_BYTES = C::P_BYTES;
+    constexpr int NPAD = C::NPAD, NKB = C::NKB, NVP = C::NVP, NP = C::NP, P_BYTES = C::P_BYTES;
     static_assert(!(PAGED && SH::SEPV), "the paged form is built for latent rows only");
     constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_Q = C::OFF_Q, OFF_P = C::OFF_P;
     constexpr uint32_t O_COL = C::O_COL;
