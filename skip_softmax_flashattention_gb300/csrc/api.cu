@@ -105,6 +105,21 @@ bool encode_pages(CUtensorMap* map, const void* base, int d, int page_size, int 
     return r == CUDA_SUCCESS;
 }
 
+// Queries [B][H][d] bf16 as a 3-D tensor, boxes of 64 columns x `rows` heads of one
+// sequence; heads past H and columns past d read as zeros.
+bool encode_heads(CUtensorMap* map, const void* base, int d, int H, int B, int rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)B};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 bool lambda_ok(float lambda) { return std::isfinite(lambda) && lambda >= 0.f && lambda <= 1.f; }
@@ -370,8 +385,14 @@ static int run_decode(const CUtensorMap& tk, const CUtensorMap& tv, blasst::Deco
     p.status = status;
     p.watchdog_ns = kWatchdogNs;
     // more than 16 query heads per KV head: the wide-group kernel (contiguous cache)
-    cudaError_t e = (G > 16 && !p.page_table) ? blasst::launch_wide_decode(tk, tv, p, st)
-                                              : blasst::launch_decode(tk, tv, p, d, st);
+    cudaError_t e;
+    if (G > 16 && !p.page_table) {
+        CUtensorMap tq;
+        if (!encode_heads(&tq, q, d, Hq, B, blasst::mla_heads_per_cta(G))) return BLASST_ERR_CUDA;
+        e = blasst::launch_wide_decode(tk, tv, tq, p, st);
+    } else {
+        e = blasst::launch_decode(tk, tv, p, d, st);
+    }
     if (e != cudaSuccess) return BLASST_ERR_CUDA;
     if (num_splits > 1) {
         blasst::CombineParams c{};
@@ -479,12 +500,13 @@ int blasst_mla_decode(const void* q, const void* kv, const int* page_table, cons
         if (workspace_bytes < need) return BLASST_ERR_WORKSPACE_TOO_SMALL;
         if (!aligned16(workspace)) return BLASST_ERR_UNSUPPORTED;
     }
-    CUtensorMap tkv;
+    CUtensorMap tkv, tq;
     const int rows = page_size < kTile ? page_size : kTile;
     if (page_table && (long long)num_pages * page_size > 0x7fffffffLL - kTile) return BLASST_ERR_UNSUPPORTED;
     if (page_table ? !encode_rows(&tkv, kv, dk, (long long)num_pages * page_size, rows)
                    : !encode_3d(&tkv, kv, dk, max_kv_len, B))
         return BLASST_ERR_CUDA;
+    if (!encode_heads(&tq, q, dk, Hq, B, blasst::mla_heads_per_cta(Hq > 64 ? 64 : Hq))) return BLASST_ERR_CUDA;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int* status = status_word();
@@ -523,7 +545,7 @@ int blasst_mla_decode(const void* q, const void* kv, const int* page_table, cons
     p.page_size = page_size;
     p.rows_per_box = rows;
     p.token_major = 1;
-    cudaError_t e = blasst::launch_mla_decode(tkv, p, st);
+    cudaError_t e = blasst::launch_mla_decode(tkv, tq, p, st);
     if (e != cudaSuccess) return BLASST_ERR_CUDA;
     if (num_splits > 1) {
         blasst::CombineParams c{};

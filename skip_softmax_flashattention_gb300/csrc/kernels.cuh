@@ -98,13 +98,18 @@ cudaError_t launch_decode(const CUtensorMap& tk, const CUtensorMap& tv, const De
                           cudaStream_t stream);
 cudaError_t launch_combine(const CombineParams& p, cudaStream_t stream);
 // MLA decode (absorbed form): rows of kMlaDk values, values = their first kMlaDv.
-// DecodeParams carries Hq = G = the query heads (1, 2, 4, 8 or 16), Hkv = 1, d = kMlaDk.
+// DecodeParams carries Hq = G = the query heads (1-128), Hkv = 1, d = kMlaDk.
 constexpr int kMlaDk = 576, kMlaDv = 512;
-cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream);
+// Query heads one CTA of the MLA / wide-group kernel holds (the MMA N) for G heads per
+// KV head; the query tensor map's boxes are this many rows high.
+__host__ __device__ constexpr int mla_heads_per_cta(int G) { return G <= 16 ? 16 : G <= 32 ? 32 : 64; }
+// tq: the queries [B][Hq][d] as a 3-D map, boxes of 64 columns x mla_heads_per_cta(G) heads.
+cudaError_t launch_mla_decode(const CUtensorMap& tkv, const CUtensorMap& tq, const DecodeParams& p,
+                              cudaStream_t stream);
 // GQA/MQA decode with G = 32, 64 or 128 query heads per KV head (contiguous cache, d 64 or
 // 128), on the MLA kernel's wide-group machinery with separate K and V tensors.
-cudaError_t launch_wide_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                               cudaStream_t stream);
+cudaError_t launch_wide_decode(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                               const DecodeParams& p, cudaStream_t stream);
 
 
 }  // namespace blasst

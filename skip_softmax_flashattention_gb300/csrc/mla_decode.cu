@@ -88,25 +88,31 @@ constexpr int ND = 8;                    // decision ring
 constexpr uint32_t TMEM_COLS = 512;
 static_assert(NS + 2 <= ND, "ring sizes");
 
-// Layout for NPAD heads per CTA (the MMA N: 16, 32, or 64).  Shared memory: NKB key
-// boxes, NVP value pairs, Q, P.  TMEM: NS S slots of NPAD columns, then O (VBLK
-// blocks of NPAD columns), one accumulator over the computed tiles, rescaled in
-// place when a head's reference max moves.  (Landing each P.V in a fresh slot and
-// folding it into registers instead measured 4 % slower at 16 heads and 30 % at 32.)
-// More value slots at the cost of key slots measured faster, up to the split used
-// for NPAD = 16.
-template <class SH, int NPAD_>
+// Layout for NPAD heads per CTA (the MMA N: 16, 32, or 64) in clusters of CG CTAs.
+// Shared memory: NKB key boxes, NVP value pairs, Q, NP P buffers.  TMEM: NS S slots of
+// NPAD columns, then O (VBLK blocks of NPAD columns), one accumulator over the
+// computed tiles, rescaled in place when a head's reference max moves.  (Landing each
+// P.V in a fresh slot and folding it into registers instead measured 4 % slower at 16
+// heads and 30 % at 32.)  More value slots at the cost of key slots measured faster,
+// up to the split used for NPAD = 16.  At 64 heads Q takes 72 KB: a lone CTA keeps one
+// P buffer and four key boxes in flight (the key stream paces it); a cluster CTA,
+// whose key ring is shared, keeps two P buffers and three key boxes.
+template <class SH, int NPAD_, int CG>
 struct MlaCfg {
     static constexpr int NPAD = NPAD_;
     static constexpr int KBOX = SH::DK / 64;         // 64-column boxes per key tile
     static constexpr int VBLK = SH::DV / 128;        // 128-column value blocks (box pairs) per key tile
     static_assert(SH::DK % 64 == 0 && SH::DV % 128 == 0 && SH::DV <= SH::DK, "row layout");
     // key box / value pair rings: MLA tiles are 9 boxes + 4 pairs, wide-group tiles 2 + 1
-    static constexpr int NKB = SH::SEPV ? 4 : NPAD == 64 ? 3 : 4;
+    static constexpr int NKB = SH::SEPV ? 4 : (NPAD == 64 && CG > 1) ? 3 : 4;
     static constexpr int NVP = SH::SEPV ? 3 : NPAD == 16 ? 4 : NPAD == 32 ? 3 : 2;
-    static constexpr int NP = 2;                     // P staging buffers
+    static constexpr int NP = (!SH::SEPV && NPAD == 64 && CG == 1) ? 1 : 2;  // P staging buffers
     static constexpr int Q_BYTES = KBOX * NPAD * 128;
-    static constexpr int P_BYTES = 2 * NPAD * 128;   // [key half][NPAD rows][64 keys]
+    // P^T is the B operand of the P.V MMAs.  64 heads: MN-major, [128 keys][64 heads], so
+    // each thread stores its key's row in 16-byte pieces; fewer: K-major, [key half][NPAD
+    // heads][64 keys].
+    static constexpr bool MNP = NPAD == 64;
+    static constexpr int P_BYTES = 2 * NPAD * 128;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + NKB * BOX_BYTES;
     static constexpr int OFF_Q = OFF_V + NVP * PAIR_BYTES;
@@ -127,6 +133,7 @@ struct MlaCfg {
         float mex[2][NPAD];         // exact running max per head, by tile parity
         float mrf[2][NPAD];         // reference max per head, by tile parity
         float alpha[NPAD];          // this tile's rescale factor per head
+        alignas(16) float nmc[NPAD];  // -(reference max) * c_log2 per head for this tile's P
         float gmar[NPAD];           // this tile's margin per head
         float lred[4][NPAD];
         float inv_l[NPAD];          // 1 / l per head for the outputs
@@ -148,9 +155,9 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 template <class SH, int G, bool PAGED, int CG>
 __global__ void __launch_bounds__(256, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tv,
-                      const DecodeParams p) {
-    using C = MlaCfg<SH, (G <= 16 ? 16 : G <= 32 ? 32 : 64)>;
-    constexpr int DK = SH::DK, DV = SH::DV, KBOX = C::KBOX, VBLK = C::VBLK;
+                      const __grid_constant__ CUtensorMap tq, const DecodeParams p) {
+    using C = MlaCfg<SH, mla_heads_per_cta(G), CG>;
+    constexpr int DV = SH::DV, KBOX = C::KBOX, VBLK = C::VBLK;
     constexpr int NPAD = C::NPAD, NKB = C::NKB, NVP = C::NVP, NP = C::NP, P_BYTES = C::P_BYTES;
     static_assert(!(PAGED && SH::SEPV), "the paged form is built for latent rows only");
     constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_Q = C::OFF_Q, OFF_P = C::OFF_P;
@@ -166,7 +173,6 @@ __global__ void __launch_bounds__(256, 1)
     // this CTA's first query head: the KV head's group of p.G heads, CTA r of a cluster
     // holding [r*NPAD, (r+1)*NPAD) of it
     const int qh0 = hk * p.G + (int)rank * NPAD;
-    const int dq = SH::SEPV ? p.d : DK;  // values per query / key row in memory
     const int dout = SH::SEPV ? p.d : DV;  // values per output row
     constexpr uint16_t kAll = (uint16_t)((1u << CG) - 1u);
     // This sequence's keys and this split's share of its tiles: [s*nT/S, (s+1)*nT/S).
@@ -198,7 +204,7 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = 0; i < 8; ++i) mbar_init(&ctrl->o_done[i], 1);
         for (int g = 0; g < NPAD; ++g)
             for (int q = 0; q < 2; ++q) ctrl->mex[q][g] = ctrl->mrf[q][g] = -CUDART_INF_F;
-        mbar_init(&ctrl->q_full, 4);
+        mbar_init(&ctrl->q_full, 1);
         mbar_init(&ctrl->drain[0], 1);
         mbar_init(&ctrl->drain[1], 1);
         ctrl->abort = 0;
@@ -267,6 +273,11 @@ __global__ void __launch_bounds__(256, 1)
         // out once every CTA released the slot's previous entry; the entry's barrier was
         // armed by the S issuer (by the set-up for the first NKB).
         if (lane == 0) {
+            // this CTA's query heads, KBOX boxes of 64 columns x NPAD heads (heads past
+            // Hq and columns past the row width read as zeros)
+            mbar_arrive_expect_tx(&ctrl->q_full, C::Q_BYTES);
+            for (int c = 0; c < KBOX; ++c)
+                tma_load_3d(smem + OFF_Q + c * (NPAD * 128), &tq, &ctrl->q_full, c * 64, qh0, b);
             tma_prefetch_desc(&tkv);
             if constexpr (SH::SEPV) tma_prefetch_desc(&tv);
         }
@@ -374,6 +385,7 @@ __global__ void __launch_bounds__(256, 1)
             const int total = n * KBOX;
             int armed = min(NKB, total), consumed = 0;
             bool ok = mbar_wait(&ctrl->q_full, 0, wd);
+            if (!ok) mbar_wait_drain(&ctrl->q_full, 0, kDrainNs);  // the Q copy lands before the CTA exits
             for (int j = 0; j < n && ok; ++j) {
                 const int ss = j % NS;
                 if (j >= NS && !(ok = mbar_wait(&ctrl->s_free[ss], ((j / NS) - 1) & 1, wd))) break;
@@ -404,7 +416,7 @@ __global__ void __launch_bounds__(256, 1)
     } else if (warp == 7) {
         // ------------------------------------------------------------ P.V issuer
         if (lane == 0) {
-            constexpr uint32_t kIdescO = idesc_bf16(128, NPAD, true, false);
+            constexpr uint32_t kIdescO = idesc_bf16(128, NPAD, true, C::MNP);
             const uint32_t sV = smem_u32(smem + OFF_V), sP = smem_u32(smem + OFF_P);
             bool ok = true;
             int comp = 0;
@@ -424,7 +436,9 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                     for (int kk = 0; kk < kTile / 16; ++kk) {
                         const uint64_t adesc = desc_mnmajor_sw128(vb + kk * 2048, BOX_BYTES);
-                        const uint64_t bdesc = desc_kmajor_sw128(pbuf + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32);
+                        const uint64_t bdesc =
+                            C::MNP ? desc_mnmajor_sw128(pbuf + kk * 2048, P_BYTES)
+                                   : desc_kmajor_sw128(pbuf + (kk >> 2) * (NPAD * 128) + (kk & 3) * 32);
                         // O accumulates over the computed tiles
                         const uint32_t acc = (kk > 0 || comp > 0) ? 1u : 0u;
                         mma_ss(tmem + O_COL + i * NPAD, adesc, bdesc, kIdescO, acc);
@@ -442,22 +456,11 @@ __global__ void __launch_bounds__(256, 1)
     } else {
         // ------------------------------------------------------------ softmax (warps 0-3)
         const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-        // Stage Q (rows = heads, zero-padded to 16) and clear the P buffers' padding rows.
-        {
-            uint8_t* sq = smem + OFF_Q;
-            for (int c = tid; c < NPAD * (DK / 8); c += 128) {
-                const int g = c / (DK / 8), ck = c % (DK / 8);
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (g < G && ck * 8 < dq)
-                    v = *reinterpret_cast<const uint4*>(p.q + ((long long)b * p.Hq + qh0 + g) * dq + ck * 8);
-                const int box = ck >> 3, cw = ck & 7;
-                *reinterpret_cast<uint4*>(sq + box * (NPAD * 128) + g * 128 + ((cw ^ (g & 7)) << 4)) = v;
-            }
+        // Clear the P buffers' padding rows (heads past G); the fence before each P
+        // arrival makes the zeros visible to the MMAs.
+        if constexpr (!C::MNP) {
             uint4* sp = reinterpret_cast<uint4*>(smem + OFF_P);
             for (int c = tid; c < NP * P_BYTES / 16; c += 128) sp[c] = make_uint4(0, 0, 0, 0);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ctrl->q_full);
         }
         const long long mapbase = (long long)zkv * p.nK;
         const float cl = p.c_log2;
@@ -556,7 +559,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             bool skip = bar_red_and(1, 128, vote);
             float margin = -CUDART_INF_F;
-            if (tid == 0)
+            if (tid == 0 && p.margins)
                 for (int g = 0; g < G; ++g) margin = fmaxf(margin, reinterpret_cast<volatile float*>(ctrl->gmar)[g]);
             if constexpr (CG > 1) {
                 // The decision covers the heads of every CTA of the cluster: send this
@@ -603,12 +606,14 @@ __global__ void __launch_bounds__(256, 1)
                     mr = mn_own;
                 }
                 ctrl->mrf[q][tid] = mr;
-                if (!skip) ctrl->alpha[tid] = a;
+                if (!skip) {
+                    ctrl->alpha[tid] = a;
+                    ctrl->nmc[tid] = -((mr == -CUDART_INF_F ? 0.f : mr) * cl);
+                }
             }
             if (!skip) {
                 cur = q;
                 const volatile float* al = ctrl->alpha;
-                const volatile float* mrv = ctrl->mrf[q];
                 {
                     // the barrier that publishes alpha, mrf[q] also tells whether any head moved;
                     // then O (the P.V of the computed tiles so far) is rescaled in TMEM once
@@ -642,19 +647,55 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 uint32_t xr[NPAD];
                 load_scores(xr);
+                // p = 2^(s*c - m_ref*c) for every head, in place, before any store, so that
+                // the loads of the per-head constants are free to run ahead
+                const float* nm = ctrl->nmc;  // published by the barrier above
+                if constexpr (G >= 4) {
+#pragma unroll
+                    for (int g = 0; g < G; g += 4) {
+                        const float4 n4 = *reinterpret_cast<const float4*>(nm + g);
+                        float x[4], a[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) x[i] = key_ok ? __uint_as_float(xr[g + i]) : -CUDART_INF_F;
+                        ffma2v(a[0], a[1], x[0], x[1], cl, n4.x, n4.y);
+                        ffma2v(a[2], a[3], x[2], x[3], cl, n4.z, n4.w);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) a[i] = ex2(a[i]);
+                        fadd2_acc(lpart[g], lpart[g + 1], a[0], a[1]);
+                        fadd2_acc(lpart[g + 2], lpart[g + 3], a[2], a[3]);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) xr[g + i] = __float_as_uint(a[i]);
+                    }
+                } else {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) {
+                        const float xg = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
+                        const float pv = ex2(fmaf(xg, cl, nm[g]));
+                        lpart[g] += pv;
+                        xr[g] = __float_as_uint(pv);
+                    }
+                }
                 const int pb = comp % NP;
                 if (comp >= NP) mbar_wait(&ctrl->p_free[pb], ((comp / NP) - 1) & 1, wd);
-                uint8_t* pbuf = smem + OFF_P + pb * P_BYTES + (tid >> 6) * (NPAD * 128);
-                const int cw = (tid & 63) >> 3;
+                if constexpr (C::MNP) {
+                    // this key's row of 64 heads, eight 16-byte pieces, 128-byte swizzle
+                    uint8_t* prow = smem + OFF_P + pb * P_BYTES + tid * 128;
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float m = mrv[g];
-                    const float mr = m == -CUDART_INF_F ? 0.f : m;
-                    const float xg = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
-                    const float pv = ex2(fmaf(xg, cl, -mr * cl));
-                    lpart[g] += pv;
-                    *reinterpret_cast<unsigned short*>(pbuf + g * 128 + ((cw ^ (g & 7)) << 4) + (tid & 7) * 2) =
-                        (unsigned short)(pack_bf16x2(pv, 0.f) & 0xffffu);
+                    for (int c = 0; c < 8; ++c) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(xr[8 * c + 0]), __uint_as_float(xr[8 * c + 1]));
+                        w.y = pack_bf16x2(__uint_as_float(xr[8 * c + 2]), __uint_as_float(xr[8 * c + 3]));
+                        w.z = pack_bf16x2(__uint_as_float(xr[8 * c + 4]), __uint_as_float(xr[8 * c + 5]));
+                        w.w = pack_bf16x2(__uint_as_float(xr[8 * c + 6]), __uint_as_float(xr[8 * c + 7]));
+                        *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = w;
+                    }
+                } else {
+                    uint8_t* pbuf = smem + OFF_P + pb * P_BYTES + (tid >> 6) * (NPAD * 128);
+                    const int cw = (tid & 63) >> 3;
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+                        *reinterpret_cast<unsigned short*>(pbuf + g * 128 + ((cw ^ (g & 7)) << 4) + (tid & 7) * 2) =
+                            (unsigned short)(pack_bf16x2(__uint_as_float(xr[g]), 0.f) & 0xffffu);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();  // TMEM-O: the rescaled O is stored before the next P.V
@@ -742,9 +783,10 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 template <class SH, int G, bool PAGED, int CG>
-cudaError_t launch_gp(const CUtensorMap& tkv, const CUtensorMap& tv, const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_gp(const CUtensorMap& tkv, const CUtensorMap& tv, const CUtensorMap& tq, const DecodeParams& p,
+                      cudaStream_t stream) {
     auto kern = mla_decode_kernel<SH, G, PAGED, CG>;
-    constexpr int SMEM = MlaCfg<SH, (G <= 16 ? 16 : G <= 32 ? 32 : 64)>::SMEM;
+    constexpr int SMEM = MlaCfg<SH, mla_heads_per_cta(G), CG>::SMEM;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -765,38 +807,39 @@ cudaError_t launch_gp(const CUtensorMap& tkv, const CUtensorMap& tv, const Decod
         if (e != cudaSuccess) return e;
         if (nclusters < 1) return cudaErrorInvalidConfiguration;
     }
-    return cudaLaunchKernelEx(&cfg, kern, tkv, tv, p);
+    return cudaLaunchKernelEx(&cfg, kern, tkv, tv, tq, p);
 }
 template <int G, int CG>
-cudaError_t launch_g(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
-    return p.page_table ? launch_gp<MlaShape, G, true, CG>(tkv, tkv, p, stream)
-                        : launch_gp<MlaShape, G, false, CG>(tkv, tkv, p, stream);
+cudaError_t launch_g(const CUtensorMap& tkv, const CUtensorMap& tq, const DecodeParams& p, cudaStream_t stream) {
+    return p.page_table ? launch_gp<MlaShape, G, true, CG>(tkv, tkv, tq, p, stream)
+                        : launch_gp<MlaShape, G, false, CG>(tkv, tkv, tq, p, stream);
 }
 
 }  // namespace
 
 // Hq <= 64: one CTA per (sequence, split); 128: clusters of 2 CTAs of 64 heads.
-cudaError_t launch_mla_decode(const CUtensorMap& tkv, const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_mla_decode(const CUtensorMap& tkv, const CUtensorMap& tq, const DecodeParams& p,
+                              cudaStream_t stream) {
     switch (p.Hq) {
-        case 1: return launch_g<1, 1>(tkv, p, stream);
-        case 2: return launch_g<2, 1>(tkv, p, stream);
-        case 4: return launch_g<4, 1>(tkv, p, stream);
-        case 8: return launch_g<8, 1>(tkv, p, stream);
-        case 16: return launch_g<16, 1>(tkv, p, stream);
-        case 32: return launch_g<32, 1>(tkv, p, stream);
-        case 64: return launch_g<64, 1>(tkv, p, stream);
-        case 128: return launch_g<64, 2>(tkv, p, stream);
+        case 1: return launch_g<1, 1>(tkv, tq, p, stream);
+        case 2: return launch_g<2, 1>(tkv, tq, p, stream);
+        case 4: return launch_g<4, 1>(tkv, tq, p, stream);
+        case 8: return launch_g<8, 1>(tkv, tq, p, stream);
+        case 16: return launch_g<16, 1>(tkv, tq, p, stream);
+        case 32: return launch_g<32, 1>(tkv, tq, p, stream);
+        case 64: return launch_g<64, 1>(tkv, tq, p, stream);
+        case 128: return launch_g<64, 2>(tkv, tq, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
 // GQA/MQA decode with G = 32, 64 or 128 query heads per KV head (contiguous cache).
-cudaError_t launch_wide_decode(const CUtensorMap& tk, const CUtensorMap& tv, const DecodeParams& p,
-                               cudaStream_t stream) {
+cudaError_t launch_wide_decode(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
+                               const DecodeParams& p, cudaStream_t stream) {
     switch (p.G) {
-        case 32: return launch_gp<WideShape, 32, false, 1>(tk, tv, p, stream);
-        case 64: return launch_gp<WideShape, 64, false, 1>(tk, tv, p, stream);
-        case 128: return launch_gp<WideShape, 64, false, 2>(tk, tv, p, stream);
+        case 32: return launch_gp<WideShape, 32, false, 1>(tk, tv, tq, p, stream);
+        case 64: return launch_gp<WideShape, 64, false, 1>(tk, tv, tq, p, stream);
+        case 128: return launch_gp<WideShape, 64, false, 2>(tk, tv, tq, p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

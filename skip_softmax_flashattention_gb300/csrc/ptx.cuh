@@ -472,6 +472,14 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
         : "=f"(d0), "=f"(d1)
         : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
+// (d0, d1) = (a0, a1) * b + (c0, c1) on the packed two-wide fp32 path.
+__device__ __forceinline__ void ffma2v(float& d0, float& d1, float a0, float a1, float b, float c0, float c1) {
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+        "fma.rn.ftz.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
 // (s0, s1) += (a0, a1) on the packed two-wide fp32 path.
 __device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float a1) {
     asm("{\n\t.reg .b64 ra, rs;\n\t"
