@@ -36,16 +36,17 @@
 //
 // Up to 16 heads the MMA N is 16, up to 32 it is 32, up to 64 it is 64.  128 heads: a
 // cluster of CG = 2 CTAs runs each (sequence, split), CTA r holding heads
-// [64r, 64r + 64).  The CTAs of a cluster read the same rows, so each key box and
-// value pair is loaded once and multicast to all of them (the entries of ring slot k
-// are issued by CTA k mod CG); a slot is refilled once every CTA's MMAs have released
-// it (each MMA commit arrives on the slot's barrier in every CTA), and only onto
-// barriers every CTA has armed: key slots are armed by each CTA's S issuer one ring
-// ahead, value slots by each CTA's value loader, which tells the issuing CTA.  So
+// [64r, 64r + 64).  The CTAs of a cluster read the same rows, so each key box is
+// loaded from memory once and multicast to all of them (the entries of ring slot k are
+// issued by CTA k mod CG); a slot is refilled once every CTA's MMAs have released it
+// (each MMA commit arrives on the slot's barrier in every CTA), and only onto barriers
+// every CTA has armed (each CTA's S issuer arms its key slots one ring ahead).  So
 // every copy into a CTA is one it waits for before it exits, also when a wait gives
-// up.  The tile's decision covers all the heads: every CTA sends its vote and margin
-// to every other through distributed shared memory, and each takes the AND of the CG
-// votes.
+// up.  The value pairs, second reads that find the rows in L2, are loaded by each CTA
+// for itself: sharing them tied every value slot to the slower CTA (measured 4.3 us
+// per tile for the value pairs alone at 128 heads).  The tile's decision covers all
+// the heads: every CTA sends its vote and margin to every other through distributed
+// shared memory, and each takes the AND of the CG votes.
 //
 // The same kernel serves GQA/MQA decode with 32-128 query heads per KV head
 // (WideShape): K and V are separate tensors of d <= 128 values per row, run at width
@@ -94,9 +95,9 @@ static_assert(NS + 2 <= ND, "ring sizes");
 // computed tiles, rescaled in place when a head's reference max moves.  (Landing each
 // P.V in a fresh slot and folding it into registers instead measured 4 % slower at 16
 // heads and 30 % at 32.)  More value slots at the cost of key slots measured faster,
-// up to the split used for NPAD = 16.  At 64 heads Q takes 72 KB: a lone CTA keeps one
-// P buffer and four key boxes in flight (the key stream paces it); a cluster CTA,
-// whose key ring is shared, keeps two P buffers and three key boxes.
+// up to the split used for NPAD = 16.  At 64 heads Q takes 72 KB, and one P buffer
+// leaves room for four key boxes in flight (the key stream paces these shapes; the
+// softmax of the next tile reaches its P store after the last P.V is done).
 template <class SH, int NPAD_, int CG>
 struct MlaCfg {
     static constexpr int NPAD = NPAD_;
@@ -104,9 +105,9 @@ struct MlaCfg {
     static constexpr int VBLK = SH::DV / 128;        // 128-column value blocks (box pairs) per key tile
     static_assert(SH::DK % 64 == 0 && SH::DV % 128 == 0 && SH::DV <= SH::DK, "row layout");
     // key box / value pair rings: MLA tiles are 9 boxes + 4 pairs, wide-group tiles 2 + 1
-    static constexpr int NKB = SH::SEPV ? 4 : (NPAD == 64 && CG > 1) ? 3 : 4;
+    static constexpr int NKB = 4;
     static constexpr int NVP = SH::SEPV ? 3 : NPAD == 16 ? 4 : NPAD == 32 ? 3 : 2;
-    static constexpr int NP = (!SH::SEPV && NPAD == 64 && CG == 1) ? 1 : 2;  // P staging buffers
+    static constexpr int NP = (!SH::SEPV && NPAD == 64) ? 1 : 2;  // P staging buffers
     static constexpr int Q_BYTES = KBOX * NPAD * 128;
     // P^T is the B operand of the P.V MMAs.  64 heads: MN-major, [128 keys][64 heads], so
     // each thread stores its key's row in 16-byte pieces; fewer: K-major, [key half][NPAD
@@ -141,7 +142,6 @@ struct MlaCfg {
         // heads skip; high word: its margin) and the barrier their arrivals complete
         uint64_t votes[ND][8];
         uint64_t vote_full[ND];
-        uint64_t v_armed[NVP];  // every CTA armed the slot's next entry (in the slot's issuing CTA)
         int cl_skip;            // the cluster's decision on the current tile
     };
     static constexpr int SMEM = OFF_CTRL + (int)sizeof(Ctrl) + 1024;
@@ -190,9 +190,8 @@ __global__ void __launch_bounds__(256, 1)
     if (tid == 0) {
         // a slot's release comes from the MMAs of every CTA of the cluster
         for (int i = 0; i < NKB; ++i) { mbar_init(&ctrl->k_full[i], 1); mbar_init(&ctrl->k_empty[i], CG); }
-        for (int i = 0; i < NVP; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], CG); }
-        for (int i = 0; i < ND; ++i) mbar_init(&ctrl->vote_full[i], CG);
-        for (int i = 0; i < NVP; ++i) mbar_init(&ctrl->v_armed[i], CG);
+        for (int i = 0; i < NVP; ++i) { mbar_init(&ctrl->v_full[i], 1); mbar_init(&ctrl->v_empty[i], 1); }
+        for (int i = 0; i < ND; ++i) mbar_init(&ctrl->vote_full[i], 1);  // own arrival + CG votes' bytes
         // the first NKB key entries are armed before any CTA of the cluster can copy
         for (int i = 0; i < min(NKB, n * KBOX); ++i) mbar_arrive_expect_tx(&ctrl->k_full[i], BOX_BYTES);
         for (int i = 0; i < NS; ++i) { mbar_init(&ctrl->s_full[i], 1); mbar_init(&ctrl->s_free[i], 4); }
@@ -258,10 +257,10 @@ __global__ void __launch_bounds__(256, 1)
     };
     // the pool is rows: page pg's row `off` is row pg * page_size + off (an out-of-range
     // page lands past the last row and reads as zeros)
-    auto issue_sub_box = [&](uint8_t* dst, uint64_t* bar, int x, int tile, int i, int pg) {
+    auto issue_sub_box = [&](uint8_t* dst, uint64_t* bar, int x, int tile, int i, int pg, bool mc) {
         const int off = (tile * kTile + i * p.rows_per_box) % p.page_size;
         const int y = pg * p.page_size + off;
-        if constexpr (CG == 1)
+        if (CG == 1 || !mc)
             tma_load_3d(dst + i * p.rows_per_box * 128, &tkv, bar, x, y, 0);
         else
             tma_load_3d_mc(dst + i * p.rows_per_box * 128, &tkv, bar, x, y, 0, kAll);
@@ -306,7 +305,8 @@ __global__ void __launch_bounds__(256, 1)
                     if (!(ok = __shfl_sync(0xffffffffu, go, 0) != 0)) break;
                     if constexpr (PAGED) {
                         if (lane < nbox)
-                            issue_sub_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, t0 + j, lane, pg);
+                            issue_sub_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, t0 + j, lane, pg,
+                                          true);
                     }
                 }
                 last = e + 1;
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(256, 1)
         }
     } else if (warp == 6) {
         // ------------------------------------------------------------ value loader
-        // pair i of the c-th computed tile is ring entry c*VBLK + i
+        // pair i of the c-th computed tile is ring entry c*VBLK + i (this CTA's own copy)
         int issued = 0;
         bool ok = true;
         for (int j = 0; j < n && ok; ++j) {
@@ -337,32 +337,25 @@ __global__ void __launch_bounds__(256, 1)
                 const int e = issued, vs = e % NVP;
                 int gv = 1;
                 if (lane == 0) {
-                    if (e >= NVP && !mbar_wait_cluster(&ctrl->v_empty[vs], ((e / NVP) - 1) & 1, wd)) {
+                    if (e >= NVP && !mbar_wait(&ctrl->v_empty[vs], ((e / NVP) - 1) & 1, wd)) {
                         gv = 0;
                     } else {
                         mbar_arrive_expect_tx(&ctrl->v_full[vs], PAIR_BYTES);
-                        if constexpr (CG > 1) {
-                            mbar_arrive_cluster(cluster_addr(&ctrl->v_armed[vs], (uint32_t)(vs % CG)));
-                            // the issuing CTA copies once every CTA armed the entry
-                            if (issues(vs) && !mbar_wait_cluster(&ctrl->v_armed[vs], (e / NVP) & 1, wd)) gv = 0;
-                        }
                         if constexpr (!PAGED) {
-                            if (gv && issues(vs)) {
 #pragma unroll
-                                for (int h = 0; h < 2; ++h)
-                                    load_box(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
-                                             i * 128 + h * 64, (t0 + j) * kTile, SH::SEPV ? &tv : &tkv);
-                            }
+                            for (int h = 0; h < 2; ++h)
+                                tma_load_3d(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, SH::SEPV ? &tv : &tkv,
+                                            &ctrl->v_full[vs], i * 128 + h * 64, (t0 + j) * kTile, zkv);
                         }
                     }
                 }
                 if (!(ok = __shfl_sync(0xffffffffu, gv, 0) != 0)) break;
                 if constexpr (PAGED) {
-                    if (lane < nbox && issues(vs)) {
+                    if (lane < nbox) {
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
                             issue_sub_box(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
-                                          i * 128 + h * 64, t0 + j, lane, pg);
+                                          i * 128 + h * 64, t0 + j, lane, pg, false);
                     }
                 }
                 issued = e + 1;
@@ -371,9 +364,6 @@ __global__ void __launch_bounds__(256, 1)
         if (lane == 0) {
             for (int e = max(0, issued - NVP); e < issued; ++e)
                 mbar_wait_drain(&ctrl->v_full[e % NVP], (e / NVP) & 1, kDrainNs);
-            if constexpr (CG > 1)
-                for (int e = max(0, issued - NVP); e < issued; ++e)
-                    mbar_wait_drain(&ctrl->v_empty[e % NVP], (e / NVP) & 1, kDrainNs);
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ S issuer
@@ -443,7 +433,7 @@ __global__ void __launch_bounds__(256, 1)
                         const uint32_t acc = (kk > 0 || comp > 0) ? 1u : 0u;
                         mma_ss(tmem + O_COL + i * NPAD, adesc, bdesc, kIdescO, acc);
                     }
-                    release(&ctrl->v_empty[vs]);
+                    mma_commit(&ctrl->v_empty[vs]);
                 }
                 if (!ok) break;
                 mma_commit(&ctrl->o_done[comp % 8]);
@@ -564,15 +554,19 @@ __global__ void __launch_bounds__(256, 1)
             if constexpr (CG > 1) {
                 // The decision covers the heads of every CTA of the cluster: send this
                 // CTA's vote and margin to all of them, wait for theirs, take the AND and
-                // the max.  A CTA runs less than a tile ahead of the slowest one in its S
-                // MMAs (a key slot is refilled only after every CTA released it), so a
-                // vote slot is never overwritten before it was read.
+                // the max.  Each vote is an asynchronous store that completes its bytes on
+                // the receiver's barrier, which the receiver arms for CG votes (a remote
+                // arrive with cluster-scope release took ~2 us here).  A CTA is never a
+                // whole tile ahead of another in this exchange, so a vote slot is never
+                // overwritten before it was read.
                 if (tid == 0) {
                     const int slot = j % ND;
                     const uint64_t word = ((uint64_t)__float_as_uint(margin) << 32) | (skip ? 1u : 0u);
-                    for (int r = 0; r < CG; ++r) st_cluster_u64(cluster_addr(&ctrl->votes[slot][rank], r), word);
-                    for (int r = 0; r < CG; ++r) mbar_arrive_cluster(cluster_addr(&ctrl->vote_full[slot], r));
-                    bool all = mbar_wait_cluster(&ctrl->vote_full[slot], (j / ND) & 1, wd);
+                    mbar_arrive_expect_tx(&ctrl->vote_full[slot], CG * 8);
+                    for (int r = 0; r < CG; ++r)
+                        st_async_cluster_u64(cluster_addr(&ctrl->votes[slot][rank], r), word,
+                                             cluster_addr(&ctrl->vote_full[slot], r));
+                    bool all = mbar_wait(&ctrl->vote_full[slot], (j / ND) & 1, wd);
                     float mg = -CUDART_INF_F;
                     for (int r = 0; r < CG; ++r) {
                         const uint64_t w = reinterpret_cast<volatile uint64_t*>(ctrl->votes[slot])[r];

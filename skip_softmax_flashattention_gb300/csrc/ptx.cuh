@@ -210,14 +210,6 @@ __device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(a) : "r"(smem_u32(p)), "r"(rank));
     return a;
 }
-__device__ __forceinline__ void st_cluster_u64(uint32_t caddr, uint64_t v) {
-    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(caddr), "l"(v) : "memory");
-}
-// Arrive on an mbarrier of a CTA of the cluster; release at cluster scope, so this
-// thread's earlier shared::cluster stores are seen by a cluster-scope acquire wait.
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
-}
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -228,6 +220,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
         : "r"(smem_u32(bar)), "r"(parity)
         : "memory");
     return ok != 0;
+}
+// 8-byte store into the shared memory of a CTA of the cluster (address from
+// cluster_addr) that completes 8 bytes of transaction count on that CTA's mbarrier
+// `cbar`; needs no fence: the receiver sees the value once the phase completes.
+__device__ __forceinline__ void st_async_cluster_u64(uint32_t caddr, uint64_t v, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b64 [%0], %1, [%2];" ::"r"(caddr), "l"(v),
+                 "r"(cbar)
+                 : "memory");
 }
 // mbar_wait with cluster-scope acquire (for phases completed by other CTAs' arrivals).
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
