@@ -234,7 +234,7 @@ size_t blasst_decode_noalloc_scratch_bytes(void);
  *   q [B, Hq, dk], o [B, Hq, dv] bf16; lse nullable fp32 [B, Hq].
  *   Hq           1, 2, 4, 8, 16, 32, 64 or 128 query heads (else
  *                BLASST_ERR_UNSUPPORTED); above 64 the heads are spread over a cluster
- *                of Hq / 64 CTAs that share every load.  dk must be 576 and dv 512
+ *                of Hq / 64 CTAs that share the key loads.  dk must be 576 and dv 512
  *                (else BLASST_ERR_UNSUPPORTED).
  *   kv           page_table NULL: contiguous bf16 [B][max_kv_len][dk];
  *                page_table set: a pool of num_pages pages of page_size rows,
@@ -242,7 +242,9 @@ size_t blasst_decode_noalloc_scratch_bytes(void);
  *                i mod page_size of page page_table[b][i / page_size] (The
  *                Hitchhiker's Guide, Phase 08, Section 3, "Paged Attention");
  *                page_size 8, 16, 32, 64 or a multiple of 128, and
- *                max_pages_per_seq * page_size >= max_kv_len.  16-byte aligned.
+ *                max_pages_per_seq * page_size >= max_kv_len; (num_pages + 1) *
+ *                page_size must stay below 2^31 - 128 (else BLASST_ERR_UNSUPPORTED).
+ *                16-byte aligned.
  *                (num_pages, page_size, max_pages_per_seq are ignored without a
  *                page table.)
  *   seq_lens     nullable device int32 [B]: rows of sequence b (NULL: max_kv_len

@@ -502,7 +502,8 @@ int blasst_mla_decode(const void* q, const void* kv, const int* page_table, cons
     }
     CUtensorMap tkv, tq;
     const int rows = page_size < kTile ? page_size : kTile;
-    if (page_table && (long long)num_pages * page_size > 0x7fffffffLL - kTile) return BLASST_ERR_UNSUPPORTED;
+    // pool rows, and the row past the last page that an out-of-range index reads, fit an int
+    if (page_table && ((long long)num_pages + 1) * page_size > 0x7fffffffLL - kTile) return BLASST_ERR_UNSUPPORTED;
     if (page_table ? !encode_rows(&tkv, kv, dk, (long long)num_pages * page_size, rows)
                    : !encode_3d(&tkv, kv, dk, max_kv_len, B))
         return BLASST_ERR_CUDA;

@@ -145,17 +145,21 @@ __global__ void __launch_bounds__(224, 1)
     // run; lane i of a loader warp reads that box's page index and issues it, so
     // the page-table reads of a tile are in flight together.
     const int nbox = PAGED ? kTile / p.rows_per_box : 1;
-    auto box_page = [&](int tile, int i) -> int {
-        int e = p.num_pages;  // out of range: the box reads as zeros
+    // A page index is loaded ahead of its copy and checked only when the copy is issued
+    // (a check right after the load would hold the loader warp for the whole load).
+    auto box_live = [&](int tile, int i) -> bool {  // boxes past the keys or before the window read zeros
         const int key = tile * kTile + i * p.rows_per_box;
-        if (i < nbox && key < Lb && key + p.rows_per_box > first_key) {  // boxes before the window read zeros
-            const int v = p.page_table[(long long)b * p.max_pages + key / p.page_size];
-            if (v >= 0 && v < p.num_pages)
-                e = v;
-            else
-                atomicOr(p.status, kStatusPageTable);
-        }
-        return e;
+        return i < nbox && key < Lb && key + p.rows_per_box > first_key;
+    };
+    auto page_load = [&](int tile, int i) -> int {
+        const int key = tile * kTile + i * p.rows_per_box;
+        return box_live(tile, i) ? p.page_table[(long long)b * p.max_pages + key / p.page_size] : -1;
+    };
+    auto page_check = [&](int v, int tile, int i) -> int {
+        if (!box_live(tile, i)) return p.num_pages;  // out of range: the box reads as zeros
+        if (v >= 0 && v < p.num_pages) return v;
+        atomicOr(p.status, kStatusPageTable);
+        return p.num_pages;
     };
     auto issue_box = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile, int i, int pg) {
         const int off = (tile * kTile + i * p.rows_per_box) % p.page_size;
@@ -192,13 +196,13 @@ __global__ void __launch_bounds__(224, 1)
             if (lane == 0) tma_prefetch_desc(&tk);
             int issued = 0;
             // each lane's page index is read two tiles ahead of its copy
-            int pg_next = n > 0 ? box_page(t0, lane) : 0;
-            int pg_next2 = n > 1 ? box_page(t0 + 1, lane) : 0;
+            int pg_next = n > 0 ? page_load(t0, lane) : 0;
+            int pg_next2 = n > 1 ? page_load(t0 + 1, lane) : 0;
             for (int j = 0; j < n; ++j) {
                 const int ks = j % NK;
-                const int pg = pg_next;
+                const int pg = page_check(pg_next, t0 + j, lane);
                 pg_next = pg_next2;
-                pg_next2 = j + 2 < n ? box_page(t0 + j + 2, lane) : 0;
+                pg_next2 = j + 2 < n ? page_load(t0 + j + 2, lane) : 0;
                 int ok = 1;
                 if (lane == 0) {
                     if (j >= NK && !mbar_wait(&ctrl->k_empty[ks], ((j / NK) - 1) & 1, wd))
@@ -218,8 +222,10 @@ __global__ void __launch_bounds__(224, 1)
         // ------------------------------------------------------------ V loader
         if (lane == 0) tma_prefetch_desc(&tv);
         int comp = 0;
+        int pg_next = (PAGED && n > 0) ? page_load(t0, lane) : 0;  // one tile ahead of its copy
         for (int j = 0; j < n; ++j) {
-            const int pg = PAGED ? box_page(t0 + j, lane) : 0;  // read while lane 0 waits for the decision
+            const int pg_raw = pg_next;
+            if constexpr (PAGED) pg_next = j + 1 < n ? page_load(t0 + j + 1, lane) : 0;
             int go = 0;  // 0: stop, 1: load V_j, 2: tile skipped
             if (lane == 0) {
                 if (mbar_wait(&ctrl->dec_full[j % ND], (j / ND) & 1, wd)) {
@@ -247,6 +253,7 @@ __global__ void __launch_bounds__(224, 1)
                                     (t0 + j) * kTile, zkv);
                 }
             } else {
+                const int pg = page_check(pg_raw, t0 + j, lane);
                 if (lane < nbox) issue_box(&tv, smem + OFF_V + vs * TILE_BYTES, &ctrl->v_full[vs], t0 + j, lane, pg);
             }
             ++comp;

@@ -243,28 +243,39 @@ __global__ void __launch_bounds__(256, 1)
     // the tile, one page run; lane i of a loader warp reads its page index once
     // per tile and issues that sub-box of every column box.
     const int nbox = PAGED ? kTile / p.rows_per_box : 1;
-    auto box_page = [&](int tile, int i) -> int {
-        int e = p.num_pages;  // out of range: the sub-box reads as zeros
+    // A page index is loaded well before its copy and checked only when the copy is
+    // issued: a check right after the load would hold the loader warp for the whole
+    // load (measured: 12 % of the paged kernel's time at 128-row pages).
+    auto page_load = [&](int tile, int i) -> int {
         const int key = tile * kTile + i * p.rows_per_box;
-        if (i < nbox && key < Lb) {
-            const int v = p.page_table[(long long)b * p.max_pages + key / p.page_size];
-            if (v >= 0 && v < p.num_pages)
-                e = v;
-            else
-                atomicOr(p.status, kStatusPageTable);
-        }
-        return e;
+        return (i < nbox && key < Lb) ? p.page_table[(long long)b * p.max_pages + key / p.page_size] : -1;
     };
-    // the pool is rows: page pg's row `off` is row pg * page_size + off (an out-of-range
-    // page lands past the last row and reads as zeros)
-    auto issue_sub_box = [&](uint8_t* dst, uint64_t* bar, int x, int tile, int i, int pg, bool mc) {
-        const int off = (tile * kTile + i * p.rows_per_box) % p.page_size;
-        const int y = pg * p.page_size + off;
+    auto page_check = [&](int v, int tile, int i) -> int {
+        const int key = tile * kTile + i * p.rows_per_box;
+        if (!(i < nbox && key < Lb)) return p.num_pages;  // past the sequence: the sub-box reads as zeros
+        if (v >= 0 && v < p.num_pages) return v;
+        atomicOr(p.status, kStatusPageTable);
+        return p.num_pages;  // out of range: zeros
+    };
+    // The pool is rows: page pg's row `off` is row pg * page_size + off (an out-of-range
+    // page lands past the last row and reads as zeros).  Pool row of sub-box i of a tile:
+    auto sub_row = [&](int pg, int tile, int i) -> int {
+        return pg * p.page_size + (tile * kTile + i * p.rows_per_box) % p.page_size;
+    };
+    // sub-box i (rows [i*rows, (i+1)*rows) of a 64-column box) from pool row y
+    auto copy_sub = [&](uint8_t* dst, uint64_t* bar, int x, int i, int y, bool mc) {
         if (CG == 1 || !mc)
             tma_load_3d(dst + i * p.rows_per_box * 128, &tkv, bar, x, y, 0);
         else
             tma_load_3d_mc(dst + i * p.rows_per_box * 128, &tkv, bar, x, y, 0, kAll);
     };
+    // With up to kLane0Subs sub-boxes a box (pages of 32 rows or more) lane 0 issues
+    // them all right after the slot wait, from rows gathered once a tile; smaller pages
+    // issue lane by lane after the wait's broadcast.  (Issuing every copy after the
+    // broadcast put a warp reconvergence between each freed slot and its copy: the
+    // paged form ran 11 % slower than the contiguous one with the same addresses.)
+    constexpr int kLane0Subs = 4;
+    const bool lane0_issues = nbox <= kLane0Subs;
 
     if (warp == 4) {
         // ------------------------------------------------------------ key loader
@@ -284,29 +295,36 @@ __global__ void __launch_bounds__(256, 1)
         bool ok = true;
         // paged: each lane's page index is read two tiles ahead, so the load's latency
         // never sits between a freed slot and its copy
-        int pg_next = (PAGED && n > 0) ? box_page(t0, lane) : 0;
-        int pg_next2 = (PAGED && n > 1) ? box_page(t0 + 1, lane) : 0;
+        int pg_next = (PAGED && n > 0) ? page_load(t0, lane) : 0;
+        int pg_next2 = (PAGED && n > 1) ? page_load(t0 + 1, lane) : 0;
         for (int j = 0; j < n && ok; ++j) {
-            const int pg = pg_next;
+            int y = 0, ys[kLane0Subs];
             if constexpr (PAGED) {
+                y = sub_row(page_check(pg_next, t0 + j, lane), t0 + j, lane);
+#pragma unroll
+                for (int i = 0; i < kLane0Subs; ++i) ys[i] = __shfl_sync(0xffffffffu, y, i);
                 pg_next = pg_next2;
-                pg_next2 = j + 2 < n ? box_page(t0 + j + 2, lane) : 0;
+                pg_next2 = j + 2 < n ? page_load(t0 + j + 2, lane) : 0;
             }
             for (int c = 0; c < KBOX; ++c) {
                 const int e = j * KBOX + c, ks = e % NKB;
                 if (issues(ks)) {
+                    uint8_t* dst = smem + OFF_K + ks * BOX_BYTES;
                     int go = 1;
                     if (lane == 0) {
-                        if (e >= NKB && !mbar_wait_cluster(&ctrl->k_empty[ks], ((e / NKB) - 1) & 1, wd))
+                        if (e >= NKB && !mbar_wait_cluster(&ctrl->k_empty[ks], ((e / NKB) - 1) & 1, wd)) {
                             go = 0;
-                        else if constexpr (!PAGED)
-                            load_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, (t0 + j) * kTile, &tkv);
+                        } else if constexpr (!PAGED) {
+                            load_box(dst, &ctrl->k_full[ks], c * 64, (t0 + j) * kTile, &tkv);
+                        } else if (lane0_issues) {
+#pragma unroll
+                            for (int i = 0; i < kLane0Subs; ++i)
+                                if (i < nbox) copy_sub(dst, &ctrl->k_full[ks], c * 64, i, ys[i], true);
+                        }
                     }
                     if (!(ok = __shfl_sync(0xffffffffu, go, 0) != 0)) break;
                     if constexpr (PAGED) {
-                        if (lane < nbox)
-                            issue_sub_box(smem + OFF_K + ks * BOX_BYTES, &ctrl->k_full[ks], c * 64, t0 + j, lane, pg,
-                                          true);
+                        if (!lane0_issues && lane < nbox) copy_sub(dst, &ctrl->k_full[ks], c * 64, lane, y, true);
                     }
                 }
                 last = e + 1;
@@ -322,8 +340,12 @@ __global__ void __launch_bounds__(256, 1)
         // pair i of the c-th computed tile is ring entry c*VBLK + i (this CTA's own copy)
         int issued = 0;
         bool ok = true;
+        // paged: each lane's page index is read one tile ahead, so the load's latency
+        // never sits between a decision and the tile's first value copy
+        int pg_next = (PAGED && n > 0) ? page_load(t0, lane) : 0;
         for (int j = 0; j < n && ok; ++j) {
-            const int pg = PAGED ? box_page(t0 + j, lane) : 0;  // read while lane 0 waits for the decision
+            const int pg_raw = pg_next;
+            if constexpr (PAGED) pg_next = j + 1 < n ? page_load(t0 + j + 1, lane) : 0;
             int go = 0;  // 0: stop, 1: load the tile's values, 2: tile skipped
             if (lane == 0 && mbar_wait(&ctrl->dec_full[j % ND], (j / ND) & 1, wd)) {
                 const bool skipped = reinterpret_cast<volatile int*>(ctrl->dec)[j % ND] != 0;
@@ -333,6 +355,12 @@ __global__ void __launch_bounds__(256, 1)
             go = __shfl_sync(0xffffffffu, go, 0);
             if (go == 0) break;
             if (go == 2) continue;
+            int y = 0, ys[kLane0Subs];
+            if constexpr (PAGED) {
+                y = sub_row(page_check(pg_raw, t0 + j, lane), t0 + j, lane);
+#pragma unroll
+                for (int i = 0; i < kLane0Subs; ++i) ys[i] = __shfl_sync(0xffffffffu, y, i);
+            }
             for (int i = 0; i < VBLK; ++i) {
                 const int e = issued, vs = e % NVP;
                 int gv = 1;
@@ -346,16 +374,24 @@ __global__ void __launch_bounds__(256, 1)
                             for (int h = 0; h < 2; ++h)
                                 tma_load_3d(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, SH::SEPV ? &tv : &tkv,
                                             &ctrl->v_full[vs], i * 128 + h * 64, (t0 + j) * kTile, zkv);
+                        } else if (lane0_issues) {
+#pragma unroll
+                            for (int sb = 0; sb < kLane0Subs; ++sb)
+#pragma unroll
+                                for (int h = 0; h < 2; ++h)
+                                    if (sb < nbox)
+                                        copy_sub(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
+                                                 i * 128 + h * 64, sb, ys[sb], false);
                         }
                     }
                 }
                 if (!(ok = __shfl_sync(0xffffffffu, gv, 0) != 0)) break;
                 if constexpr (PAGED) {
-                    if (lane < nbox) {
+                    if (!lane0_issues && lane < nbox) {
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
-                            issue_sub_box(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
-                                          i * 128 + h * 64, t0 + j, lane, pg, false);
+                            copy_sub(smem + OFF_V + vs * PAIR_BYTES + h * BOX_BYTES, &ctrl->v_full[vs],
+                                     i * 128 + h * 64, lane, y, false);
                     }
                 }
                 issued = e + 1;

@@ -183,6 +183,8 @@ def test_prefill_window_validation(kw, code):
     (dict(table=FAKE, mp=1), K.BLASST_ERR_INVALID_ARG),   # one 64-row page cannot hold 1000 rows
     (dict(table=FAKE, npg=0), K.BLASST_ERR_INVALID_ARG),
     (dict(table=FAKE, ps=24, mp=42), K.BLASST_ERR_UNSUPPORTED),
+    # the pool's rows plus the row an out-of-range page reads must fit a 32-bit row index
+    (dict(table=FAKE, ps=128, npg=(2 ** 31 - 128) // 128 - 1, mp=8), K.BLASST_ERR_UNSUPPORTED),
     (dict(table=FAKE + 2), K.BLASST_ERR_UNSUPPORTED),
     (dict(kv=FAKE + 2), K.BLASST_ERR_UNSUPPORTED),
     (dict(S=2, ws=None), K.BLASST_ERR_INVALID_ARG),
