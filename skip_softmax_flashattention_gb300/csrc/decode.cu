@@ -161,6 +161,12 @@ __global__ void __launch_bounds__(224, 1)
         atomicOr(p.status, kStatusPageTable);
         return p.num_pages;
     };
+    // With up to kLane0Subs boxes a tile (pages of 32 keys or more) lane 0 issues them
+    // all right after its slot wait, with page indices gathered once a tile; smaller
+    // pages issue lane by lane after the wait's broadcast (a warp reconvergence then
+    // sits between the freed slot and the copies).
+    constexpr int kLane0Subs = 4;
+    const bool lane0_issues = nbox <= kLane0Subs;
     auto issue_box = [&](const CUtensorMap* map, uint8_t* dst, uint64_t* bar, int tile, int i, int pg) {
         const int off = (tile * kTile + i * p.rows_per_box) % p.page_size;
 #pragma unroll
@@ -201,17 +207,28 @@ __global__ void __launch_bounds__(224, 1)
             for (int j = 0; j < n; ++j) {
                 const int ks = j % NK;
                 const int pg = page_check(pg_next, t0 + j, lane);
+                int pgs[kLane0Subs];
+#pragma unroll
+                for (int i = 0; i < kLane0Subs; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
                 pg_next = pg_next2;
                 pg_next2 = j + 2 < n ? page_load(t0 + j + 2, lane) : 0;
                 int ok = 1;
                 if (lane == 0) {
-                    if (j >= NK && !mbar_wait(&ctrl->k_empty[ks], ((j / NK) - 1) & 1, wd))
+                    if (j >= NK && !mbar_wait(&ctrl->k_empty[ks], ((j / NK) - 1) & 1, wd)) {
                         ok = 0;
-                    else
+                    } else {
                         mbar_arrive_expect_tx(&ctrl->k_full[ks], TILE_BYTES);
+                        if (lane0_issues) {
+#pragma unroll
+                            for (int i = 0; i < kLane0Subs; ++i)
+                                if (i < nbox)
+                                    issue_box(&tk, smem + OFF_K + ks * TILE_BYTES, &ctrl->k_full[ks], t0 + j, i, pgs[i]);
+                        }
+                    }
                 }
                 if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-                if (lane < nbox) issue_box(&tk, smem + OFF_K + ks * TILE_BYTES, &ctrl->k_full[ks], t0 + j, lane, pg);
+                if (!lane0_issues && lane < nbox)
+                    issue_box(&tk, smem + OFF_K + ks * TILE_BYTES, &ctrl->k_full[ks], t0 + j, lane, pg);
                 issued = j + 1;
             }
             if (lane == 0)
@@ -222,10 +239,16 @@ __global__ void __launch_bounds__(224, 1)
         // ------------------------------------------------------------ V loader
         if (lane == 0) tma_prefetch_desc(&tv);
         int comp = 0;
-        int pg_next = (PAGED && n > 0) ? page_load(t0, lane) : 0;  // one tile ahead of its copy
+        int pg_next = (PAGED && n > 0) ? page_load(t0, lane) : 0;  // one tile ahead of its check
         for (int j = 0; j < n; ++j) {
-            const int pg_raw = pg_next;
-            if constexpr (PAGED) pg_next = j + 1 < n ? page_load(t0 + j + 1, lane) : 0;
+            int pg = 0, pgs[kLane0Subs];
+            if constexpr (PAGED) {
+                pg = page_check(pg_next, t0 + j, lane);
+#pragma unroll
+                for (int i = 0; i < kLane0Subs; ++i) pgs[i] = __shfl_sync(0xffffffffu, pg, i);
+                pg_next = j + 1 < n ? page_load(t0 + j + 1, lane) : 0;
+            }
+            const int vs = comp % NV;
             int go = 0;  // 0: stop, 1: load V_j, 2: tile skipped
             if (lane == 0) {
                 if (mbar_wait(&ctrl->dec_full[j % ND], (j / ND) & 1, wd)) {
@@ -233,28 +256,33 @@ __global__ void __launch_bounds__(224, 1)
                     mbar_arrive(&ctrl->dec_free[j % ND]);
                     go = skipped ? 2 : 1;  // skipped: V never loaded
                     if (!skipped) {
-                        const int vs = comp % NV;
-                        if (comp >= NV && !mbar_wait(&ctrl->v_empty[vs], ((comp / NV) - 1) & 1, wd))
+                        if (comp >= NV && !mbar_wait(&ctrl->v_empty[vs], ((comp / NV) - 1) & 1, wd)) {
                             go = 0;
-                        else
+                        } else {
+                            // the copies go out before the broadcast
                             mbar_arrive_expect_tx(&ctrl->v_full[vs], TILE_BYTES);
+                            if constexpr (!PAGED) {
+#pragma unroll
+                                for (int x = 0; x < D / 64; ++x)
+                                    tma_load_3d(smem + OFF_V + vs * TILE_BYTES + x * BOX_BYTES, &tv, &ctrl->v_full[vs],
+                                                x * 64, (t0 + j) * kTile, zkv);
+                            } else if (lane0_issues) {
+#pragma unroll
+                                for (int i = 0; i < kLane0Subs; ++i)
+                                    if (i < nbox)
+                                        issue_box(&tv, smem + OFF_V + vs * TILE_BYTES, &ctrl->v_full[vs], t0 + j, i,
+                                                  pgs[i]);
+                            }
+                        }
                     }
                 }
             }
             go = __shfl_sync(0xffffffffu, go, 0);
             if (go == 0) break;
             if (go == 2) continue;
-            const int vs = comp % NV;
-            if constexpr (!PAGED) {
-                if (lane == 0) {
-#pragma unroll
-                    for (int x = 0; x < D / 64; ++x)
-                        tma_load_3d(smem + OFF_V + vs * TILE_BYTES + x * BOX_BYTES, &tv, &ctrl->v_full[vs], x * 64,
-                                    (t0 + j) * kTile, zkv);
-                }
-            } else {
-                const int pg = page_check(pg_raw, t0 + j, lane);
-                if (lane < nbox) issue_box(&tv, smem + OFF_V + vs * TILE_BYTES, &ctrl->v_full[vs], t0 + j, lane, pg);
+            if constexpr (PAGED) {
+                if (!lane0_issues && lane < nbox)
+                    issue_box(&tv, smem + OFF_V + vs * TILE_BYTES, &ctrl->v_full[vs], t0 + j, lane, pg);
             }
             ++comp;
         }
