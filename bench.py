@@ -36,8 +36,8 @@ DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture of the current kernels; None until captured for this version of the kernels.
 # prefill: prefill2_kernel<128, false> capture (365.6 MB read + 100.3 MB written).
-# decode: decode_kernel<4, false> B=8 capture (1074.0 MB read + 4.3 MB written) x 8 for the B=64 launch.
-TRAFFIC_BYTES = {"prefill": 365569024 + 100312832, "decode": 8 * (1073967000 + 4270336)}
+# decode: decode_kernel<4, false> B=8 capture (1073.9 MB read + 4.0 MB written) x 8 for the B=64 launch.
+TRAFFIC_BYTES = {"prefill": 365569024 + 100312832, "decode": 8 * (1073891000 + 3998976)}
 
 
 def load_peaks():
