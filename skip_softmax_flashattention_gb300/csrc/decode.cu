@@ -519,21 +519,31 @@ __global__ void __launch_bounds__(224, 1)
 
 // Merge the per-split results by log-sum-exp: lse = ln(sum_s e^{lse_s}),
 // O = sum_s e^{lse_s - lse} O_s.  One CTA per (head, batch), one thread per column.
+// Each warp reads the split lse values lane by lane (split s in lane s mod 32) and
+// reduces their max and sum with shuffles, so the reads are in flight together; the
+// weighted sum then streams the partials with independent loads.  (Reading the lse
+// values split after split in every thread made the merge latency-bound: 12.8 us for
+// 7 splits of 64 x 16 rows of 512 values.)
 __global__ void combine_kernel(const CombineParams p) {
-    const int hq = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+    const int hq = blockIdx.x, b = blockIdx.y, t = threadIdx.x, lane = t & 31;
     const long long bh = (long long)b * p.Hq + hq;
     const long long stride = (long long)p.B * p.Hq;
     float M = -CUDART_INF_F;
-    for (int s = 0; s < p.S; ++s) M = fmaxf(M, p.lse_part[s * stride + bh]);
+    for (int s = lane; s < p.S; s += 32) M = fmaxf(M, p.lse_part[s * stride + bh]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
     if (M == -CUDART_INF_F) {  // no split saw a key (a sequence of length 0)
         reinterpret_cast<unsigned short*>(p.o)[bh * p.d + t] = 0;
         if (t == 0 && p.lse) p.lse[bh] = -CUDART_INF_F;
         return;
     }
     float tot = 0.f;
-    for (int s = 0; s < p.S; ++s) tot += __expf(p.lse_part[s * stride + bh] - M);
+    for (int s = lane; s < p.S; s += 32) tot += __expf(p.lse_part[s * stride + bh] - M);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
     const float L = M + __logf(tot);
     float acc = 0.f;
+#pragma unroll 4
     for (int s = 0; s < p.S; ++s) {
         const float w = __expf(p.lse_part[s * stride + bh] - L);
         acc = fmaf(w, p.o_part[(s * stride + bh) * p.d + t], acc);
