@@ -130,7 +130,7 @@ struct MlaCfg {
         uint32_t tmem_base;
         int dec[ND];
         int abort;
-        float red[2][4][NPAD];      // per-warp tile maxima, by tile parity
+        alignas(16) float red[2][4][NPAD];  // per-warp tile maxima, by tile parity
         float mex[2][NPAD];         // exact running max per head, by tile parity
         float mrf[2][NPAD];         // reference max per head, by tile parity
         float alpha[NPAD];          // this tile's rescale factor per head
@@ -536,15 +536,27 @@ __global__ void __launch_bounds__(256, 1)
                 fence_regs<NPAD>(xr);
             };
             {
-                // per-head max over the warp's 32 keys by a transposing butterfly: each
-                // step hands half of the remaining heads to the partner lane, so lane L
+                // Per-head max over the warp's 32 keys.  From 32 heads: one warp-wide
+                // reduction (redux.sync max.f32) per head, stored by lane 0 (measured 1-2 %
+                // faster than the butterfly there).  Below: a transposing butterfly, where
+                // each step hands half of the remaining heads to the partner lane, so lane L
                 // ends with the max of head L >> (5 - log2 G) after G - 1 + (5 - log2 G)
-                // shuffles instead of 5 G
+                // shuffles instead of 5 G.
                 uint32_t xr[NPAD];
                 load_scores(xr);
                 float v[G];
 #pragma unroll
                 for (int g = 0; g < G; ++g) v[g] = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
+                if constexpr (G >= 32) {
+#pragma unroll
+                    for (int g = 0; g < G; ++g) v[g] = warp_max_f32(v[g]);
+                    if (lane == 0) {
+#pragma unroll
+                        for (int g = 0; g < G; g += 4)
+                            *reinterpret_cast<float4*>(&ctrl->red[q][warp][g]) =
+                                make_float4(v[g], v[g + 1], v[g + 2], v[g + 3]);
+                    }
+                } else {
                 int hl = 0;  // head index held by this lane
 #pragma unroll
                 for (int st = 0; st < 5; ++st) {
@@ -568,6 +580,7 @@ __global__ void __launch_bounds__(256, 1)
                 if ((lane & (kLow - 1)) == 0) {
 #pragma unroll
                     for (int r = 0; r < kPer; ++r) ctrl->red[q][warp][hl + r] = v[r];
+                }
                 }
             }
             named_bar_sync(1, 128);

@@ -458,6 +458,12 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
 }
+// Maximum of x over the 32 lanes of the warp, in every lane (all lanes must take part).
+__device__ __forceinline__ float warp_max_f32(float x) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+    return r;
+}
 // Three-input maximum (one instruction on sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
