@@ -163,6 +163,7 @@ __global__ void __launch_bounds__(256, 1)
     constexpr int OFF_K = C::OFF_K, OFF_V = C::OFF_V, OFF_Q = C::OFF_Q, OFF_P = C::OFF_P;
     constexpr uint32_t O_COL = C::O_COL;
     static_assert(CG == 1 || G == NPAD, "a cluster's CTAs hold NPAD heads each");
+    static_assert(!C::MNP || G == NPAD, "the MN-major P rows are written for every one of the NPAD heads");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align1024(smem_raw);
     auto* ctrl = reinterpret_cast<typename C::Ctrl*>(smem + C::OFF_CTRL);
