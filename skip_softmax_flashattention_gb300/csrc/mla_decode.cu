@@ -95,9 +95,10 @@ static_assert(NS + 2 <= ND, "ring sizes");
 // computed tiles, rescaled in place when a head's reference max moves.  (Landing each
 // P.V in a fresh slot and folding it into registers instead measured 4 % slower at 16
 // heads and 30 % at 32.)  More value slots at the cost of key slots measured faster,
-// up to the split used for NPAD = 16.  At 64 heads Q takes 72 KB, and one P buffer
-// leaves room for four key boxes in flight (the key stream paces these shapes; the
-// softmax of the next tile reaches its P store after the last P.V is done).
+// up to the split used for NPAD = 16.  From 32 heads one P buffer frees room for key
+// boxes: five at 32 heads (Q 36 KB), four at 64 (Q 72 KB).  The key stream paces these
+// shapes, and the softmax of the next tile reaches its P store after the last P.V is
+// done.
 template <class SH, int NPAD_, int CG>
 struct MlaCfg {
     static constexpr int NPAD = NPAD_;
@@ -105,9 +106,9 @@ struct MlaCfg {
     static constexpr int VBLK = SH::DV / 128;        // 128-column value blocks (box pairs) per key tile
     static_assert(SH::DK % 64 == 0 && SH::DV % 128 == 0 && SH::DV <= SH::DK, "row layout");
     // key box / value pair rings: MLA tiles are 9 boxes + 4 pairs, wide-group tiles 2 + 1
-    static constexpr int NKB = 4;
+    static constexpr int NKB = (!SH::SEPV && NPAD == 32) ? 5 : 4;
     static constexpr int NVP = SH::SEPV ? 3 : NPAD == 16 ? 4 : NPAD == 32 ? 3 : 2;
-    static constexpr int NP = (!SH::SEPV && NPAD == 64) ? 1 : 2;  // P staging buffers
+    static constexpr int NP = (!SH::SEPV && NPAD >= 32) ? 1 : 2;  // P staging buffers
     static constexpr int Q_BYTES = KBOX * NPAD * 128;
     // P^T is the B operand of the P.V MMAs.  64 heads: MN-major, [128 keys][64 heads], so
     // each thread stores its key's row in 16-byte pieces; fewer: K-major, [key half][NPAD
