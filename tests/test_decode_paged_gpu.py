@@ -35,7 +35,7 @@ def _run(a, lam, S, **kw):
 LENS = [1000, 1, 517, 768, 100]
 
 
-@pytest.mark.parametrize("page_size", [8, 16, 64, 128, 256])
+@pytest.mark.parametrize("page_size", [8, 16, 32, 64, 128, 256])
 @pytest.mark.parametrize("token_major", [True, False], ids=["key-major", "head-major"])
 @pytest.mark.parametrize("S", [1, 3])
 @pytest.mark.parametrize("lam", [0.0, 0.3])

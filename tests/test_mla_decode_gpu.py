@@ -65,7 +65,7 @@ def test_sequence_lengths_including_empty_and_tile_edges():
         parity.mla_check(a, res, lam, S)
 
 
-@pytest.mark.parametrize("page_size", [8, 16, 64, 128, 256])
+@pytest.mark.parametrize("page_size", [8, 16, 32, 64, 128, 256])
 def test_paged_cache_matches_contiguous_bitwise_and_oracle(page_size):
     """The paged form reads the same rows through a page table: its map, O and lse
     equal the contiguous form's bit for bit, and the oracle's."""
