@@ -1,7 +1,9 @@
 // api.cu -- the C ABI declared in include/blasst.h: argument validation, the
 // threshold resolution, TMA descriptor encoding and kernel launches.
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <initializer_list>
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -36,16 +38,44 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// Device address of the status word on the current device, looked up once per device.
+// Host threads may make their first calls at the same time: each looks the address up
+// and stores the same value, so an atomic slot is all the synchronisation needed.  The
+// cached address does not survive cudaDeviceReset (the array moves to a new context).
 int* status_word() {
-    static int* ptrs[kMaxDevices] = {};
+    static std::atomic<int*> ptrs[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (!ptrs[dev]) {
+    int* cached = ptrs[dev].load(std::memory_order_acquire);
+    if (!cached) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_blasst_status) != cudaSuccess) return nullptr;
-        ptrs[dev] = static_cast<int*>(p);
+        if (cudaGetSymbolAddress(&p, g_blasst_status) != cudaSuccess || !p) return nullptr;
+        cached = static_cast<int*>(p);
+        ptrs[dev].store(cached, std::memory_order_release);
     }
-    return ptrs[dev];
+    return cached;
+}
+
+// True iff every pointer is device memory of the current device.  The cluster
+// kernels (MLA decode above 64 heads, GQA decode with 128 heads per KV head) multicast
+// their TMA key loads to the CTAs of a cluster; those loads must read this GPU's own
+// memory, so memory of another GPU (peer-mapped or imported), managed memory and host
+// memory are refused.  A failed query counts as a refusal.
+bool local_device_memory(std::initializer_list<const void*> ptrs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return false;
+    }
+    for (const void* p : ptrs) {
+        cudaPointerAttributes a{};
+        if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return false;
+        }
+        if (a.type != cudaMemoryTypeDevice || a.device != dev) return false;
+    }
+    return true;
 }
 
 // [Z][L][d] bf16 viewed as a 3-D tensor (d fastest); boxes of 64 columns x 128 rows,
@@ -176,6 +206,30 @@ bool page_size_ok(int page_size) {
 }
 
 }  // namespace
+
+namespace blasst {
+
+int decode_args_status(const void* q, const void* k_cache, const void* v_cache, const void* o, const float* lse,
+                       int B, int Hq, int Hkv, int Lkv, int d, float scale, float lambda, int num_splits,
+                       const unsigned long long* skipped_tiles_out, const float* margins) {
+    if (!q || !k_cache || !v_cache || !o) return BLASST_ERR_INVALID_ARG;
+    if (B < 1 || Hq < 1 || Hkv < 1 || Lkv < 1 || Hq % Hkv != 0) return BLASST_ERR_INVALID_ARG;
+    if (!scale_ok(scale) || !lambda_ok(lambda)) return BLASST_ERR_INVALID_ARG;
+    const int nT = (Lkv + kTile - 1) / kTile;
+    if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
+    const int G = Hq / Hkv;
+    if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
+    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16 && G != 32 && G != 64 && G != 128)
+        return BLASST_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
+        (reinterpret_cast<uintptr_t>(skipped_tiles_out) & 7u))
+        return BLASST_ERR_UNSUPPORTED;
+    if (Hkv > 65535 || B > 65535) return BLASST_ERR_UNSUPPORTED;
+    return BLASST_OK;
+}
+
+}  // namespace blasst
 
 extern "C" {
 
@@ -317,26 +371,17 @@ int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void*
                   int Hkv, int Lkv, int d, float scale, float lambda, int num_splits, void* workspace,
                   size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
                   float* margins, void* stream) {
-    if (!q || !k_cache || !v_cache || !o) return BLASST_ERR_INVALID_ARG;
-    if (B < 1 || Hq < 1 || Hkv < 1 || Lkv < 1 || Hq % Hkv != 0) return BLASST_ERR_INVALID_ARG;
-    if (!scale_ok(scale) || !lambda_ok(lambda)) return BLASST_ERR_INVALID_ARG;
-    const int nT = (Lkv + kTile - 1) / kTile;
-    if (num_splits < 1 || num_splits > nT) return BLASST_ERR_INVALID_ARG;
-    const int G = Hq / Hkv;
-    if (d != 64 && d != 128) return BLASST_ERR_UNSUPPORTED;
-    if (G != 1 && G != 2 && G != 4 && G != 8 && G != 16 && G != 32 && G != 64 && G != 128)
-        return BLASST_ERR_UNSUPPORTED;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(o)) return BLASST_ERR_UNSUPPORTED;
-    if ((reinterpret_cast<uintptr_t>(lse) & 3u) || (reinterpret_cast<uintptr_t>(margins) & 3u) ||
-        (reinterpret_cast<uintptr_t>(skipped_tiles_out) & 7u))
-        return BLASST_ERR_UNSUPPORTED;
-    if (Hkv > 65535 || B > 65535) return BLASST_ERR_UNSUPPORTED;
+    const int rc = blasst::decode_args_status(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Lkv, d, scale, lambda,
+                                              num_splits, skipped_tiles_out, margins);
+    if (rc != BLASST_OK) return rc;
     const size_t need = blasst_decode_workspace_size(B, Hq, Hkv, Lkv, d, num_splits);
     if (num_splits > 1) {
         if (!workspace) return BLASST_ERR_INVALID_ARG;
         if (workspace_bytes < need) return BLASST_ERR_WORKSPACE_TOO_SMALL;
         if (!aligned16(workspace)) return BLASST_ERR_UNSUPPORTED;
     }
+    // 128 heads per KV head run as clusters whose key loads are multicast
+    if (Hq / Hkv > 64 && !local_device_memory({q, k_cache, v_cache})) return BLASST_ERR_UNSUPPORTED;
 
     CUtensorMap tk, tv;
     if (!encode_3d(&tk, k_cache, d, Lkv, (long long)B * Hkv) || !encode_3d(&tv, v_cache, d, Lkv, (long long)B * Hkv))
@@ -500,6 +545,8 @@ int blasst_mla_decode(const void* q, const void* kv, const int* page_table, cons
         if (workspace_bytes < need) return BLASST_ERR_WORKSPACE_TOO_SMALL;
         if (!aligned16(workspace)) return BLASST_ERR_UNSUPPORTED;
     }
+    // above 64 heads the CTAs of a cluster share key loads by multicast
+    if (Hq > 64 && !local_device_memory({q, kv})) return BLASST_ERR_UNSUPPORTED;
     CUtensorMap tkv, tq;
     const int rows = page_size < kTile ? page_size : kTile;
     // pool rows, and the row past the last page that an out-of-range index reads, fit an int

@@ -13,14 +13,18 @@
 // holds it until the process exits.  Its host-side name is only a stand-in, so the
 // device address is looked up with cudaGetSymbolAddress, once per device, on the
 // first call made with that device current (make that first call before any
-// stream capture).  All calls on a device share the one array: calls whose work
+// stream capture).  Host threads making their first calls at once each look it up
+// and store the same value in an atomic slot.  The cached address does not survive
+// cudaDeviceReset.  All calls on a device share the one array: calls whose work
 // overlaps on the GPU (different streams, or host threads racing) overwrite each
 // other's partial results.  Nothing in it has to start at zero -- each call's split
 // pass writes every partial it later merges.
+#include <atomic>
 #include <cstdint>
 #include <cuda_runtime.h>
 
 #include "blasst.h"
+#include "kernels.cuh"
 
 namespace {
 
@@ -36,22 +40,24 @@ static __device__ __align__(256) float g_decode_scratch[kScratchFloats];
 namespace {
 
 void* scratch_address(int* status) {
-    static void* addr[kMaxDevices] = {};
+    static std::atomic<void*> addr[kMaxDevices] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
         *status = BLASST_ERR_CUDA;
         return nullptr;
     }
-    if (!addr[dev]) {
+    void* cached = addr[dev].load(std::memory_order_acquire);
+    if (!cached) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess || !p) {
             *status = BLASST_ERR_CUDA;
             return nullptr;
         }
-        addr[dev] = p;
+        cached = p;
+        addr[dev].store(cached, std::memory_order_release);
     }
     *status = BLASST_OK;
-    return addr[dev];
+    return cached;
 }
 
 }  // namespace
@@ -62,7 +68,10 @@ extern "C" int blasst_decode_noalloc(const void* q, const void* k_cache, const v
                                      int B, int Hq, int Hkv, int Lkv, int d, float scale, float lambda,
                                      int num_splits, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
                                      float* margins, void* stream) {
-    if (B < 1 || Hq < 1 || Hkv < 1 || Lkv < 1 || d < 1 || num_splits < 1) return BLASST_ERR_INVALID_ARG;
+    // bad arguments are reported as such before the size check
+    const int rc = blasst::decode_args_status(q, k_cache, v_cache, o, lse, B, Hq, Hkv, Lkv, d, scale, lambda,
+                                              num_splits, skipped_tiles_out, margins);
+    if (rc != BLASST_OK) return rc;
     const size_t need = blasst_decode_workspace_size(B, Hq, Hkv, Lkv, d, num_splits);
     if (need > kScratchFloats * sizeof(float)) return BLASST_ERR_SCRATCH_LIMIT;
     void* ws = nullptr;

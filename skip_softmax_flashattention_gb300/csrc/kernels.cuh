@@ -111,5 +111,10 @@ cudaError_t launch_mla_decode(const CUtensorMap& tkv, const CUtensorMap& tq, con
 cudaError_t launch_wide_decode(const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tq,
                                const DecodeParams& p, cudaStream_t stream);
 
+// Host-side validation of blasst_decode's arguments other than the workspace
+// (BLASST_OK or the status blasst_decode returns for them).
+int decode_args_status(const void* q, const void* k_cache, const void* v_cache, const void* o, const float* lse,
+                       int B, int Hq, int Hkv, int Lkv, int d, float scale, float lambda, int num_splits,
+                       const unsigned long long* skipped_tiles_out, const float* margins);
 
 }  // namespace blasst

@@ -206,3 +206,41 @@ def test_mla_split_request_and_workspace_host_logic():
     assert K.blasst_mla_decode_workspace_size(4, 16, 1000, 1) == 0
     o_bytes = 3 * 4 * 16 * 512 * 4
     assert K.blasst_mla_decode_workspace_size(4, 16, 1000, 3) == ((o_bytes + 255) & ~255) + 3 * 4 * 16 * 4
+
+
+# The cluster paths (MLA decode above 64 heads, GQA decode with 128 heads per KV
+# head) multicast their key loads inside a cluster; they accept only device memory
+# of the current GPU.  A host address (here one that is never dereferenced) is
+# refused after argument validation and before any work is enqueued.
+def test_cluster_paths_refuse_memory_not_on_this_gpu():
+    rc = K.blasst_mla_decode(FAKE, FAKE, None, None, FAKE, None, 2, 128, 1000, 576, 512, 0, 0, 0, 0.1, 0.01, 1,
+                             None, 0, None, None, None, stream=0)
+    assert rc == K.BLASST_ERR_UNSUPPORTED
+    rc = K.blasst_mla_decode(FAKE, FAKE, FAKE, None, FAKE, None, 2, 128, 1000, 576, 512, 40, 64, 16, 0.1, 0.01, 1,
+                             None, 0, None, None, None, stream=0)
+    assert rc == K.BLASST_ERR_UNSUPPORTED
+    rc = K.blasst_decode(FAKE, FAKE, FAKE, FAKE, None, 2, 128, 1, 1000, 128, 0.1, 0.01, 1, None, 0, None, None, None,
+                         stream=0)
+    assert rc == K.BLASST_ERR_UNSUPPORTED
+    # validation still comes first: a bad argument is reported as such
+    rc = K.blasst_mla_decode(FAKE, FAKE, None, None, FAKE, None, 2, 128, 1000, 576, 512, 0, 0, 0, 0.1, 2.0, 1,
+                             None, 0, None, None, None, stream=0)
+    assert rc == K.BLASST_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(S=300), K.BLASST_ERR_INVALID_ARG),           # more splits than the 256 key tiles
+    (dict(Hq=96, Hkv=2), K.BLASST_ERR_UNSUPPORTED),    # G = 48
+    (dict(d=96), K.BLASST_ERR_UNSUPPORTED),
+    (dict(lam=1.5), K.BLASST_ERR_INVALID_ARG),
+    (dict(q=None), K.BLASST_ERR_INVALID_ARG),
+    (dict(S=64), K.BLASST_ERR_SCRATCH_LIMIT),          # valid, but the partials exceed the scratch
+])
+def test_noalloc_validates_before_the_scratch_limit(kw, code):
+    # every case but the last is also far beyond the scratch size, so the argument
+    # error must win over BLASST_ERR_SCRATCH_LIMIT
+    a = dict(q=FAKE, B=64, Hq=32, Hkv=8, Lkv=32768, d=128, lam=0.0, S=200)
+    a.update(kw)
+    rc = K.blasst_decode_noalloc(a["q"], FAKE, FAKE, FAKE, None, a["B"], a["Hq"], a["Hkv"], a["Lkv"], a["d"], 0.1,
+                                 a["lam"], a["S"], None, None, None, stream=0)
+    assert rc == code
