@@ -34,10 +34,39 @@ UNIT = "TFLOP/s"
 PREFILL = dict(B=1, Hq=32, Hkv=8, L=16384, d=128)
 DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture of the current kernels; None until captured for this version of the kernels.
-# prefill: prefill2_kernel<128, false> capture (365.6 MB read + 100.3 MB written).
-# decode: decode_kernel<4, false> B=8 capture (1073.9 MB read + 4.0 MB written) x 8 for the B=64 launch.
-TRAFFIC_BYTES = {"prefill": 365569024 + 100312832, "decode": 8 * (1073891000 + 3998976)}
+# capture, with the SHA-256 of the kernel's sources when it was taken.  The line
+# reports the figure only while those sources are unchanged (else traffic is null:
+# the counters belong to another version of the kernel).
+KERNEL_SOURCES = {
+    "prefill": ["csrc/prefill.cu", "csrc/ptx.cuh", "csrc/kernels.cuh"],
+    "decode": ["csrc/decode.cu", "csrc/ptx.cuh", "csrc/kernels.cuh"],
+}
+TRAFFIC = {
+    "prefill": {"bytes": None, "sources_sha256": None, "capture": None},
+    "decode": {"bytes": 8 * (1073936640 + 3331584), "sources_sha256": "82829ad849fca2be004c7210f220a6ae8251b9fdc7390a1fece2d6779c67aecf",
+               "capture": "decode_kernel<4, 0> at B=8 Hq=32 Hkv=8 Lkv=32768 d=128 (7 splits), one launch, "
+                          "dram__bytes_read.sum + dram__bytes_write.sum, scaled x8 by sequences to B=64"},
+}
+
+
+def sources_sha256(kernel):
+    import hashlib
+
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "skip_softmax_flashattention_gb300", rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def traffic_for(kernel):
+    """(bytes or None, note) for the roofline's traffic field."""
+    t = TRAFFIC[kernel]
+    if t["bytes"] is None:
+        return None, "not captured for this version of the kernel"
+    if t["sources_sha256"] != sources_sha256(kernel):
+        return None, "kernel sources changed since the capture (" + t["capture"] + ")"
+    return t["bytes"], t["capture"]
 
 
 def load_peaks():
@@ -246,6 +275,64 @@ def run_reference(args):
     return 0
 
 
+# ----------------------------------------------------------------- skipping points
+def measure_skip_points(K, W, dev, flush, peaks, dcfg, q3):
+    """The workloads' ~70 % sparsity points against the same kernel at lambda = 0:
+    planted-70 prefill (the LLM prefill shapes, non-causal, the last 70 % of key
+    tiles hold K = 0) at lambda = 1e-2, and the bench's decode at the threshold
+    whose sparsity is 70 % by the lambda = 0 margins (read off with calibrate)."""
+    import torch
+
+    from skip_softmax_flashattention_gb300 import calibrate
+
+    out = {}
+    a = W.planted70(seed=0, L=PREFILL["L"], device=dev)
+    nQ, nK = -(-a.Lq // 128), -(-a.Lkv // 128)
+    visited = nQ * nK * a.B * a.Hq
+    dense = 4.0 * a.B * a.Hq * a.d * a.Lq * a.Lkv
+    o = torch.empty_like(a.q)
+    ms, skip = {}, {}
+    for lam in (0.0, 1e-2):
+        r = K.prefill(a.q, a.k, a.v, False, a.scale, lam, out=o)
+        torch.cuda.synchronize()
+        skip[lam] = int(r["skipped"].item())
+        ms[lam] = _time_ms(lambda: K.prefill(a.q, a.k, a.v, False, a.scale, lam, out=o), flush)
+    ex = 2.0 * 128 * 128 * a.d * (2 * visited - skip[1e-2])
+    out["prefill_planted70"] = {
+        "workload": "planted70 B=1 Hq=32 Hkv=8 L=16384 d=128 non-causal", "lambda": 1e-2,
+        "skip_pct": 100.0 * skip[1e-2] / visited, "ms": ms[1e-2], "ms_lambda0": ms[0.0],
+        "speedup_vs_lambda0": ms[0.0] / ms[1e-2],
+        "flop_bound_speedup": 2.0 * visited / (2.0 * visited - skip[1e-2]),
+        "dense_tflops": dense / (ms[1e-2] * 1e-3) / 1e12, "executed_tflops": ex / (ms[1e-2] * 1e-3) / 1e12,
+        "executed_frac_of_measured_bf16": ex / (ms[1e-2] * 1e-3) / 1e12 / peaks["bf16_tflops"]}
+    del a, o, r
+    torch.cuda.empty_cache()
+
+    r0 = K.decode(q3, dcfg.k, dcfg.v, dcfg.scale, 0.0, want_margins=True)
+    torch.cuda.synchronize()
+    S = r0["num_splits"]
+    lam70 = calibrate.lambda_for_sparsity(r0["margins"].cpu().numpy(), 0.70)
+    tiles = dcfg.B * dcfg.Hkv * (-(-dcfg.Lkv // 128))
+    ms, skip = {}, {}
+    for lam in (0.0, lam70):
+        r = K.decode(q3, dcfg.k, dcfg.v, dcfg.scale, lam, num_splits=S)
+        torch.cuda.synchronize()
+        skip[lam] = int(r["skipped"].item())
+        ms[lam] = _time_ms(lambda: K.decode(q3, dcfg.k, dcfg.v, dcfg.scale, lam, num_splits=S), flush)
+    tile_bytes = 128 * dcfg.d * 2
+    kv = tile_bytes * (2 * tiles - skip[lam70])
+    out["decode_70pct"] = {
+        "workload": "split-kv-decode B=64 Hq=32 Hkv=8 Lkv=32768 d=128", "splits": S, "lambda": lam70,
+        "lambda_rule": "smallest threshold whose sparsity by the lambda=0 margins is >= 70 %",
+        "skip_pct": 100.0 * skip[lam70] / tiles, "ms": ms[lam70], "ms_lambda0": ms[0.0],
+        "speedup_vs_lambda0": ms[0.0] / ms[lam70],
+        "byte_bound_speedup": 2.0 * tiles / (2.0 * tiles - skip[lam70]),
+        "kv_gbs": kv / (ms[lam70] * 1e-3) / 1e9,
+        "frac_of_measured_hbm": kv / (ms[lam70] * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+    out["timing"] = "CUDA events, 512 MB L2 flush before each launch, median of 10 after 3 warm-up launches"
+    return out
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args):
     import numpy as np
@@ -347,6 +434,8 @@ def run_ours(args):
     dense_flop = 4.0 * P["B"] * P["Hq"] * P["d"] * pairs
     visited = visited_tiles_causal(L, L) * P["B"] * P["Hq"]
     exec_flop = 2.0 * 128 * 128 * P["d"] * (2 * visited - n_skip_p)
+    # prefill algorithmic bytes: Q, K, V read once, O and lse written once
+    prefill_alg_bytes = (a.q.numel() + a.k.numel() + a.v.numel() + o.numel()) * 2 + lse.numel() * 4
     p_mean = sum(p_ms) / len(p_ms)
     d_mean = sum(d_ms) / len(d_ms)
     p_max = max_over_ranks(pg, p_mean)
@@ -422,6 +511,40 @@ def run_ours(args):
     h2d = qh.numel() * 2 + kh.numel() * 2 + vh.numel() * 2
     d2h = oh[0].numel() * 2 + lseh[0].numel() * 4
 
+    # ---- the same call with each step's copies and kernel serialised on one stream
+    # (the latency of one call with host buffers; the pipelined figure above is the
+    # throughput of a loop of them)
+    for i in range(max(1, args.warmup)):
+        qd[0].copy_(qh, non_blocking=True)
+        kd[0].copy_(kh, non_blocking=True)
+        vd[0].copy_(vh, non_blocking=True)
+        assert K.blasst_prefill(qd[0], kd[0], vd[0], od[0], lsed[0], P["B"], P["Hq"], P["Hkv"], L, L, P["d"], 1,
+                                a.scale, lam_p(), skipped_p, stream) == 0
+        oh[0].copy_(od[0], non_blocking=True)
+        lseh[0].copy_(lsed[0], non_blocking=True)
+    torch.cuda.synchronize()
+    e_s.record(stream)
+    for i in range(args.steps):
+        qd[0].copy_(qh, non_blocking=True)
+        kd[0].copy_(kh, non_blocking=True)
+        vd[0].copy_(vh, non_blocking=True)
+        assert K.blasst_prefill(qd[0], kd[0], vd[0], od[0], lsed[0], P["B"], P["Hq"], P["Hkv"], L, L, P["d"], 1,
+                                a.scale, lam_p(), skipped_p, stream) == 0
+        oh[0].copy_(od[0], non_blocking=True)
+        lseh[0].copy_(lsed[0], non_blocking=True)
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_serial_ms = max_over_ranks(pg, e_s.elapsed_time(e_e) / args.steps)
+    e2e_serial_value = sum_over_ranks(pg, dense_flop / (e2e_serial_ms * 1e-3) / 1e12)
+    del qd, kd, vd, od, lsed
+    torch.cuda.empty_cache()
+
+    # ---- skipping points: each workload timed at ~70 % tile sparsity and at lambda = 0
+    # with the same kernel (CUDA events, L2 flushed, median of 10)
+    skip_points = None
+    if not args.no_skip_points:
+        skip_points = measure_skip_points(K, W, dev, flush, peaks, dcfg, q3)
+
     # ---- CPU baseline: the oracle on a bounded sample of the same prefill workload
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -439,13 +562,17 @@ def run_ours(args):
                          f"{secs:.1f} s of fp32 oracle time"}
 
     ach = exec_flop / (p_max * 1e-3) / 1e12
+    tr_p, tr_p_note = traffic_for("prefill")
+    tr_d, tr_d_note = traffic_for("decode")
     roof = {"bound": "tensor", "kernel": "prefill2_kernel<128, false> (two query tiles per CTA)", "achieved": ach,
             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": ach / peaks["bf16_tflops"],
             "peak_source": peaks["source"] + " burst bf16",
-            "traffic": TRAFFIC_BYTES["prefill"]}
+            "traffic": tr_p, "traffic_source": tr_p_note,
+            "algorithmic_bytes": prefill_alg_bytes}
     roof_d = {"bound": "hbm", "kernel": "decode_kernel<4, false> + combine", "achieved": dec_gbs,
               "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dec_gbs / peaks["hbm_gbs"],
-              "peak_source": peaks["source"] + " HBM copy", "traffic": TRAFFIC_BYTES["decode"]}
+              "peak_source": peaks["source"] + " HBM copy", "traffic": tr_d, "traffic_source": tr_d_note,
+              "algorithmic_bytes": kv_bytes + other_bytes}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": max_over_ranks(pg, sum(step_ms) / len(step_ms)),
@@ -468,7 +595,10 @@ def run_ours(args):
         "roofline": roof, "roofline_decode": roof_d,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_ms},
+                "ms_per_step": e2e_ms, "mode": "steps pipelined over two buffer sets and three streams",
+                "serialised": {"value": e2e_serial_value, "unit": UNIT, "ms_per_step": e2e_serial_ms,
+                               "mode": "copy in, kernel, copy out on one stream, step after step"}},
+        "skip_points": skip_points,
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
@@ -730,6 +860,7 @@ def main():
     ap.add_argument("--lam-a", type=float, default=40.0, help="lambda = a / Lkv (the LLM workloads' rule)")
     ap.add_argument("--threshold", type=float, default=None, help="use lambda = threshold instead")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-skip-points", action="store_true", help="leave out the ~70 %% sparsity points")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-units", type=int, default=16)
     ap.add_argument("--only", choices=["prefill", "decode", "mla"], default=None,

@@ -230,6 +230,59 @@ def mla_check(a, res, lam, S, seqs=None, log=None):
     return band_total
 
 
+def oracle_map_at(margin, lam):
+    """The oracle's own decisions at threshold lam, read off the margins of its fp32
+    pass: a visited tile is skipped iff its margin (max over the voting rows of
+    m~ - m) is below ln(lam) rounded to fp32 -- the very comparison of the oracle's
+    test, row by row, since max_r x_r < t iff x_r < t for every r.  The margins do
+    not depend on lam <= 1 (a skip never moves the running max), so one lam = 0
+    pass decides every threshold.  Not visited: 2."""
+    g = np.asarray(margin, np.float32)
+    lnl = np.float32(-np.inf) if lam <= 0 else np.float32(math.log(lam))
+    out = np.full(g.shape, 2, np.uint8)
+    vis = ~np.isnan(g)
+    out[vis] = (g[vis] < lnl).astype(np.uint8)
+    return out
+
+
+def margins_check(g_gpu, g_ref, what, tol=BAND):
+    """GPU margins against the oracle's: the same not-visited (NaN) and +inf tiles,
+    finite values within tol."""
+    g_gpu = np.asarray(g_gpu, np.float64)
+    g_ref = np.asarray(g_ref, np.float64)
+    assert np.array_equal(np.isnan(g_gpu), np.isnan(g_ref)), f"{what}: visited tiles differ"
+    assert np.array_equal(np.isposinf(g_gpu), np.isposinf(g_ref)), f"{what}: +inf margins differ"
+    fin = np.isfinite(g_ref)
+    assert np.array_equal(fin, np.isfinite(g_gpu)), f"{what}: finite margins differ"
+    if fin.any():
+        err = float(np.abs(g_gpu[fin] - g_ref[fin]).max())
+        assert err < tol, f"{what}: margin abs err {err:.3e} >= {tol}"
+
+
+def whole_check(what, lam, res, own0, forced_run, log=None):
+    """Whole-problem acceptance for one threshold from one lam = 0 oracle pass.
+
+    res: the GPU result (map, skipped, o, lse); own0: the oracle's lam = 0 pass over
+    the same problem (margins, and O/lse with every tile computed); forced_run(map):
+    the oracle with the GPU's map forced, run only when the GPU skipped a tile.
+    Checks every decision outside the 1e-3 band, the exact skipped count, O and lse.
+    Returns (#band tiles, GPU count)."""
+    gmap = res["map"].cpu().numpy()
+    omap = oracle_map_at(own0["margin"], lam)
+    band = _decisions(gmap, omap, own0["margin"], lam, what)
+    n_gpu = int(res["skipped"].item())
+    assert n_gpu == int((gmap == 1).sum()), f"{what}: reported count differs from the map"
+    n_ora = int((omap == 1).sum())
+    assert abs(n_gpu - n_ora) <= band, f"{what}: count {n_gpu} vs oracle {n_ora} (band {band})"
+    if band == 0:
+        assert n_gpu == n_ora, f"{what}: count {n_gpu} vs oracle {n_ora}"
+    ref = forced_run(gmap) if (gmap == 1).any() else own0
+    _check_rows(res["o"].float().cpu().numpy(), res["lse"].cpu().numpy(), ref["o"], ref["lse"], what)
+    if log is not None and band:
+        log.append(f"{what}: {band} tiles inside the 1e-3 margin band")
+    return band, n_gpu
+
+
 def sample_units(rng, B, H, nQ, k, always=()):
     """k random (b, h, qtile) units plus the listed ones (first/last tiles)."""
     units = set(always)

@@ -111,3 +111,55 @@ def test_decode_wide_group_full_size_sampled():
         parity.decode_units_check(a, res, lam, res["num_splits"], [(0, 0), (63, 0)])
     del a, res
     torch.cuda.empty_cache()
+
+
+MARGIN_SHAPES = [
+    # B, Hq, Hkv, Lkv, d, S
+    (2, 8, 2, 1000, 128, 3),
+    (3, 4, 4, 129, 128, 1),
+    (1, 16, 1, 5000, 128, 5),
+    (2, 8, 2, 777, 64, 2),
+    (2, 32, 1, 1000, 128, 2),    # wide group, one CTA
+    (1, 128, 1, 600, 128, 2),    # wide group, cluster of two
+]
+
+
+@pytest.mark.parametrize("shape", MARGIN_SHAPES, ids=[str(s) for s in MARGIN_SHAPES])
+def test_decode_margins_match_oracle(shape):
+    """The decode margins (what threshold calibration reads) against the oracle's, tile
+    by tile; at lambda = 0 the margins are the same for every threshold."""
+    from oracle import oracle as orc
+
+    B, Hq, Hkv, L, d, S = shape
+    a = parity.to_gpu(W.decode(seed=41, B=B, Hq=Hq, Hkv=Hkv, Lkv=L, d=d))
+    res = K.decode(a.q, a.k, a.v, a.scale, 0.0, num_splits=S, want_map=True, want_margins=True)
+    torch.cuda.synchronize()
+    own = orc.decode_tiled(a.q.float().cpu(), a.k.float().cpu(), a.v.float().cpu(), a.scale, 0.0, num_splits=S,
+                           precision="f32")
+    parity.margins_check(res["margins"].cpu().numpy(), own["margin"], f"decode margins {shape}")
+    # and a threshold taken from them skips exactly the oracle's tiles (outside the band)
+    from skip_softmax_flashattention_gb300 import calibrate
+
+    lam = calibrate.lambda_for_sparsity(own["margin"], 0.5)
+    r2 = K.decode(a.q, a.k, a.v, a.scale, lam, num_splits=S, want_map=True)
+    torch.cuda.synchronize()
+    parity.decode_full_check(a, r2, lam, S)
+
+
+def test_decode_margins_full_size_sampled():
+    """The bench's decode workload: margins of sampled (sequence, KV head) units against
+    the oracle (the 70 % threshold of the bench is read off these margins)."""
+    from oracle import oracle as orc
+
+    a = parity.to_gpu(W.decode(seed=0, device="cuda"))
+    res = K.decode(a.q, a.k, a.v, a.scale, 0.0, want_map=True, want_margins=True)
+    torch.cuda.synchronize()
+    S = res["num_splits"]
+    g = res["margins"].cpu().numpy()
+    G = a.Hq // a.Hkv
+    for (b, hk) in [(0, 0), (17, 3), (63, 7)]:
+        own = orc.decode_tiled(a.q[b:b + 1, hk * G:(hk + 1) * G].float().cpu(), a.k[b:b + 1, hk:hk + 1].float().cpu(),
+                               a.v[b:b + 1, hk:hk + 1].float().cpu(), a.scale, 0.0, num_splits=S, precision="f32")
+        parity.margins_check(g[b:b + 1, hk:hk + 1], own["margin"], f"decode margins b={b} hkv={hk}")
+    del a, res
+    torch.cuda.empty_cache()

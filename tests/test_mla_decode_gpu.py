@@ -192,3 +192,30 @@ def test_bad_page_index_and_length_are_contained_and_reported(Hq):
     res = _run(a, 0.03, 2, page=True)
     torch.cuda.synchronize()
     parity.mla_check(a, res, 0.03, 2)
+
+
+def test_cluster_paths_refuse_host_and_managed_memory():
+    """The cluster kernels multicast key loads and accept only device memory of the
+    current GPU: pinned host memory is refused before any work is enqueued, while
+    the same data in device memory runs."""
+    K.blasst_device_status(1)
+    a = W.mla_decode(seed=5, B=1, Hq=128, L=300, device="cuda", q_shared=6.0, sink_norm=32.0)
+    kv = a.extra["kv"]
+    kv_host = kv.cpu().pin_memory()
+    o = torch.empty(1, 128, 512, device="cuda", dtype=torch.bfloat16)
+    rc = K.blasst_mla_decode(a.q, kv_host, None, None, o, None, 1, 128, 300, 576, 512, 0, 0, 0, a.scale, 0.1, 1,
+                             None, 0, None, None, None)
+    assert rc == K.BLASST_ERR_UNSUPPORTED
+    rc = K.blasst_mla_decode(a.q, kv, None, None, o, None, 1, 128, 300, 576, 512, 0, 0, 0, a.scale, 0.1, 1,
+                             None, 0, None, None, None)
+    assert rc == K.BLASST_OK
+    d = W.decode(seed=6, B=1, Hq=128, Hkv=1, Lkv=300, device="cuda")
+    q3 = d.q.reshape(1, 128, 128)
+    od = torch.empty(1, 128, 128, device="cuda", dtype=torch.bfloat16)
+    rc = K.blasst_decode(q3, d.k.cpu().pin_memory(), d.v, od, None, 1, 128, 1, 300, 128, d.scale, 0.1, 1, None, 0,
+                         None, None, None)
+    assert rc == K.BLASST_ERR_UNSUPPORTED
+    rc = K.blasst_decode(q3, d.k, d.v, od, None, 1, 128, 1, 300, 128, d.scale, 0.1, 1, None, 0, None, None, None)
+    assert rc == K.BLASST_OK
+    torch.cuda.synchronize()
+    assert K.blasst_device_status(1) == K.BLASST_OK

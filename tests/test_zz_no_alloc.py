@@ -12,6 +12,7 @@ import torch
 
 from skip_softmax_flashattention_gb300 import blasst as K
 from skip_softmax_flashattention_gb300 import workloads as W
+from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -31,6 +32,13 @@ def _run_noalloc(a, lam, S):
     assert rc == K.BLASST_OK, K.blasst_status_string(rc)
     torch.cuda.synchronize()
     return o, lse, skipped, mp
+
+
+def _compare_oracle(a, lam, S, got):
+    """The no-alloc result against the CPU oracle: every tile decision (outside the
+    1e-3 margin band), the exact skipped count, O and lse."""
+    o, lse, skipped, mp = got
+    parity.decode_full_check(a, {"o": o, "lse": lse, "skipped": skipped, "map": mp}, lam, S)
 
 
 def _compare(ref, got):
@@ -56,6 +64,50 @@ def test_noalloc_matches_workspace_decode_on_consecutive_calls():
     _compare(ref2, _run_noalloc(second, lam, S))
     # and once more on the first input
     _compare(ref1, _run_noalloc(first, lam, S))
+    assert K.blasst_device_status(1) == K.BLASST_OK
+
+
+def test_noalloc_matches_the_oracle():
+    torch.cuda.set_device(0)
+    K.blasst_device_status(1)
+    a = W.decode(seed=33, B=3, Hq=16, Hkv=4, Lkv=1500, device="cuda")
+    for lam, S in ((0.0, 3), (0.3, 3), (0.3, 1)):
+        _compare_oracle(a, lam, S, _run_noalloc(a, lam, S))
+    assert K.blasst_device_status(1) == K.BLASST_OK
+
+
+def test_noalloc_wide_group_head_dim_64():
+    """32 query heads per KV head (the wide-group kernel, which also writes its split
+    partials to the scratch) at head dim 64."""
+    torch.cuda.set_device(0)
+    K.blasst_device_status(1)
+    a = W.decode(seed=34, B=2, Hq=64, Hkv=2, Lkv=1000, d=64, device="cuda")
+    for lam in (0.0, 0.3):
+        got = _run_noalloc(a, lam, 3)
+        ref = K.decode(a.q, a.k, a.v, a.scale, lam, num_splits=3, want_map=True)
+        torch.cuda.synchronize()
+        _compare(ref, got)
+        _compare_oracle(a, lam, 3, got)
+    assert K.blasst_device_status(1) == K.BLASST_OK
+
+
+def test_noalloc_large_call_then_smaller_call():
+    """A call that fills much of the scratch (8 splits) followed by a smaller one (2
+    splits, other inputs, other shape): the smaller call must read only its own
+    partials, not what the larger one left behind."""
+    torch.cuda.set_device(0)
+    K.blasst_device_status(1)
+    big = W.decode(seed=35, B=8, Hq=32, Hkv=8, Lkv=4096, device="cuda")
+    small = W.decode(seed=36, B=5, Hq=16, Hkv=4, Lkv=2000, device="cuda")
+    lam = 0.2
+    assert K.blasst_decode_workspace_size(big.B, big.Hq, big.Hkv, big.Lkv, big.d, 8) > \
+        K.blasst_decode_workspace_size(small.B, small.Hq, small.Hkv, small.Lkv, small.d, 2)
+    _compare_oracle(big, lam, 8, _run_noalloc(big, lam, 8))
+    got = _run_noalloc(small, lam, 2)
+    _compare_oracle(small, lam, 2, got)
+    ref = K.decode(small.q, small.k, small.v, small.scale, lam, num_splits=2, want_map=True)
+    torch.cuda.synchronize()
+    _compare(ref, got)
     assert K.blasst_device_status(1) == K.BLASST_OK
 
 
