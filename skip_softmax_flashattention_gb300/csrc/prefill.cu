@@ -446,11 +446,13 @@ struct Prefill2Ctrl {
     uint64_t q_full;
     uint64_t k_full[NK], v_full[NV];
     uint64_t rel[2][NR];
-    uint64_t p_full[2][2];  // p_full[w][h]: half h (keys 64h..64h+63) of P_w stored
+    uint64_t p_full[2][2];  // p_full[w][h]: half h (keys 64h..64h+63) of P_w stored (computed tiles only)
+    uint64_t vote[2];       // vote[w]: the four softmax warps of tile w have voted on the current key tile
     uint64_t never;
     uint32_t tmem_base;
     int keep[2];  // keep[w] = j+1 once a warp of tile w keeps key tile j (only grows)
     int dec[2];   // V elision: 2(j+1) + kept, tile w's decision on key tile j, from its issuer (only grows)
+    int v_issued; // V tiles the V producer has issued (or completed without data); only grows
     int abort;
     int turn;       // which issuer may put its next group of MMAs into the tensor queue
     int active[2];  // issuer w still has key tiles to process
@@ -539,11 +541,13 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < Ctrl::NR; ++i) mbar_init(&ctrl->rel[w][i], 1);
             mbar_init(&ctrl->p_full[w][0], 4);
             mbar_init(&ctrl->p_full[w][1], 4);
+            mbar_init(&ctrl->vote[w], 4);
             ctrl->keep[w] = 0;
             ctrl->dec[w] = 0;
         }
         mbar_init(&ctrl->never, 1);
         ctrl->abort = 0;
+        ctrl->v_issued = 0;
         ctrl->turn = nvis[0] > 0 ? 0 : 1;
         ctrl->active[0] = nvis[0] > 0;
         ctrl->active[1] = nvis[1] > 0;
@@ -561,28 +565,36 @@ __global__ void __launch_bounds__(384, 1)
     const Watchdog wd{&ctrl->abort, p.status, p.watchdog_ns};
     if (warp >= 8) {
       regs_dec<kRegsProducer2>();
-      if (warp == 8) {
-        // ------------------------------------------------------------ TMA producer
+      if (warp == 8 || warp == 11) {
+        // ------------------------------------------------------------ TMA producers
+        // Warp 8 loads Q and the K tiles, warp 11 the V tiles (lane 0 of each), so a K
+        // load never queues behind the wait for a V slot.
+        const bool kq = warp == 8;
         if (lane == 0 && N > 0) {
-            tma_prefetch_desc(&tq);
-            tma_prefetch_desc(&tk);
-            tma_prefetch_desc(&tv);
+            if (kq) {
+                tma_prefetch_desc(&tq);
+                tma_prefetch_desc(&tk);
+            } else {
+                tma_prefetch_desc(&tv);
+            }
             const int zq = b * p.Hq + h, zkv = b * p.Hkv + hk;
-            const int nq = (nvis[0] > 0) + (nvis[1] > 0);
-            mbar_arrive_expect_tx(&ctrl->q_full, nq * C::TILE_BYTES);
+            if (kq) {
+                const int nq = (nvis[0] > 0) + (nvis[1] > 0);
+                mbar_arrive_expect_tx(&ctrl->q_full, nq * C::TILE_BYTES);
 #pragma unroll
-            for (int w = 0; w < 2; ++w) {
-                if (nvis[w] == 0) continue;
+                for (int w = 0; w < 2; ++w) {
+                    if (nvis[w] == 0) continue;
 #pragma unroll
-                for (int x = 0; x < D / 64; ++x)
-                    tma_load_3d(smem + C::OFF_Q + w * C::TILE_BYTES + x * C::BOX_BYTES, &tq, &ctrl->q_full, x * 64,
-                                (2 * pi + w) * kTile, zq);
+                    for (int x = 0; x < D / 64; ++x)
+                        tma_load_3d(smem + C::OFF_Q + w * C::TILE_BYTES + x * C::BOX_BYTES, &tq, &ctrl->q_full,
+                                    x * 64, (2 * pi + w) * kTile, zq);
+                }
             }
             // A slot is reused once every query tile that read its previous occupant is done
             // with it: K_m by QK_w(m), covered by commit m of issuer w; V_m by PV_w(m), covered
             // by commit m+1.
             constexpr int NR = Ctrl::NR;
-            int issued_k = 0, issued_v = 0;
+            int issued = 0;
             auto load_k = [&](int m) -> bool {
                 const int ks = m % C::NK;
                 if (m >= C::NK) {
@@ -599,7 +611,7 @@ __global__ void __launch_bounds__(384, 1)
                 for (int x = 0; x < D / 64; ++x)
                     tma_load_3d(smem + C::OFF_K + ks * C::TILE_BYTES + x * C::BOX_BYTES, &tk, &ctrl->k_full[ks],
                                 x * 64, (base + m) * kTile, zkv);
-                issued_k = m + 1;
+                issued = m + 1;
                 return true;
             };
             auto load_v = [&](int m) -> bool {
@@ -613,13 +625,17 @@ __global__ void __launch_bounds__(384, 1)
                             !mbar_wait(&ctrl->rel[w][(unsigned)(jp + 1) % NR], ((unsigned)(jp + 1) / NR) & 1u, wd))
                             return false;
                     }
+                    // The slot's previous copy must have landed before the slot's barrier is
+                    // armed again: an issuer whose tile skipped key tile `prev` released the
+                    // slot without waiting for it.
+                    if (!mbar_wait(&ctrl->v_full[vs], ((unsigned)prev / C::NV) & 1u, wd)) return false;
                 }
                 bool need = true;
                 if (p.elide_v) {
                     // V_m is needed only if a query tile keeps key tile m.  Tile w's issuer
-                    // publishes its decision as dec[w] = 2(m+1) + kept; tile w cannot pass key
-                    // tile m before v_full of V_m completes (its issuer waits for it), so
-                    // dec[w] stops there.  A word that only grows, unlike a barrier phase,
+                    // publishes its decision as dec[w] = 2(m+1) + kept; with V elision every
+                    // issuer waits for v_full of V_m (loaded or not) before it passes key tile
+                    // m, so dec[w] stops there.  A word that only grows, unlike a barrier phase,
                     // may be read for any key tile without having watched the earlier ones:
                     // tile B is asked only when tile A does not keep the tile.
                     need = false;
@@ -641,26 +657,23 @@ __global__ void __launch_bounds__(384, 1)
                 } else {
                     mbar_arrive(&ctrl->v_full[vs]);  // completes the slot's phase without data
                 }
-                issued_v = m + 1;
+                issued = m + 1;
+                reinterpret_cast<volatile int*>(&ctrl->v_issued)[0] = m + 1;
                 return true;
             };
-            if (!p.elide_v) {
+            if (kq) {
                 for (int j = 0; j < N; ++j)
-                    if (!load_k(j) || !load_v(j)) break;
+                    if (!load_k(j)) break;
+                mbar_wait_drain(&ctrl->q_full, 0, kDrainNs);
+                for (int j = max(0, issued - C::NK); j < issued; ++j)
+                    mbar_wait_drain(&ctrl->k_full[j % C::NK], (j / C::NK) & 1, kDrainNs);
             } else {
-                // V loads wait for the votes, so K runs NK-1 tiles ahead of them
-                bool ok = true;
-                int jk = 0;
-                for (int j = 0; j < N && ok; ++j) {
-                    for (; ok && jk < N && jk <= j + C::NK - 1; ++jk) ok = load_k(jk);
-                    ok = ok && load_v(j);
-                }
+                for (int j = 0; j < N; ++j)
+                    if (!load_v(j)) break;
+                // every V copy before the last NV was waited for at its slot's reuse
+                for (int j = max(0, issued - C::NV); j < issued; ++j)
+                    mbar_wait_drain(&ctrl->v_full[j % C::NV], (j / C::NV) & 1, kDrainNs);
             }
-            mbar_wait_drain(&ctrl->q_full, 0, kDrainNs);
-            for (int j = max(0, issued_k - C::NK); j < issued_k; ++j)
-                mbar_wait_drain(&ctrl->k_full[j % C::NK], (j / C::NK) & 1, kDrainNs);
-            for (int j = max(0, issued_v - C::NV); j < issued_v; ++j)
-                mbar_wait_drain(&ctrl->v_full[j % C::NV], (j / C::NV) & 1, kDrainNs);
         }
     } else if (warp == 9 || warp == 10) {
         // ------------------------------------------------------------ MMA issuers (warp 9: tile A, warp 10: tile B)
@@ -711,15 +724,22 @@ __global__ void __launch_bounds__(384, 1)
             // The two issuers alternate groups (PV_w(j) + QK_w(j+1)) so that the tensor
             // queue runs PV_A, QK_A, PV_B, QK_B, ... and the two softmaxes stay half a
             // period apart; an issuer waits for its turn only while the other is active.
+            // (MMAs that two threads issue at once are interleaved by the tensor core, which
+            // delays both groups: measured 24 % slower without turns.)  The wait is a tight
+            // poll of the turn word -- the hand-over gaps the tensor core while it runs --
+            // with the limit checked every 256 polls.
             auto take_turn = [&]() -> bool {
                 if (*turn == w || !active[1 - w]) return true;
                 const uint64_t t0 = globaltimer_ns();
+                uint32_t it = 0;
                 while (*turn != w && active[1 - w]) {
-                    if (*wd.abort_flag) return false;
-                    if (globaltimer_ns() - t0 > wd.limit_ns) {
-                        *wd.abort_flag = 1;
-                        atomicOr(wd.status, kStatusTimeout);
-                        return false;
+                    if ((++it & 255u) == 0) {
+                        if (*wd.abort_flag) return false;
+                        if (globaltimer_ns() - t0 > wd.limit_ns) {
+                            *wd.abort_flag = 1;
+                            atomicOr(wd.status, kStatusTimeout);
+                            return false;
+                        }
                     }
                 }
                 return true;
@@ -730,14 +750,27 @@ __global__ void __launch_bounds__(384, 1)
             for (int j = 0; j < n && ok; ++j) {
                 const int ij = sw + j;
                 const int vs = ij % C::NV;
-                if (!(ok = mbar_wait(&ctrl->p_full[w][0], j & 1, wd))) break;
+                // While the softmax works on S_j: K_(j+1) for the next QK, and V_j issued.  A
+                // skipped tile needs no more of V_j than that: the V producer has then consumed
+                // the release of V_(j-NV), so this issuer stays within two commits of the
+                // release the producer waits for next (the release ring holds NR > 2 entries).
+                if (j + 1 < n && !(ok = mbar_wait(&ctrl->k_full[(ij + 1) % C::NK], ((ij + 1) / C::NK) & 1, wd))) break;
+                if (!p.elide_v) {
+                    int vi = 0;
+                    if (!(ok = spin_until_ge(&ctrl->v_issued, ij + 1, vi, wd))) break;
+                }
                 // all four warps have voted: the tile is kept iff one of them raised keep[w] to j+1
+                if (!(ok = mbar_wait_spin(&ctrl->vote[w], j & 1, wd))) break;
                 const bool skip = reinterpret_cast<volatile int*>(ctrl->keep)[w] <= j;
                 if (p.elide_v) reinterpret_cast<volatile int*>(ctrl->dec)[w] = 2 * (j + 1) + (skip ? 0 : 1);
-                // V_j must have landed before its slot is released, also when the tile is skipped
-                if (!(ok = mbar_wait(&ctrl->v_full[vs], (ij / C::NV) & 1, wd))) break;
-                if (j + 1 < n && !(ok = mbar_wait(&ctrl->k_full[(ij + 1) % C::NK], ((ij + 1) / C::NK) & 1, wd))) break;
-                if (!(ok = take_turn())) break;
+                // V_j itself is read only by a computed tile's P.V.  With V elision the producer
+                // reads the decision words, which must not run past a key tile whose V phase is
+                // still open, so there every tile waits for V_j's phase.
+                if ((!skip || p.elide_v) && !(ok = mbar_wait(&ctrl->v_full[vs], (ij / C::NV) & 1, wd))) break;
+                // a computed tile's first P half (the barrier's phases count computed tiles only)
+                if (!skip && !(ok = mbar_wait_spin(&ctrl->p_full[w][0], npv & 1, wd))) break;
+                // a skipped tile's group is a lone QK: it goes into the queue without its turn
+                if (!skip && !(ok = take_turn())) break;
                 tc_fence_after();
                 if (!skip) issue_pv_half(vs, 0, npv == 0);
                 // the tile's record, written while the tensor core works through the queued MMAs
@@ -747,15 +780,15 @@ __global__ void __launch_bounds__(384, 1)
                     const volatile float* mr = ctrl->mred[w][j & 1];
                     p.margins[mapbase + j] = fmaxf(fmaxf(mr[0], mr[1]), fmaxf(mr[2], mr[3])) * p.scale;
                 }
-                if (!(ok = mbar_wait(&ctrl->p_full[w][1], j & 1, wd))) break;
-                tc_fence_after();
                 if (!skip) {
+                    if (!(ok = mbar_wait_spin(&ctrl->p_full[w][1], npv & 1, wd))) break;
+                    tc_fence_after();
                     issue_pv_half(vs, 1, npv == 0);
                     ++npv;
                 }
                 if (j + 1 < n) issue_qk(ij + 1);
-                commit();  // commit j+1: PV_w(j) and QK_w(j+1)
-                *turn = 1 - w;
+                *turn = 1 - w;  // the group is queued: the other issuer may go on
+                commit();       // commit j+1: PV_w(j) and QK_w(j+1)
             }
             active[w] = 0;
             *turn = 1 - w;
@@ -818,6 +851,12 @@ __global__ void __launch_bounds__(384, 1)
             // vote to skip wait there for the other warps.  keep[w] only grows, and key
             // tile j+1 starts after every warp has finished tile j, so it needs no reset.
             // The MMA issuer reads the same word and writes the tile's record.
+            // Lane 0 of every warp also arrives on vote[w], which is how the MMA issuer learns
+            // the decision (a skipped tile needs no other signal from the softmax): a warp
+            // that votes to skip right away, a warp that keeps the tile just before it
+            // signals P's first half (the issuer needs no earlier word of a kept tile, and
+            // the arrive, with release order after the keep store, then stays off the path
+            // from the vote to the exponentials).
             const unsigned all = __all_sync(0xffffffffu, vote_skip);
             bool skip = false;
             if (!all) {
@@ -826,6 +865,7 @@ __global__ void __launch_bounds__(384, 1)
                 __syncwarp();
                 named_bar_arrive(1 + w, 128);
             } else {
+                mbar_arrive_if(&ctrl->vote[w], lane == 0);
                 named_bar_sync(1 + w, 128);
                 skip = reinterpret_cast<volatile int*>(ctrl->keep)[w] <= j;
             }
@@ -864,6 +904,7 @@ __global__ void __launch_bounds__(384, 1)
                         tmem_st_wait();
                         tc_fence_before();
                         __syncwarp();
+                        mbar_arrive_if(&ctrl->vote[w], lane == 0 && !all);
                         mbar_arrive_if(&ctrl->p_full[w][0], lane == 0);
                         fence_regs<64>(xr + 64);  // keep the second half's math after the signal
                     }
@@ -874,12 +915,6 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 __syncwarp();
                 mbar_arrive_if(&ctrl->p_full[w][1], lane == 0);
-            } else {
-                __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&ctrl->p_full[w][0]);
-                    mbar_arrive(&ctrl->p_full[w][1]);
-                }
             }
         }
 

@@ -110,6 +110,37 @@ __device__ __forceinline__ bool spin_until_ge(const int* addr, int target, int& 
     }
 }
 
+// Non-blocking test of a phase (the thread is never suspended).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// As mbar_wait, polling with test_wait: for a thread on the critical path that must see
+// the phase complete as early as possible (a suspended try_wait wakes a few hundred
+// cycles late).  The abort flag and the limit are checked every 64 polls.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, const Watchdog& wd) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if ((++n & 63u) == 0) {
+            if (*wd.abort_flag) return false;
+            if (globaltimer_ns() - t0 > wd.limit_ns) {
+                *wd.abort_flag = 1;
+                atomicOr(wd.status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
 // Wait that ignores the abort flag (used only to drain copies this thread issued;
 // they complete on their own).  Bounded by `limit_ns`.
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
