@@ -446,8 +446,8 @@ struct Prefill2Ctrl {
     uint64_t q_full;
     uint64_t k_full[NK], v_full[NV];
     uint64_t rel[2][NR];
-    uint64_t p_full[2][2];  // p_full[w][h]: half h (keys 64h..64h+63) of P_w stored (computed tiles only)
-    uint64_t vote[2];       // vote[w]: the four softmax warps of tile w have voted on the current key tile
+    uint64_t p_full[2][2];  // p_full[w][0]: tile w voted (and stored P's first half, keys 0..63,
+                            // on a computed tile); p_full[w][1]: P's second half (computed tiles only)
     uint64_t never;
     uint32_t tmem_base;
     int keep[2];  // keep[w] = j+1 once a warp of tile w keeps key tile j (only grows)
@@ -541,7 +541,6 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < Ctrl::NR; ++i) mbar_init(&ctrl->rel[w][i], 1);
             mbar_init(&ctrl->p_full[w][0], 4);
             mbar_init(&ctrl->p_full[w][1], 4);
-            mbar_init(&ctrl->vote[w], 4);
             ctrl->keep[w] = 0;
             ctrl->dec[w] = 0;
         }
@@ -759,18 +758,23 @@ __global__ void __launch_bounds__(384, 1)
                     int vi = 0;
                     if (!(ok = spin_until_ge(&ctrl->v_issued, ij + 1, vi, wd))) break;
                 }
-                // all four warps have voted: the tile is kept iff one of them raised keep[w] to j+1
-                if (!(ok = mbar_wait_spin(&ctrl->vote[w], j & 1, wd))) break;
+                // V_j is read only by a computed tile's P.V.  Whether it has landed is tested
+                // now, without blocking, so that the path from P's first half to the P.V MMAs
+                // holds a single barrier wait when it has (an mbarrier operation costs the
+                // issuer a few hundred cycles while a softmax warp shares its scheduler).
+                const bool v_landed = mbar_test_wait(&ctrl->v_full[vs], (ij / C::NV) & 1);
+                // p_full[w][0], one phase per key tile: the four warps of tile w have voted and,
+                // on a computed tile, stored P's first half.  The tile is kept iff one of them
+                // raised keep[w] to j+1.
+                if (!(ok = mbar_wait_spin(&ctrl->p_full[w][0], j & 1, wd))) break;
                 const bool skip = reinterpret_cast<volatile int*>(ctrl->keep)[w] <= j;
                 if (p.elide_v) reinterpret_cast<volatile int*>(ctrl->dec)[w] = 2 * (j + 1) + (skip ? 0 : 1);
-                // V_j itself is read only by a computed tile's P.V.  With V elision the producer
-                // reads the decision words, which must not run past a key tile whose V phase is
-                // still open, so there every tile waits for V_j's phase.
-                if ((!skip || p.elide_v) && !(ok = mbar_wait(&ctrl->v_full[vs], (ij / C::NV) & 1, wd))) break;
-                // a computed tile's first P half (the barrier's phases count computed tiles only)
-                if (!skip && !(ok = mbar_wait_spin(&ctrl->p_full[w][0], npv & 1, wd))) break;
-                // a skipped tile's group is a lone QK: it goes into the queue without its turn
-                if (!skip && !(ok = take_turn())) break;
+                // With V elision the producer reads the decision words, which must not run
+                // past a key tile whose V phase is still open, so there every tile waits for
+                // V_j's phase.
+                if ((!skip || p.elide_v) && !v_landed && !(ok = mbar_wait(&ctrl->v_full[vs], (ij / C::NV) & 1, wd)))
+                    break;
+                if (!(ok = take_turn())) break;
                 tc_fence_after();
                 if (!skip) issue_pv_half(vs, 0, npv == 0);
                 // the tile's record, written while the tensor core works through the queued MMAs
@@ -851,12 +855,9 @@ __global__ void __launch_bounds__(384, 1)
             // vote to skip wait there for the other warps.  keep[w] only grows, and key
             // tile j+1 starts after every warp has finished tile j, so it needs no reset.
             // The MMA issuer reads the same word and writes the tile's record.
-            // Lane 0 of every warp also arrives on vote[w], which is how the MMA issuer learns
-            // the decision (a skipped tile needs no other signal from the softmax): a warp
-            // that votes to skip right away, a warp that keeps the tile just before it
-            // signals P's first half (the issuer needs no earlier word of a kept tile, and
-            // the arrive, with release order after the keep store, then stays off the path
-            // from the vote to the exponentials).
+            // The MMA issuer learns the decision from p_full[w][0]: every warp arrives on it
+            // once per key tile, after P's first half on a computed tile and right after the
+            // decision on a skipped one.
             const unsigned all = __all_sync(0xffffffffu, vote_skip);
             bool skip = false;
             if (!all) {
@@ -865,7 +866,6 @@ __global__ void __launch_bounds__(384, 1)
                 __syncwarp();
                 named_bar_arrive(1 + w, 128);
             } else {
-                mbar_arrive_if(&ctrl->vote[w], lane == 0);
                 named_bar_sync(1 + w, 128);
                 skip = reinterpret_cast<volatile int*>(ctrl->keep)[w] <= j;
             }
@@ -904,7 +904,6 @@ __global__ void __launch_bounds__(384, 1)
                         tmem_st_wait();
                         tc_fence_before();
                         __syncwarp();
-                        mbar_arrive_if(&ctrl->vote[w], lane == 0 && !all);
                         mbar_arrive_if(&ctrl->p_full[w][0], lane == 0);
                         fence_regs<64>(xr + 64);  // keep the second half's math after the signal
                     }
@@ -915,6 +914,9 @@ __global__ void __launch_bounds__(384, 1)
                 tc_fence_before();
                 __syncwarp();
                 mbar_arrive_if(&ctrl->p_full[w][1], lane == 0);
+            } else {
+                __syncwarp();
+                mbar_arrive_if(&ctrl->p_full[w][0], lane == 0);
             }
         }
 
