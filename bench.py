@@ -38,8 +38,8 @@ DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # reports the figure only while those sources are unchanged (else traffic is null:
 # the counters belong to another version of the kernel).
 KERNEL_SOURCES = {
-    "prefill": ["csrc/prefill.cu", "csrc/ptx.cuh", "csrc/kernels.cuh"],
-    "decode": ["csrc/decode.cu", "csrc/ptx.cuh", "csrc/kernels.cuh"],
+    "prefill": ["csrc/prefill.cu", "csrc/ptx.cuh", "csrc/kernels.cuh", "csrc/api.cu"],
+    "decode": ["csrc/decode.cu", "csrc/ptx.cuh", "csrc/kernels.cuh", "csrc/api.cu"],
 }
 TRAFFIC = {
     "prefill": {"bytes": None, "sources_sha256": None, "capture": None},
@@ -827,6 +827,16 @@ def run_sweep(args):
         torch.cuda.empty_cache()
     pts = calibrate.sweep(margins, cands)
     fitted = calibrate.fit(pts)
+    # Table 6 of the BLASST talk notes: one fixed threshold skips more at longer contexts.
+    # Checked on the seed-1 margins at every candidate that skips anything.
+    drift = {}
+    for lam in cands:
+        by_len = [calibrate.sparsity_at(margins[L], lam) for L in sorted(margins)]
+        if by_len[-1] > 0:
+            drift[f"{lam:.3g}"] = by_len
+    emit({"sweep": "drift-check-fixed-lambda", "seed": 1, "lengths": sorted(margins),
+          "sparsity_by_length": drift,
+          "non_decreasing_in_length": all(all(b >= a for a, b in zip(v, v[1:])) for v in drift.values())})
     emit({"sweep": "calibration", "seed": 1, "lengths": sorted(margins), "candidates": len(cands),
           "informative_points": sum(1 for _, _, S_ in pts if 0 < S_ < 1),
           "max_sparsity_at_lambda1": {L: calibrate.sparsity_at(g, 1.0) for L, g in margins.items()},
