@@ -42,10 +42,11 @@ KERNEL_SOURCES = {
     "decode": ["csrc/decode.cu", "csrc/ptx.cuh", "csrc/kernels.cuh", "csrc/api.cu"],
 }
 TRAFFIC = {
-    "prefill": {"bytes": None, "sources_sha256": None, "capture": None},
-    "decode": {"bytes": 8 * (1073936640 + 3331584), "sources_sha256": "82829ad849fca2be004c7210f220a6ae8251b9fdc7390a1fece2d6779c67aecf",
-               "capture": "decode_kernel<4, 0> at B=8 Hq=32 Hkv=8 Lkv=32768 d=128 (7 splits), one launch, "
-                          "dram__bytes_read.sum + dram__bytes_write.sum, scaled x8 by sequences to B=64"},
+    "prefill": {"bytes": 201395200 + 99382016,
+                "sources_sha256": "8b006b0ffadb142d7f4fe1a146f9e15475da2100abd805ff9204d439615f0882",
+                "capture": "prefill2_kernel<128, false> on the bench's causal L=16384 GQA prefill, one launch, "
+                           "dram__bytes_read.sum + dram__bytes_write.sum (ncu --set full)"},
+    "decode": {"bytes": None, "sources_sha256": None, "capture": None},
 }
 
 
