@@ -12,7 +12,7 @@ GPU threshold is then checked on every visited tile:
 
 Workloads: causal GQA LLM prefill at 16384 (whole), split-KV decode of 64 x 32768
 (whole), video DiT (two whole heads: every query tile of each), the long-context
-prefill at 8192 on the evaluation seed (whole).  These are slow (minutes of CPU
+prefill at 8192 on the evaluation seed (whole), planted-70 (two whole heads).  These are slow (minutes of CPU
 oracle time in total)."""
 from __future__ import annotations
 
@@ -145,3 +145,14 @@ def test_decode_whole_problem_exact_counts():
         if lam == 0.0:
             assert n == 0
     assert int(results[0.3]["skipped"].item()) > 0
+
+
+def test_planted70_two_whole_heads_exact_counts():
+    """The bench's skip point: planted-70 (the LLM prefill shapes, non-causal, the last
+    70 % of key tiles hold K = 0) at lambda = 1e-2, every query tile of two heads of one
+    K/V group, with the exact count; 70.3 % of their tiles are skipped."""
+    a = W.planted70(seed=0, L=16384, device="cuda")
+    counts = _prefill_whole(a, [0.0, 1e-2], heads=(4, 7))
+    n, band = counts[1e-2]
+    assert band == 0
+    assert n == 2 * 128 * 90  # key tiles 38..127 of every query tile of the two heads
