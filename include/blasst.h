@@ -52,7 +52,8 @@ extern "C" {
 #define BLASST_OK 0
 #define BLASST_WARN_LAMBDA_GE_1 1        /* blasst_lambda: curve gave lambda > 1 (value still returned) */
 #define BLASST_ERR_INVALID_ARG (-1)      /* null required pointer, bad size, lambda/scale out of range */
-#define BLASST_ERR_UNSUPPORTED (-2)      /* valid request the library does not support (d, G, alignment) */
+#define BLASST_ERR_UNSUPPORTED (-2)      /* valid request the library does not support (d, G, alignment,
+                                            memory that is not this GPU's on a cluster path) */
 #define BLASST_ERR_WORKSPACE_TOO_SMALL (-3)
 #define BLASST_ERR_CUDA (-4)             /* a CUDA runtime/driver call failed */
 #define BLASST_ERR_TIMEOUT (-5)          /* a device-side wait ran past its limit (see blasst_device_status) */
@@ -154,6 +155,10 @@ size_t blasst_decode_workspace_size(int B, int Hq, int Hkv, int Lkv, int d, int 
  *   skip_map     nullable device uint8 [B, Hkv, nT] (0 computed, 1 skipped).
  *   margins      nullable device fp32 [B, Hkv, nT] (as for prefill).
  */
+/*   With 128 heads per KV head (the cluster form) q, k_cache and v_cache must be device
+ *   memory of the current GPU: the two CTAs of a cluster share key loads by multicast,
+ *   which must read this GPU's own memory.  Host, managed or another GPU's memory
+ *   returns BLASST_ERR_UNSUPPORTED. */
 int blasst_decode(const void* q, const void* k_cache, const void* v_cache, void* o, float* lse, int B, int Hq,
                   int Hkv, int Lkv, int d, float scale, float lambda, int num_splits, void* workspace,
                   size_t workspace_bytes, unsigned long long* skipped_tiles_out, unsigned char* skip_map,
@@ -263,6 +268,9 @@ size_t blasst_decode_noalloc_scratch_bytes(void);
  *                visited).
  *   Out-of-range page indices and lengths are handled as for blasst_decode_paged.
  */
+/*   Above 64 heads (the cluster form) q and kv must be device memory of the current GPU
+ *   (the CTAs of a cluster share key loads by multicast): anything else returns
+ *   BLASST_ERR_UNSUPPORTED. */
 int blasst_mla_decode(const void* q, const void* kv, const int* page_table, const int* seq_lens, void* o,
                       float* lse, int B, int Hq, int max_kv_len, int dk, int dv, int num_pages, int page_size,
                       int max_pages_per_seq, float scale, float lambda, int num_splits, void* workspace,
