@@ -419,11 +419,11 @@ __global__ void __launch_bounds__(192, 1)
 //
 // The CTA owns query tiles A = 2i and B = 2i+1 of one head; each K/V tile is
 // staged once and used by both.  Warps 0-3 run the softmax of tile A, warps 4-7
-// that of tile B, warp 8 is the TMA producer, warps 9 and 10 issue the MMAs of
-// tiles A and B (one thread each, so that one issuer's barrier waits overlap the
-// other's MMAs; warp 11 only completes the third warpgroup, whose registers move to the softmax
-// warpgroups: 168 per thread at launch, 72 for warpgroup 2 and 216 for the
-// softmax warpgroups afterwards -- 2*128*216 + 128*72 = 384*168).  TMEM:
+// that of tile B, warp 8 loads Q and the K tiles, warp 11 the V tiles, warps 9 and
+// 10 issue the MMAs of tiles A and B (one thread each, so that one issuer's barrier
+// waits overlap the other's MMAs).  Registers: 168 per thread at launch, 72 for
+// warpgroup 2 and 216 for the softmax warpgroups afterwards -- 2*128*216 + 128*72 =
+// 384*168.  TMEM:
 // S_A = [0,128), S_B = [128,256), O_A = [256, 256+D), O_B = [256+D, 256+2D);
 // P_w overwrites the first 64 columns of S_w.  The tensor core runs, per key
 // tile j:  ... PV_A(j), QK_A(j+1), PV_B(j), QK_B(j+1) ...  so the softmax of one

@@ -228,3 +228,30 @@ def test_short_watchdog_reports_timeout_and_context_survives():
     torch.cuda.synchronize()
     assert K.blasst_device_status(0) == K.BLASST_OK
     parity.prefill_full_check(a, res, 0.0)
+
+
+@pytest.mark.parametrize("flags", [0, K.BLASST_PREFILL_ELIDE_V], ids=["two-qtiles", "two-qtiles-elide-V"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_long_runs_of_skipped_tiles(flags, causal):
+    """The last 90 % of the keys hold K = 0, so at lambda = 0.1 almost every key tile
+    after the first few is skipped by both query tiles of a CTA: long runs in which the
+    MMA issuers wait for no V tile and run ahead of the V producer by as much as the
+    kernel allows.  Every decision, the exact count, O and lse against the oracle."""
+    a = W.planted70(seed=5, L=4096, Hq=4, Hkv=2, device="cuda", frac=0.9)
+    a.causal = causal
+    res = K.prefill(a.q, a.k, a.v, a.causal, a.scale, 0.1, want_map=True, flags=flags)
+    torch.cuda.synchronize()
+    band, mx, mean, n = parity.prefill_full_check(a, res, 0.1)
+    visited = int((res["map"] != 2).sum().item())
+    assert n > 0.75 * visited, (n, visited)
+
+
+def test_long_skip_runs_in_a_window():
+    """The same with a causal sliding window of 1000 keys (windowed CTAs start their key
+    walk past tile 0)."""
+    a = W.planted70(seed=6, L=4096, Hq=4, Hkv=2, device="cuda", frac=0.9)
+    a.causal = True
+    for flags in (0, K.BLASST_PREFILL_ELIDE_V):
+        res = K.prefill(a.q, a.k, a.v, True, a.scale, 0.1, want_map=True, flags=flags, window=1000)
+        torch.cuda.synchronize()
+        parity.prefill_full_check(a, res, 0.1, window=1000)
