@@ -29,7 +29,8 @@
 // before the next P.V.  The per-head maxima, the same in every thread, live in
 // shared memory; each thread keeps its partial row sums.
 //
-// Warp roles (256 threads): warps 0-3 softmax, warp 4 key loader, warp 5 issuer of
+// Warp roles (256 threads; 384 at 64 heads per CTA, whose softmax also runs on warps
+// 8-11, see MlaCfg): warps 0-3 softmax, warp 4 key loader, warp 5 issuer of
 // the S MMAs and TMEM owner, warp 6 value loader, warp 7 issuer of the P.V MMAs.
 // The two MMA streams have their own issuing threads, so a P.V pass waiting for a
 // decision or a value pair never holds up the S MMAs that drain the key ring.
@@ -114,6 +115,14 @@ struct MlaCfg {
     // each thread stores its key's row in 16-byte pieces; fewer: K-major, [key half][NPAD
     // heads][64 keys].
     static constexpr bool MNP = NPAD == 64;
+    // Softmax warpgroups.  64 heads per CTA split their heads over two warpgroups, warps
+    // 0-3 (heads 0-31) and 8-11 (heads 32-63), which read the same TMEM lanes: each
+    // thread's share of a tile's softmax (per-head maxima, exponentials, P stores, O
+    // rescale) halves.  Fewer heads: one warpgroup (warps 0-3).
+    static constexpr int NGRP = NPAD == 64 ? 2 : 1;
+    static constexpr int HPG = NPAD / NGRP;          // heads per softmax warpgroup
+    static constexpr int THREADS = NGRP == 2 ? 384 : 256;
+    static constexpr int NSW = 4 * NGRP;             // softmax warps
     static constexpr int P_BYTES = 2 * NPAD * 128;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + NKB * BOX_BYTES;
@@ -154,7 +163,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 template <class SH, int G, bool PAGED, int CG>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(MlaCfg<SH, mla_heads_per_cta(G), CG>::THREADS, 1)
     mla_decode_kernel(const __grid_constant__ CUtensorMap tkv, const __grid_constant__ CUtensorMap tv,
                       const __grid_constant__ CUtensorMap tq, const DecodeParams p) {
     using C = MlaCfg<SH, mla_heads_per_cta(G), CG>;
@@ -196,12 +205,12 @@ __global__ void __launch_bounds__(256, 1)
         for (int i = 0; i < ND; ++i) mbar_init(&ctrl->vote_full[i], 1);  // own arrival + CG votes' bytes
         // the first NKB key entries are armed before any CTA of the cluster can copy
         for (int i = 0; i < min(NKB, n * KBOX); ++i) mbar_arrive_expect_tx(&ctrl->k_full[i], BOX_BYTES);
-        for (int i = 0; i < NS; ++i) { mbar_init(&ctrl->s_full[i], 1); mbar_init(&ctrl->s_free[i], 4); }
+        for (int i = 0; i < NS; ++i) { mbar_init(&ctrl->s_full[i], 1); mbar_init(&ctrl->s_free[i], C::NSW); }
         for (int i = 0; i < ND; ++i) {
             mbar_init(&ctrl->dec_full[i], 1);
             mbar_init(&ctrl->dec_free[i], 2);  // released by the P.V issuer and the value loader
         }
-        for (int i = 0; i < NP; ++i) { mbar_init(&ctrl->p_full[i], 4); mbar_init(&ctrl->p_free[i], 1); }
+        for (int i = 0; i < NP; ++i) { mbar_init(&ctrl->p_full[i], C::NSW); mbar_init(&ctrl->p_free[i], 1); }
         for (int i = 0; i < 8; ++i) mbar_init(&ctrl->o_done[i], 1);
         for (int g = 0; g < NPAD; ++g)
             for (int q = 0; q < 2; ++q) ctrl->mex[q][g] = ctrl->mrf[q][g] = -CUDART_INF_F;
@@ -482,13 +491,21 @@ __global__ void __launch_bounds__(256, 1)
             mbar_wait_drain(&ctrl->drain[1], 0, kDrainNs);
         }
     } else {
-        // ------------------------------------------------------------ softmax (warps 0-3)
-        const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+        // ------------------------------------------------------------ softmax (warps 0-3, and 8-11 at 64 heads)
+        constexpr int NGRP = C::NGRP, NST = 128 * NGRP;  // warpgroups, threads
+        // this thread's key lane (= TMEM lane) and its warpgroup's heads [hb, hb + GH)
+        const int kl = tid & 127, grp = warp >> 3;
+        constexpr int GH = NGRP == 2 ? C::HPG : G;
+        const int hb = grp * C::HPG;
+        // in each warpgroup the thread of key lane g judges and finishes head hb + g
+        const bool judge = kl < GH;
+        const int hj = hb + kl;
+        const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16);
         // Clear the P buffers' padding rows (heads past G); the fence before each P
         // arrival makes the zeros visible to the MMAs.
         if constexpr (!C::MNP) {
             uint4* sp = reinterpret_cast<uint4*>(smem + OFF_P);
-            for (int c = tid; c < NP * P_BYTES / 16; c += 128) sp[c] = make_uint4(0, 0, 0, 0);
+            for (int c = kl; c < NP * P_BYTES / 16; c += 128) sp[c] = make_uint4(0, 0, 0, 0);
         }
         const long long mapbase = (long long)zkv * p.nK;
         const float cl = p.c_log2;
@@ -497,8 +514,10 @@ __global__ void __launch_bounds__(256, 1)
         // written by thread g for head g and read by everyone from tile j+1 on (after
         // that tile's first barrier).  Per thread: the scores of its key, its partial
         // row sums and its four value columns of every head.
-        // O is read and written in chunks of OCH columns (heads)
+        // O is read and written in chunks of OCH columns (heads); a warpgroup touches OH of
+        // them, from its first head on
         constexpr int OCH = NPAD < 32 ? NPAD : 32;
+        constexpr int OH = NGRP == 2 ? C::HPG : NPAD;
         auto o_ld = [&](uint32_t ta, uint32_t* r) {
             if constexpr (OCH == 16)
                 tmem_ld16(ta, r);
@@ -513,9 +532,9 @@ __global__ void __launch_bounds__(256, 1)
             else
                 tmem_st32(ta, r);
         };
-        float lpart[G];
+        float lpart[GH];  // partial row sums of this warpgroup's heads
 #pragma unroll
-        for (int g = 0; g < G; ++g) lpart[g] = 0.f;
+        for (int g = 0; g < GH; ++g) lpart[g] = 0.f;
         int comp = 0, cur = 1;  // mrf[cur]: the reference max as of the last tile
         unsigned long long nskip = 0;
 
@@ -523,19 +542,20 @@ __global__ void __launch_bounds__(256, 1)
             const int ss = j % NS, q = j & 1, qp = q ^ 1;
             mbar_wait(&ctrl->s_full[ss], (j / NS) & 1, wd);
             tc_fence_after();
-            const int key = (t0 + j) * kTile + tid;
+            const int key = (t0 + j) * kTile + kl;
             const bool key_ok = key < Lb;
-            // the scores of this thread's key, one per head; read again for P, so the
-            // slot is released after P (nothing stays live across the decision)
+            // the scores of this thread's key, one per head of its warpgroup; read again for
+            // P, so the slot is released after P (nothing stays live across the decision)
+            constexpr int NLD = NGRP == 2 ? C::HPG : NPAD;
             auto load_scores = [&](uint32_t* xr) {
-                if constexpr (NPAD == 16)
-                    tmem_ld16(tl + ss * NPAD, xr);
-                else if constexpr (NPAD == 32)
-                    tmem_ld32(tl + ss * NPAD, xr);
+                if constexpr (NLD == 16)
+                    tmem_ld16(tl + ss * NPAD + hb, xr);
+                else if constexpr (NLD == 32)
+                    tmem_ld32(tl + ss * NPAD + hb, xr);
                 else
-                    tmem_ld64(tl + ss * NPAD, xr);
+                    tmem_ld64(tl + ss * NPAD + hb, xr);
                 tmem_ld_wait();
-                fence_regs<NPAD>(xr);
+                fence_regs<NLD>(xr);
             };
             {
                 // Per-head max over the warp's 32 keys.  From 32 heads: one warp-wide
@@ -544,18 +564,18 @@ __global__ void __launch_bounds__(256, 1)
                 // each step hands half of the remaining heads to the partner lane, so lane L
                 // ends with the max of head L >> (5 - log2 G) after G - 1 + (5 - log2 G)
                 // shuffles instead of 5 G.
-                uint32_t xr[NPAD];
+                uint32_t xr[NLD];
                 load_scores(xr);
-                float v[G];
+                float v[GH];
 #pragma unroll
-                for (int g = 0; g < G; ++g) v[g] = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
-                if constexpr (G >= 32) {
+                for (int g = 0; g < GH; ++g) v[g] = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
+                if constexpr (GH >= 32) {
 #pragma unroll
-                    for (int g = 0; g < G; ++g) v[g] = warp_max_f32(v[g]);
+                    for (int g = 0; g < GH; ++g) v[g] = warp_max_f32(v[g]);
                     if (lane == 0) {
 #pragma unroll
-                        for (int g = 0; g < G; g += 4)
-                            *reinterpret_cast<float4*>(&ctrl->red[q][warp][g]) =
+                        for (int g = 0; g < GH; g += 4)
+                            *reinterpret_cast<float4*>(&ctrl->red[q][warp & 3][hb + g]) =
                                 make_float4(v[g], v[g + 1], v[g + 2], v[g + 3]);
                     }
                 } else {
@@ -585,20 +605,21 @@ __global__ void __launch_bounds__(256, 1)
                 }
                 }
             }
-            named_bar_sync(1, 128);
-            // the decision: thread g judges head g, the barrier takes the AND
+            named_bar_sync(1, NST);
+            // the decision: in each warpgroup the thread of key lane g judges head hb + g,
+            // the barrier takes the AND
             float mn_own = -CUDART_INF_F;
             bool vote = true;
-            if (tid < G) {
-                const volatile float* rd = &ctrl->red[q][0][tid];
+            if (judge) {
+                const volatile float* rd = &ctrl->red[q][0][hj];
                 const float mt = fmaxf(fmaxf(rd[0], rd[NPAD]), fmaxf(rd[2 * NPAD], rd[3 * NPAD]));
-                mn_own = fmaxf(reinterpret_cast<volatile float*>(ctrl->mex[qp])[tid], mt);
+                mn_own = fmaxf(reinterpret_cast<volatile float*>(ctrl->mex[qp])[hj], mt);
                 const float diff = mt - mn_own;
                 vote = diff < p.thr_raw;
-                ctrl->gmar[tid] = (mt == -CUDART_INF_F && mn_own == -CUDART_INF_F) ? CUDART_INF_F : diff;
-                ctrl->mex[q][tid] = mn_own;
+                ctrl->gmar[hj] = (mt == -CUDART_INF_F && mn_own == -CUDART_INF_F) ? CUDART_INF_F : diff;
+                ctrl->mex[q][hj] = mn_own;
             }
-            bool skip = bar_red_and(1, 128, vote);
+            bool skip = bar_red_and(1, NST, vote);
             float margin = -CUDART_INF_F;
             if (tid == 0 && p.margins)
                 for (int g = 0; g < G; ++g) margin = fmaxf(margin, reinterpret_cast<volatile float*>(ctrl->gmar)[g]);
@@ -627,7 +648,7 @@ __global__ void __launch_bounds__(256, 1)
                     margin = mg;
                     reinterpret_cast<volatile int*>(&ctrl->cl_skip)[0] = all ? 1 : 0;
                 }
-                named_bar_sync(1, 128);
+                named_bar_sync(1, NST);
                 skip = reinterpret_cast<volatile int*>(&ctrl->cl_skip)[0] != 0;
             }
             if (tid == 0) {
@@ -641,19 +662,19 @@ __global__ void __launch_bounds__(256, 1)
                     nskip += skip ? 1 : 0;
                 }
             }
-            // thread g moves head g's reference max (computed tiles only) and carries it
-            // into this tile's buffer; the factor for O and l goes to alpha[g]
-            if (tid < G) {
-                const float mro = reinterpret_cast<volatile float*>(ctrl->mrf[qp])[tid];
+            // the judge of head g moves its reference max (computed tiles only) and carries
+            // it into this tile's buffer; the factor for O and l goes to alpha[g]
+            if (judge) {
+                const float mro = reinterpret_cast<volatile float*>(ctrl->mrf[qp])[hj];
                 float mr = mro, a = 1.f;
                 if (!skip && mn_own != -CUDART_INF_F && (mro == -CUDART_INF_F || mn_own > mro + p.lazy_raw)) {
                     a = mro == -CUDART_INF_F ? 0.f : ex2((mro - mn_own) * cl);
                     mr = mn_own;
                 }
-                ctrl->mrf[q][tid] = mr;
+                ctrl->mrf[q][hj] = mr;
                 if (!skip) {
-                    ctrl->alpha[tid] = a;
-                    ctrl->nmc[tid] = -((mr == -CUDART_INF_F ? 0.f : mr) * cl);
+                    ctrl->alpha[hj] = a;
+                    ctrl->nmc[hj] = -((mr == -CUDART_INF_F ? 0.f : mr) * cl);
                 }
             }
             if (!skip) {
@@ -663,11 +684,11 @@ __global__ void __launch_bounds__(256, 1)
                     // the barrier that publishes alpha, mrf[q] also tells whether any head moved;
                     // then O (the P.V of the computed tiles so far) is rescaled in TMEM once
                     // the newest P.V is done
-                    const bool moved = tid < G && reinterpret_cast<volatile float*>(ctrl->alpha)[tid] != 1.f;
-                    if (bar_red_or(1, 128, moved)) {
+                    const bool moved = judge && reinterpret_cast<volatile float*>(ctrl->alpha)[hj] != 1.f;
+                    if (bar_red_or(1, NST, moved)) {
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float a = al[g];
+                        for (int g = 0; g < GH; ++g) {
+                            const float a = al[hb + g];
                             if (a != 1.f) lpart[g] *= a;
                         }
                         if (comp > 0) {
@@ -676,13 +697,13 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll 1
                             for (int i = 0; i < VBLK; ++i) {
 #pragma unroll
-                                for (int h = 0; h < NPAD / OCH; ++h) {
+                                for (int h = 0; h < OH / OCH; ++h) {
                                     uint32_t tt[OCH];
-                                    const uint32_t ta = tl + O_COL + i * NPAD + h * OCH;
+                                    const uint32_t ta = tl + O_COL + i * NPAD + hb + h * OCH;
                                     o_ld(ta, tt);
 #pragma unroll
                                     for (int c2 = 0; c2 < OCH; ++c2)
-                                        tt[c2] = __float_as_uint(__uint_as_float(tt[c2]) * al[h * OCH + c2]);
+                                        tt[c2] = __float_as_uint(__uint_as_float(tt[c2]) * al[hb + h * OCH + c2]);
                                     o_st(ta, tt);
                                 }
                             }
@@ -690,14 +711,14 @@ __global__ void __launch_bounds__(256, 1)
                         }
                     }
                 }
-                uint32_t xr[NPAD];
+                uint32_t xr[NLD];
                 load_scores(xr);
                 // p = 2^(s*c - m_ref*c) for every head, in place, before any store, so that
                 // the loads of the per-head constants are free to run ahead
-                const float* nm = ctrl->nmc;  // published by the barrier above
-                if constexpr (G >= 4) {
+                const float* nm = ctrl->nmc + hb;  // published by the barrier above
+                if constexpr (GH >= 4) {
 #pragma unroll
-                    for (int g = 0; g < G; g += 4) {
+                    for (int g = 0; g < GH; g += 4) {
                         const float4 n4 = *reinterpret_cast<const float4*>(nm + g);
                         float x[4], a[4];
 #pragma unroll
@@ -713,7 +734,7 @@ __global__ void __launch_bounds__(256, 1)
                     }
                 } else {
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
+                    for (int g = 0; g < GH; ++g) {
                         const float xg = key_ok ? __uint_as_float(xr[g]) : -CUDART_INF_F;
                         const float pv = ex2(fmaf(xg, cl, nm[g]));
                         lpart[g] += pv;
@@ -723,23 +744,25 @@ __global__ void __launch_bounds__(256, 1)
                 const int pb = comp % NP;
                 if (comp >= NP) mbar_wait(&ctrl->p_free[pb], ((comp / NP) - 1) & 1, wd);
                 if constexpr (C::MNP) {
-                    // this key's row of 64 heads, eight 16-byte pieces, 128-byte swizzle
-                    uint8_t* prow = smem + OFF_P + pb * P_BYTES + tid * 128;
+                    // this key's row of 64 heads, eight 16-byte pieces, 128-byte swizzle; each
+                    // warpgroup writes the pieces of its heads
+                    uint8_t* prow = smem + OFF_P + pb * P_BYTES + kl * 128;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
+                    for (int c = 0; c < GH / 8; ++c) {
                         uint4 w;
                         w.x = pack_bf16x2(__uint_as_float(xr[8 * c + 0]), __uint_as_float(xr[8 * c + 1]));
                         w.y = pack_bf16x2(__uint_as_float(xr[8 * c + 2]), __uint_as_float(xr[8 * c + 3]));
                         w.z = pack_bf16x2(__uint_as_float(xr[8 * c + 4]), __uint_as_float(xr[8 * c + 5]));
                         w.w = pack_bf16x2(__uint_as_float(xr[8 * c + 6]), __uint_as_float(xr[8 * c + 7]));
-                        *reinterpret_cast<uint4*>(prow + ((c ^ (tid & 7)) << 4)) = w;
+                        const int piece = hb / 8 + c;
+                        *reinterpret_cast<uint4*>(prow + ((piece ^ (kl & 7)) << 4)) = w;
                     }
                 } else {
-                    uint8_t* pbuf = smem + OFF_P + pb * P_BYTES + (tid >> 6) * (NPAD * 128);
-                    const int cw = (tid & 63) >> 3;
+                    uint8_t* pbuf = smem + OFF_P + pb * P_BYTES + (kl >> 6) * (NPAD * 128);
+                    const int cw = (kl & 63) >> 3;
 #pragma unroll
                     for (int g = 0; g < G; ++g)
-                        *reinterpret_cast<unsigned short*>(pbuf + g * 128 + ((cw ^ (g & 7)) << 4) + (tid & 7) * 2) =
+                        *reinterpret_cast<unsigned short*>(pbuf + g * 128 + ((cw ^ (g & 7)) << 4) + (kl & 7) * 2) =
                             (unsigned short)(pack_bf16x2(__uint_as_float(xr[g]), 0.f) & 0xffffu);
                 }
                 fence_proxy_async_smem();
@@ -752,35 +775,35 @@ __global__ void __launch_bounds__(256, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&ctrl->s_free[ss]);
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, NST);
         cur = (n - 1) & 1;  // the last tile's buffer holds every head's final reference max
 
         // l = sum over the 128 key lanes; O = (TMEM accumulator) / l
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < GH; ++g) {
             float v = lpart[g];
 #pragma unroll
             for (int sh = 16; sh > 0; sh >>= 1) v += __shfl_xor_sync(0xffffffffu, v, sh);
-            if (lane == 0) ctrl->lred[warp][g] = v;
+            if (lane == 0) ctrl->lred[warp & 3][hb + g] = v;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, NST);
         {
-            // thread g finishes head g (l, lse); then every thread writes its value
-            // columns of every head from the TMEM accumulator
-            if (tid < G) {
-                const volatile float* lr = &ctrl->lred[0][tid];
+            // the judge of head g finishes it (l, lse); then every thread writes its value
+            // columns of its warpgroup's heads from the TMEM accumulator
+            if (judge) {
+                const volatile float* lr = &ctrl->lred[0][hj];
                 const float l = lr[0] + lr[NPAD] + lr[2 * NPAD] + lr[3 * NPAD];
-                const float mrg = reinterpret_cast<volatile float*>(ctrl->mrf[cur])[tid];
+                const float mrg = reinterpret_cast<volatile float*>(ctrl->mrf[cur])[hj];
                 const float lse = l > 0.f ? mrg * p.scale + __logf(l) : -CUDART_INF_F;
-                ctrl->inv_l[tid] = l > 0.f ? 1.f / l : 0.f;
-                const long long hq = (long long)b * p.Hq + qh0 + tid;
+                ctrl->inv_l[hj] = l > 0.f ? 1.f / l : 0.f;
+                const long long hq = (long long)b * p.Hq + qh0 + hj;
                 if (p.S == 1) {
                     if (p.lse) p.lse[hq] = lse;
                 } else {
                     p.lse_part[(long long)s * p.B * p.Hq + hq] = lse;
                 }
             }
-            named_bar_sync(1, 128);
+            named_bar_sync(1, NST);
             if (comp > 0) {
                 mbar_wait(&ctrl->o_done[(comp - 1) % 8], ((comp - 1) / 8) & 1, wd);
                 tc_fence_after();
@@ -789,21 +812,21 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll 1
             for (int i = 0; i < VBLK; ++i) {
 #pragma unroll
-                for (int h = 0; h < NPAD / OCH; ++h) {
+                for (int h = 0; h < OH / OCH; ++h) {
                     uint32_t tt[OCH];
                     if (comp > 0) {
-                        o_ld(tl + O_COL + i * NPAD + h * OCH, tt);
+                        o_ld(tl + O_COL + i * NPAD + hb + h * OCH, tt);
                     } else {
 #pragma unroll
                         for (int c2 = 0; c2 < OCH; ++c2) tt[c2] = 0u;
                     }
 #pragma unroll
                     for (int c2 = 0; c2 < OCH; ++c2) {
-                        const int g = h * OCH + c2;
+                        const int g = hb + h * OCH + c2;
                         if (g >= G) continue;
                         const float v = __uint_as_float(tt[c2]) * il[g];
                         const long long hq = (long long)b * p.Hq + qh0 + g;
-                        const int col = i * 128 + tid;
+                        const int col = i * 128 + kl;
                         if (col >= dout) continue;
                         if (p.S == 1)
                             reinterpret_cast<unsigned short*>(p.o)[hq * dout + col] =
@@ -836,7 +859,7 @@ cudaError_t launch_gp(const CUtensorMap& tkv, const CUtensorMap& tv, const CUten
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.S * CG), (unsigned)p.Hkv, (unsigned)p.B);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(MlaCfg<SH, mla_heads_per_cta(G), CG>::THREADS, 1, 1);
     cfg.dynamicSmemBytes = SMEM;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
