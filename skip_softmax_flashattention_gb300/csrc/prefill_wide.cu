@@ -251,17 +251,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 volatile int* turn = &ctrl->turn;
                 volatile int* active = ctrl->active;
                 // Groups (PV_w(j) + QK_w(j+1)) of the two issuers alternate in the tensor
-                // queue, which keeps the two tiles' softmaxes half a period apart.
+                // queue, which keeps the two tiles' softmaxes half a period apart.  The turn
+                // word is polled tightly (the limit is checked every 256 polls) and handed
+                // over before the commit, as in the default kernel.
                 auto take_turn = [&]() -> bool {
                     if (*turn == w || !active[1 - w]) return true;
                     const uint64_t t0 = globaltimer_ns();
+                    uint32_t it = 0;
                     while (*turn != w && active[1 - w]) {
-                        __nanosleep(32);
-                        if (*wd.abort_flag) return false;
-                        if (globaltimer_ns() - t0 > wd.limit_ns) {
-                            *wd.abort_flag = 1;
-                            atomicOr(wd.status, kStatusTimeout);
-                            return false;
+                        if ((++it & 255u) == 0) {
+                            if (*wd.abort_flag) return false;
+                            if (globaltimer_ns() - t0 > wd.limit_ns) {
+                                *wd.abort_flag = 1;
+                                atomicOr(wd.status, kStatusTimeout);
+                                return false;
+                            }
                         }
                     }
                     return true;
@@ -277,25 +281,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int npv = 0;
                 for (int j = 0; j < n && ok; ++j) {
                     const int vs = j % C::NV;
-                    if (!(ok = mbar_wait(&ctrl->p_full[w][0], j & 1, wd))) break;
-                    const bool skip = reinterpret_cast<volatile int*>(ctrl->dec)[w] != 0;
-                    // V_j must have landed before its slot is released, also when the tile is skipped
-                    if (!(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
                     if (j + 1 < n &&
                         !(ok = mbar_wait(&ctrl->k_full[(j + 1) % C::NK], ((j + 1) / C::NK) & 1, wd)))
                         break;
+                    const bool v_landed = mbar_test_wait(&ctrl->v_full[vs], (j / C::NV) & 1);
+                    if (!(ok = mbar_wait_spin(&ctrl->p_full[w][0], j & 1, wd))) break;
+                    const bool skip = reinterpret_cast<volatile int*>(ctrl->dec)[w] != 0;
+                    // V_j must have landed before its slot is released, also when the tile is skipped
+                    if (!v_landed && !(ok = mbar_wait(&ctrl->v_full[vs], (j / C::NV) & 1, wd))) break;
                     if (!(ok = take_turn())) break;
                     tc_fence_after();
                     if (!skip) issue_pv_half(vs, 0, npv == 0);
-                    if (!(ok = mbar_wait(&ctrl->p_full[w][1], j & 1, wd))) break;
+                    if (!(ok = mbar_wait_spin(&ctrl->p_full[w][1], j & 1, wd))) break;
                     tc_fence_after();
                     if (!skip) {
                         issue_pv_half(vs, 1, npv == 0);
                         ++npv;
                     }
                     if (j + 1 < n) issue_qk(j + 1);
-                    commit();  // commit j+1: PV_w(j) and QK_w(j+1)
                     *turn = 1 - w;
+                    commit();  // commit j+1: PV_w(j) and QK_w(j+1)
                 }
                 active[w] = 0;
                 *turn = 1 - w;
