@@ -256,22 +256,44 @@ def run_reference(args):
     nQ = L // 128
     rng = np.random.default_rng(1234)
     per_step_units = max(1, args.ref_units)
+    # the decode half of the step: two sequences of the bench's decode shape and
+    # distribution (all 8 KV heads, 32768 keys each, the same split plan)
+    Dd = DECODE
+    dq = W.decode(seed=0, B=2, Hq=Dd["Hq"], Hkv=Dd["Hkv"], Lkv=Dd["Lkv"], d=Dd["d"], device="cpu")
+    dq_q, dq_k, dq_v = dq.q.float(), dq.k.float(), dq.v.float()
+    lam_d = args.lam_a / Dd["Lkv"]
+    S_d = 2  # the library's plan for B=64 on 148 SMs (fewest splits filling the last wave to 90 %)
+
+    def decode_sample():
+        t0 = time.perf_counter()
+        orc.decode_tiled(dq_q, dq_k, dq_v, dq.scale, lam_d, num_splits=S_d, precision="f32")
+        return time.perf_counter() - t0
+
     for _ in range(args.warmup):
         oracle_sample(a, random_units(rng, a.Hq, nQ, 1), lam)
-    flops, secs = 0, 0.0
+    decode_sample()
+    flops, secs, dsecs = 0, 0.0, 0.0
     for _ in range(args.steps):
-        f, s = oracle_sample(a, random_units(rng, a.Hq, nQ, per_step_units), lam)
+        f, s_ = oracle_sample(a, random_units(rng, a.Hq, nQ, per_step_units), lam)
         flops += f
-        secs += s
+        secs += s_
+        dsecs += decode_sample()
     value = flops / secs / 1e12
+    dec_bytes = 2 * Dd["Hkv"] * Dd["Lkv"] * Dd["d"] * 2 * 2  # K and V of the two sequences (bf16)
     cores = orc.num_threads()
-    sample = (f"{args.steps} steps x {per_step_units} random (head, 128-row query tile) units of the causal "
-              f"L=16384 GQA prefill, full key rows, lambda={lam:.3g}")
+    sample = (f"{args.steps} steps x ({per_step_units} random (head, 128-row query tile) units of the causal "
+              f"L=16384 GQA prefill, full key rows, lambda={lam:.3g}; and 2 whole sequences of the B=64 "
+              f"split-KV decode, lambda={lam_d:.3g}, {S_d} splits)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": (secs + dsecs) / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "llm-prefill-causal-gqa B=1 Hq=32 Hkv=8 L=16384 d=128", "lambda": lam,
-                       "l2": "not applicable (CPU)"},
+            "config": {"workload": "llm-prefill-causal-gqa B=1 Hq=32 Hkv=8 L=16384 d=128 + "
+                                   "split-kv-decode B=64 Hq=32 Hkv=8 Lkv=32768 d=128",
+                       "lambda": {"prefill": lam, "decode": lam_d,
+                                  "rule": (f"threshold {args.threshold}" if args.threshold is not None
+                                           else f"a/Lkv, a={args.lam_a}")},
+                       "l2": "not applicable (CPU)", "decode_splits": S_d},
+            "decode": {"kv_gbs": dec_bytes * args.steps / dsecs / 1e9, "ms_per_sequence": dsecs / args.steps / 2 * 1e3},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
