@@ -255,24 +255,25 @@ __global__ void __launch_bounds__(192, 1)
             mbar_wait(&ctrl->s_full[j & 1], (j >> 1) & 1, wd);
             tc_fence_after();
             uint32_t xr[128];
+            float lm[4];  // maximum of each 32-column quarter (load and reduce)
             const uint32_t sc = tl + (uint32_t)(j & 1) * 128u;
-            tmem_ld32(sc + 0, xr);
-            tmem_ld32(sc + 32, xr + 32);
-            tmem_ld32(sc + 64, xr + 64);
-            tmem_ld32(sc + 96, xr + 96);
+            tmem_ld32_max(sc + 0, xr, lm[0]);
+            tmem_ld32_max(sc + 32, xr + 32, lm[1]);
+            tmem_ld32_max(sc + 64, xr + 64, lm[2]);
+            tmem_ld32_max(sc + 96, xr + 96, lm[3]);
             tmem_ld_wait();
             fence_regs<128>(xr);
+            asm volatile("" : "+f"(lm[0]), "+f"(lm[1]), "+f"(lm[2]), "+f"(lm[3]));  // used after the wait
 
             // mask keys beyond Lkv and (causal) beyond the row's diagonal
             const int lim = min(p.Lkv - 1, lim_row) - j * kTile;
+            float mt = fmaxf(fmaxf(lm[0], lm[1]), fmaxf(lm[2], lm[3]));
             if (lim < kTile - 1) {
 #pragma unroll
                 for (int c = 0; c < kTile; ++c)
                     if (c > lim) xr[c] = __float_as_uint(-CUDART_INF_F);
+                mt = row_max128(xr);
             }
-            float mt = -CUDART_INF_F;
-#pragma unroll
-            for (int c = 0; c < kTile; ++c) mt = fmaxf(mt, __uint_as_float(xr[c]));
             const float mnew = fmaxf(m_exact, mt);
             const float diff = mt - mnew;  // NaN when both are -inf: votes "compute"
             const bool vote = !valid || (diff < p.thr_raw);
@@ -823,23 +824,31 @@ __global__ void __launch_bounds__(384, 1)
             // commit j: S_j is in TMEM and O holds PV_w(j-1)
             mbar_wait(&ctrl->rel[w][(unsigned)j % Ctrl::NR], ((unsigned)j / Ctrl::NR) & 1u, wd);
             tc_fence_after();
+            // S_j with the maximum of each 32-column quarter of the row (load and reduce)
             uint32_t xr[128];
-            tmem_ld32(tl + s_col + 0, xr);
-            tmem_ld32(tl + s_col + 32, xr + 32);
-            tmem_ld32(tl + s_col + 64, xr + 64);
-            tmem_ld32(tl + s_col + 96, xr + 96);
+            float lm[4];
+            tmem_ld32_max(tl + s_col + 0, xr, lm[0]);
+            tmem_ld32_max(tl + s_col + 32, xr + 32, lm[1]);
+            tmem_ld32_max(tl + s_col + 64, xr + 64, lm[2]);
+            tmem_ld32_max(tl + s_col + 96, xr + 96, lm[3]);
             tmem_ld_wait();
             fence_regs<128>(xr);
+            asm volatile("" : "+f"(lm[0]), "+f"(lm[1]), "+f"(lm[2]), "+f"(lm[3]));  // used after the wait
             const int kt = (lo_w + j) * kTile;  // first key of this key tile
             const int lim = min(p.Lkv - 1, lim_row) - kt;
             // sliding window: keys before r' - W + 1 are outside it
             const int lim_lo = WIN ? rabs + off - p.window + 1 - kt : 0;
+            // the row's tile max: from the loads, unless a mask cuts the tile (diagonal,
+            // ragged or window tiles), whose visible scores need their own maximum
+            float mt;
             if (lim < kTile - 1 || lim_lo > 0) {
 #pragma unroll
                 for (int c = 0; c < kTile; ++c)
                     if (c > lim || c < lim_lo) xr[c] = __float_as_uint(-CUDART_INF_F);
+                mt = row_max128(xr);
+            } else {
+                mt = fmaxf(fmaxf(lm[0], lm[1]), fmaxf(lm[2], lm[3]));
             }
-            const float mt = row_max128(xr);
             const float mnew = fmaxf(m_exact, mt);
             const float diff = mt - mnew;
             const bool vote_skip = !valid || (diff < p.thr_raw);

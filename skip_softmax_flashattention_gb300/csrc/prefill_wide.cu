@@ -335,18 +335,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // commit j: S_j is in TMEM and O holds PV_w(j-1)
             mbar_wait(&ctrl->rel[w][(unsigned)j % Ctrl::NR], ((unsigned)j / Ctrl::NR) & 1u, wd);
             tc_fence_after();
+            // this thread's 64 scores with the maximum of each 32-column half (load and reduce)
             uint32_t xr[64];
-            tmem_ld32(tl + s_col, xr);
-            tmem_ld32(tl + s_col + 32, xr + 32);
+            float lm[2];
+            tmem_ld32_max(tl + s_col, xr, lm[0]);
+            tmem_ld32_max(tl + s_col + 32, xr + 32, lm[1]);
             tmem_ld_wait();
             fence_regs<64>(xr);
+            asm volatile("" : "+f"(lm[0]), "+f"(lm[1]));  // used after the wait
             const int lim = min(p.Lkv - 1, lim_row) - j * kTile - half * 64;
-            if (lim < 63) {
+            float mth;
+            if (lim < 63) {  // a mask cuts the tile: the visible scores need their own maximum
 #pragma unroll
                 for (int c = 0; c < 64; ++c)
                     if (c > lim) xr[c] = __float_as_uint(-CUDART_INF_F);
+                mth = row_max64(xr);
+            } else {
+                mth = fmaxf(lm[0], lm[1]);
             }
-            const float mth = row_max64(xr);
             ctrl->mx[w][half][r] = mth;
             // this half's vote; the row votes "skip" iff both halves do (see the header)
             const bool vote_skip = !valid || (mth < m_exact + p.thr_raw);
