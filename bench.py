@@ -46,8 +46,8 @@ TRAFFIC = {
                 "sources_sha256": "458997ec262f293d3c485419454ccdcea91b7aa4a7ef62f1de8f53d5c2981e1f",
                 "capture": "prefill2_kernel<128, false> on the bench's causal L=16384 GQA prefill, one launch, "
                            "dram__bytes_read.sum + dram__bytes_write.sum (ncu --set full)"},
-    "decode": {"bytes": 8 * (1073876992 + 4134144),
-               "sources_sha256": "0f56ef8b5abebf5205625fc827541e7541cffac30fe9b0afdc3a384e473b6744",
+    "decode": {"bytes": 8 * (1073871872 + 3653120),
+               "sources_sha256": "bab7aa3259ac3223d3bd554609342a713ec414216cff1eb18533fadfc7763773",
                "capture": "decode_kernel<4, 0> at B=8 Hq=32 Hkv=8 Lkv=32768 d=128 (7 splits), one launch, "
                           "dram__bytes_read.sum + dram__bytes_write.sum, scaled x8 by sequences to B=64"},
 }
