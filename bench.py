@@ -42,8 +42,8 @@ KERNEL_SOURCES = {
     "decode": ["csrc/decode.cu", "csrc/ptx.cuh", "csrc/kernels.cuh", "csrc/api.cu"],
 }
 TRAFFIC = {
-    "prefill": {"bytes": 201397760 + 99049984,
-                "sources_sha256": "458997ec262f293d3c485419454ccdcea91b7aa4a7ef62f1de8f53d5c2981e1f",
+    "prefill": {"bytes": 201398528 + 99127808,
+                "sources_sha256": "4de5b31a2d0e830ff11f66790b2f0a5f62ceb50591027167765fa2b16147680d",
                 "capture": "prefill2_kernel<128, false> on the bench's causal L=16384 GQA prefill, one launch, "
                            "dram__bytes_read.sum + dram__bytes_write.sum (ncu --set full)"},
     "decode": {"bytes": 8 * (1073871872 + 3653120),
@@ -655,6 +655,11 @@ def run_only(args):
         lam = args.lam_a / a.Lkv
         for _ in range(args.warmup + args.steps):
             K.prefill(a.q, a.k, a.v, True, a.scale, lam)
+    elif args.only == "planted70":
+        a = W.planted70(seed=0, L=args.prefill_len, device=dev)
+        lam = args.threshold if args.threshold is not None else 1e-2
+        for _ in range(args.warmup + args.steps):
+            K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam)
     elif args.only == "mla":
         a = W.mla_decode(seed=0, B=args.decode_batch, device=dev)
         lam = args.threshold if args.threshold is not None else MLA_LAMBDAS[2]
@@ -899,7 +904,7 @@ def main():
     ap.add_argument("--no-skip-points", action="store_true", help="leave out the ~70 %% sparsity points")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-units", type=int, default=16)
-    ap.add_argument("--only", choices=["prefill", "decode", "mla"], default=None,
+    ap.add_argument("--only", choices=["prefill", "planted70", "decode", "mla"], default=None,
                     help="launch one kernel only (profiling case); no JSON metric line")
     ap.add_argument("--prefill-len", type=int, default=16384)
     ap.add_argument("--decode-batch", type=int, default=64)
