@@ -692,8 +692,9 @@ __global__ void __launch_bounds__(384, 1)
             // QK_w(j) into S_w.  With hand_over, the turn passes to the other issuer once all
             // but kQkLeft of the k-steps are queued: the other issuer then notices it, and
             // its first MMA starts, while the tensor core still works through those steps
-            // (planted-70 skipping 2.076 -> 2.030 ms, LLM prefill +0.4 %).
-            constexpr int kQkLeft = 2;
+            // (planted-70 skipping 2.076 -> 2.026 ms; LLM prefill unchanged with one step
+            // left, +0.2 % with two, +1 % with three).
+            constexpr int kQkLeft = 1;
             auto issue_qk = [&](int j, bool hand_over = false) {
                 const uint32_t b0 = klo + (uint32_t)(j % C::NK) * kTileLo;
 #pragma unroll
