@@ -39,6 +39,14 @@ __device__ __forceinline__ void mbar_arrive_if(uint64_t* bar, bool pred) {
         "r"((uint32_t)pred)
         : "memory");
 }
+// As mbar_arrive_if, counting `count` arrivals at once.
+__device__ __forceinline__ void mbar_arrive_cnt_if(uint64_t* bar, uint32_t count, bool pred) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t"
+        "@p mbarrier.arrive.release.cta.shared::cta.b64 _, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
+        "r"(count), "r"((uint32_t)pred)
+        : "memory");
+}
 // 32-bit shared-memory store executed only where `pred` holds (predicated, no branch).
 __device__ __forceinline__ void st_shared_if(const void* addr, uint32_t v, bool pred) {
     asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %2, 0;\n\t@p st.shared.u32 [%0], %1;\n\t}" ::"r"(
