@@ -42,12 +42,12 @@ KERNEL_SOURCES = {
     "decode": ["csrc/decode.cu", "csrc/ptx.cuh", "csrc/kernels.cuh", "csrc/api.cu"],
 }
 TRAFFIC = {
-    "prefill": {"bytes": 201398528 + 99127808,
-                "sources_sha256": "4de5b31a2d0e830ff11f66790b2f0a5f62ceb50591027167765fa2b16147680d",
+    "prefill": {"bytes": 201467648 + 99919872,
+                "sources_sha256": "8485fdc510ece7eb64353189692b9481f6663d24dbc923c8587b36696c062480",
                 "capture": "prefill2_kernel<128, false> on the bench's causal L=16384 GQA prefill, one launch, "
                            "dram__bytes_read.sum + dram__bytes_write.sum (ncu --set full)"},
-    "decode": {"bytes": 8 * (1073871872 + 3653120),
-               "sources_sha256": "bab7aa3259ac3223d3bd554609342a713ec414216cff1eb18533fadfc7763773",
+    "decode": {"bytes": 8 * (1073872640 + 3618304),
+               "sources_sha256": "c537d2e014b679f88c183d77d1bc4bfff41695e8314745297f08b610b0ef8eeb",
                "capture": "decode_kernel<4, 0> at B=8 Hq=32 Hkv=8 Lkv=32768 d=128 (7 splits), one launch, "
                           "dram__bytes_read.sum + dram__bytes_write.sum, scaled x8 by sequences to B=64"},
 }
