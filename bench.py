@@ -35,22 +35,35 @@ PREFILL = dict(B=1, Hq=32, Hkv=8, L=16384, d=128)
 DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
 # capture, with the SHA-256 of the kernel's sources when it was taken.  The line
-# reports the figure only while those sources are unchanged (else traffic is null:
-# the counters belong to another version of the kernel).
+# reports the figure only while the code of those sources is unchanged, comments aside
+# (else traffic is null: the counters belong to another version of the kernel).
 KERNEL_SOURCES = {
     "prefill": ["csrc/prefill.cu", "csrc/ptx.cuh", "csrc/kernels.cuh", "csrc/api.cu"],
     "decode": ["csrc/decode.cu", "csrc/ptx.cuh", "csrc/kernels.cuh", "csrc/api.cu"],
 }
 TRAFFIC = {
     "prefill": {"bytes": 201467648 + 99919872,
-                "sources_sha256": "8485fdc510ece7eb64353189692b9481f6663d24dbc923c8587b36696c062480",
+                "sources_sha256": "37af018f9d950099639fb00ec76dbe09e69a8d58b298a4c8507a04310b3db58b",
                 "capture": "prefill2_kernel<128, false> on the bench's causal L=16384 GQA prefill, one launch, "
                            "dram__bytes_read.sum + dram__bytes_write.sum (ncu --set full)"},
     "decode": {"bytes": 8 * (1073872640 + 3618304),
-               "sources_sha256": "c537d2e014b679f88c183d77d1bc4bfff41695e8314745297f08b610b0ef8eeb",
+               "sources_sha256": "2e4e91b4785503b4bf77e3241d2db5b44d84dc2ca6f71fe618aca3120de8572e",
                "capture": "decode_kernel<4, 0> at B=8 Hq=32 Hkv=8 Lkv=32768 d=128 (7 splits), one launch, "
                           "dram__bytes_read.sum + dram__bytes_write.sum, scaled x8 by sequences to B=64"},
 }
+
+
+def _code_only(text):
+    """The source without its // comments, trailing blanks and empty lines: the part
+    that a kernel's DRAM traffic can depend on (the sources hold no /* */ comments and
+    no "//" inside a string)."""
+    out = []
+    for line in text.splitlines():
+        i = line.find("//")
+        line = (line[:i] if i >= 0 else line).rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out) + "\n"
 
 
 def sources_sha256(kernel):
@@ -58,8 +71,8 @@ def sources_sha256(kernel):
 
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "skip_softmax_flashattention_gb300", rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "skip_softmax_flashattention_gb300", rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode("utf-8"))
     return h.hexdigest()
 
 

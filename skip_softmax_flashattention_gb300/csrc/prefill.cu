@@ -1,5 +1,10 @@
 // prefill.cu -- skip-softmax (BLASST) FlashAttention forward for prefill on sm_103a.
 //
+// Two kernels: prefill2_kernel, the default, runs two query tiles per CTA with their
+// softmaxes half a period apart on the tensor core (described where it is defined);
+// prefill_kernel, described here, runs one query tile per CTA and serves the
+// BLASST_PREFILL_ONE_QTILE and BLASST_PREFILL_P_VIA_SMEM variants.
+//
 // One CTA computes one 128-row query tile of one query head against the key tiles
 // it can see, in ascending order (Hitchhiker's Guide Phase 08, Section 1,
 // "FlashAttention Tiling Strategy"), with the BLASST per-tile test between S and
