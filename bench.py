@@ -34,7 +34,7 @@ UNIT = "TFLOP/s"
 PREFILL = dict(B=1, Hq=32, Hkv=8, L=16384, d=128)
 DECODE = dict(B=64, Hq=32, Hkv=8, Lkv=32768, d=128)
 # Per-launch DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu
-# capture, with the SHA-256 of the kernel's sources when it was taken.  The line
+# capture, with the SHA-256 of the kernel's code when it was taken.  The line
 # reports the figure only while the code of those sources is unchanged, comments aside
 # (else traffic is null: the counters belong to another version of the kernel).
 KERNEL_SOURCES = {
