@@ -887,6 +887,7 @@ def run_sweep(args):
           "fit": None if fitted is None else {"a": fitted[0], "b": fitted[1]}})
     for L in (8192, 32768, 65536):
         a = W.llm(seed=2, L=L, device=dev)
+        lams_run = []
         for s_t in (0.5, 0.7):
             if fitted is None:
                 emit({"sweep": f"long-context-L{L}", "target": s_t, "result": "no calibration: the sparsity is 0 "
@@ -900,6 +901,9 @@ def run_sweep(args):
             visited = visited_tiles_causal(L, L) * a.B * a.Hq
             emit({"sweep": f"long-context-L{L}", "target": s_t, "lambda": lam, "lambda_run": lam_run,
                   "unreachable": unreachable, "achieved_skip_pct": 100.0 * int(r["skipped"].item()) / visited})
+            lams_run.append(lam_run)
+        # the kernel's time on the evaluation seed at lambda = 0 and at the thresholds run
+        prefill_case(f"long-context-L{L}-timed", a, [0.0] + sorted(set(lams_run)))
         del a
         torch.cuda.empty_cache()
     return 0
