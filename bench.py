@@ -674,7 +674,8 @@ def run_only(args):
         for _ in range(args.warmup + args.steps):
             K.prefill(a.q, a.k, a.v, a.causal, a.scale, lam)
     elif args.only == "mla":
-        a = W.mla_decode(seed=0, B=args.decode_batch, device=dev)
+        kw = dict(q_shared=6.0, sink_norm=32.0) if args.mla_heads > 16 else {}
+        a = W.mla_decode(seed=0, B=args.decode_batch, Hq=args.mla_heads, device=dev, **kw)
         lam = args.threshold if args.threshold is not None else MLA_LAMBDAS[2]
         for _ in range(args.warmup + args.steps):
             K.mla_decode(a.q, a.extra["kv"], a.scale, lam, args.splits)
@@ -926,6 +927,7 @@ def main():
     ap.add_argument("--prefill-len", type=int, default=16384)
     ap.add_argument("--decode-batch", type=int, default=64)
     ap.add_argument("--splits", type=int, default=0)
+    ap.add_argument("--mla-heads", type=int, default=16, help="query heads of the MLA profiling case")
     ap.add_argument("--sweep", action="store_true", help="every workload at its thresholds (JSON lines)")
     args = ap.parse_args()
     if args.warmup < 3:
