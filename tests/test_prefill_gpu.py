@@ -122,6 +122,31 @@ def test_llm_prefill_long_context_sampled(L):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("L,B,Hq,Hkv", [(16384, 3, 4, 1), (8192, 3, 8, 2)], ids=["L16384-B3-H4", "L8192-B3-H8"])
+def test_causal_prefill_bands_with_a_partial_last_band(L, B, Hq, Hkv):
+    """Causal CTAs run in bands of (sequence, head) pairs whose K/V fit an eighth of L2,
+    longest-first within each band (two KV-head groups per band at L = 16384 and d = 128,
+    four at 8192 on this part).  With an odd number of KV heads in all, the last band is
+    partial.  The first, middle and last query tiles of every (sequence, head) pair are
+    checked against the oracle, at lambda = 0 and at lambda = 1."""
+    a = parity.to_gpu(W.llm(seed=5, L=L, B=B, Hq=Hq, Hkv=Hkv, device="cuda"))
+    nQ = L // 128
+    units = [(b, h, qt) for b in range(B) for h in range(Hq) for qt in (0, nQ // 2, nQ - 1)]
+    for lam in (0.0, 1.0):
+        res = K.prefill(a.q, a.k, a.v, True, a.scale, lam, want_map=True)
+        torch.cuda.synchronize()
+        n = int(res["skipped"].item())
+        assert n == int((res["map"] == 1).sum().item())
+        # every visited tile has a decision in the map (0 or 1), none is left unvisited
+        visited = int((res["map"] != 2).sum().item())
+        assert visited == B * Hq * (nQ * (nQ + 1) // 2)
+        if lam == 0.0:
+            assert n == 0
+        parity.prefill_units_check(a, res, lam, units)
+    del a, res
+    torch.cuda.empty_cache()
+
+
 def test_dit_full_size():
     a = parity.to_gpu(W.dit(seed=0, device="cuda"))
     rng = np.random.default_rng(1)
