@@ -168,6 +168,7 @@ def decode_paged_check(a, res, lam, S, seqs=None, log=None, window=0):
     lse_gpu = res["lse"].cpu().numpy()
     B = len(lens)
     assert int(res["skipped"].item()) == int((gmap == 1).sum())
+    band_total, oracle_skipped = 0, 0
     for b in (range(B) if seqs is None else seqs):
         L = lens[b]
         nt = -(-L // 128)
@@ -187,11 +188,14 @@ def decode_paged_check(a, res, lam, S, seqs=None, log=None, window=0):
         Sb = min(S, nt - lo)
         own = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=Sb, precision="f32", window=window)
         band = _decisions(gmap[b:b + 1, :, :nt], own["map"], own["margin"], lam, what)
+        band_total += band
+        oracle_skipped += int(own["skipped"])
         ref = orc.decode_tiled(q, k, v, a.scale, lam, num_splits=Sb, forced=gmap[b:b + 1, :, :nt], precision="f32",
                                window=window)
         _check_rows(o_gpu[b:b + 1], lse_gpu[b:b + 1], ref["o"], ref["lse"], what)
         if log is not None and band:
             log.append(f"{what}: {band} tiles inside the 1e-3 margin band")
+    return band_total, oracle_skipped
 
 
 def mla_check(a, res, lam, S, seqs=None, log=None):

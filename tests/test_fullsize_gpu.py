@@ -12,7 +12,8 @@ GPU threshold is then checked on every visited tile:
 
 Workloads: causal GQA LLM prefill at 16384 (whole), split-KV decode of 64 x 32768
 (whole), video DiT (two whole heads: every query tile of each), the long-context
-prefill at 8192 on the evaluation seed (whole), planted-70 (two whole heads).  These are slow (minutes of CPU
+prefill at 8192 on the evaluation seed (whole), planted-70 (two whole heads), paged
+decode of a 64-sequence serving batch (whole).  These are slow (minutes of CPU
 oracle time in total)."""
 from __future__ import annotations
 
@@ -156,3 +157,29 @@ def test_planted70_two_whole_heads_exact_counts():
     n, band = counts[1e-2]
     assert band == 0
     assert n == 2 * 128 * 90  # key tiles 38..127 of every query tile of the two heads
+
+
+def test_paged_decode_whole_serving_batch_exact_counts():
+    """Paged decode of a serving batch: 64 sequences of 16k-32k keys in 16-key pages
+    (key-major pool), the library's split plan, at lambda = 0 and 0.3.  Every sequence
+    against the oracle run on it alone (decisions outside the 1e-3 band, O, lse), and
+    the batch's skipped count equal to the oracle's up to the decisions that differ
+    inside the band (exactly, when none do)."""
+    a = W.paged_decode(seed=8, B=64, Hq=32, Hkv=8, max_len=32768, page_size=16, min_len=16384, device="cuda")
+    e = a.extra
+    for lam in (0.0, 0.3):
+        res = K.decode_paged(a.q, e["k_pages"], e["v_pages"], e["page_table"], e["seq_lens"], e["max_len"],
+                             e["page_size"], e["token_major"], a.scale, lam, 0, want_map=True)
+        torch.cuda.synchronize()
+        n = int(res["skipped"].item())
+        differ, n_oracle = parity.decode_paged_check(a, res, lam, res["num_splits"])
+        assert abs(n - n_oracle) <= differ
+        if differ == 0:
+            assert n == n_oracle
+        if lam == 0.0:
+            assert n == 0
+        else:
+            assert n > 0
+        del res
+    del a
+    torch.cuda.empty_cache()
