@@ -198,11 +198,13 @@ def decode_paged_check(a, res, lam, S, seqs=None, log=None, window=0):
     return band_total, oracle_skipped
 
 
-def mla_check(a, res, lam, S, seqs=None, log=None):
+def mla_check(a, res, lam, S, seqs=None, log=None, counts=False):
     """An MLA decode (workloads.mla_decode) against the oracle run on each checked
     sequence with its own key count, the call's lambda and split count: every tile
     decision (outside the 1e-3 margin band), then O and lse with the GPU's decisions
-    forced.  Tiles past a sequence's end must stay "not visited"."""
+    forced.  Tiles past a sequence's end must stay "not visited".  Returns the number
+    of decisions that differ inside the band (and, with counts, the oracle's skipped
+    count over the checked sequences)."""
     kv = a.extra["kv"]
     dv = a.extra["dv"]
     Lmax = kv.shape[1]
@@ -212,7 +214,7 @@ def mla_check(a, res, lam, S, seqs=None, log=None):
     o_gpu = res["o"].float().cpu().numpy()
     lse_gpu = res["lse"].cpu().numpy()
     assert int(res["skipped"].item()) == int((gmap == 1).sum())
-    band_total = 0
+    band_total, oracle_skipped = 0, 0
     for b in (range(a.B) if seqs is None else seqs):
         L = min(max(lens[b], 0), Lmax)
         nt = -(-L // 128)
@@ -229,9 +231,10 @@ def mla_check(a, res, lam, S, seqs=None, log=None):
                                    precision="f32")
         _check_rows(o_gpu[b:b + 1], lse_gpu[b:b + 1], ref["o"], ref["lse"], what)
         band_total += band
+        oracle_skipped += int(own["skipped"])
         if log is not None and band:
             log.append(f"{what}: {band} tiles inside the 1e-3 margin band")
-    return band_total
+    return (band_total, oracle_skipped) if counts else band_total
 
 
 def oracle_map_at(margin, lam):

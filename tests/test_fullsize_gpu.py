@@ -13,7 +13,7 @@ GPU threshold is then checked on every visited tile:
 Workloads: causal GQA LLM prefill at 16384 (whole), split-KV decode of 64 x 32768
 (whole), video DiT (two whole heads: every query tile of each), the long-context
 prefill at 8192 on the evaluation seed (whole), planted-70 (two whole heads), paged
-decode of a 64-sequence serving batch (whole).  These are slow (minutes of CPU
+decode of a 64-sequence serving batch (whole), MLA decode with 16 heads (whole).  These are slow (minutes of CPU
 oracle time in total)."""
 from __future__ import annotations
 
@@ -180,6 +180,26 @@ def test_paged_decode_whole_serving_batch_exact_counts():
             assert n == 0
         else:
             assert n > 0
+        del res
+    del a
+    torch.cuda.empty_cache()
+
+
+def test_mla_decode_whole_problem_exact_counts():
+    """MLA decode, 64 sequences x 32768 latent rows, 16 query heads, the planner's
+    splits, at lambda = 0 and 0.03: every sequence against the oracle (decisions
+    outside the 1e-3 band, O, lse), and the skipped count equal to the oracle's up to
+    the decisions that differ inside the band (exactly, when none do)."""
+    a = W.mla_decode(seed=0, B=64, Hq=16, L=32768, device="cuda")
+    for lam in (0.0, 0.03):
+        res = K.mla_decode(a.q, a.extra["kv"], a.scale, lam, 0, want_map=True)
+        torch.cuda.synchronize()
+        n = int(res["skipped"].item())
+        differ, n_oracle = parity.mla_check(a, res, lam, res["num_splits"], counts=True)
+        assert abs(n - n_oracle) <= differ
+        if differ == 0:
+            assert n == n_oracle
+        assert (n == 0) if lam == 0.0 else (n > 0)
         del res
     del a
     torch.cuda.empty_cache()
